@@ -1,0 +1,540 @@
+"""Benchmark of the quantized-linear hot path on GB300.
+
+Headline workload (the configuration the metric is quoted on): the W4A16
+decode GEMM at the Llama-3.1-8B MLP shape, K = 4096, N = 14336, activations
+bf16 M in {1, 4, 16} ~ N(0,1) with 1% channels x20, weights N(0, 0.02)
+quantized to symmetric INT4 with one bf16 scale per 128 along K.
+
+One step = one decode pass over 8 distinct weight copies (think 8 layers) at
+each of M = 1, 4 and 16: 24 GEMM launches, 8 x 30.3 MB = 242 MB of weights,
+more than L2 (so every step streams its weights from HBM; no flush needed).
+
+value  = algorithmic bytes of the step (packed weights + scales + A + Y) / time,
+         GB/s, inputs resident in HBM, CUDA events on the launching stream.
+e2e    = the same metric through the public API with host buffers: each GEMM's
+         activations copied from pinned host memory and its output copied back,
+         inside the timed region.
+Secondary measurements of the other rows (quantizers, KV write, FP8/NVFP4/MXFP4
+GEMMs, the Qwen3-0.6B decode step) are reported beside the headline under
+"rows", each timed on its own with CUDA events.
+
+`--impl reference` times the CPU oracle (single-threaded C, test
+infrastructure) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 decode GEMM HBM GB/s; FP8/NVFP4 GEMM TFLOPS; % of GB300 roofline"
+K_DIM, N_DIM = 4096, 14336
+MS = (1, 4, 16)
+COPIES = 8
+WORKLOAD = "W4A16 decode GEMM, Llama-3.1-8B MLP 4096x14336, INT4 g128 bf16 scales, M in {1,4,16}"
+
+
+# ------------------------------------------------------------------ shared
+
+def step_bytes(M: int, K: int = K_DIM, N: int = N_DIM) -> int:
+    """Algorithmic bytes of one W4A16 GEMM: packed INT4 weights, bf16 scales, A, Y."""
+    return K * N // 2 + (K // 128) * N * 2 + M * K * 2 + M * N * 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (its file hash is recorded beside the number)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path, encoding="utf-8"):
+        f = line.split("#", 1)[0].split()
+        if len(f) == 5 and f[0] == kernel and f[1] == workload:
+            src = os.path.join(ROOT, "bit_quantized_linear_quantizers_gb300", "csrc", f[3])
+            if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == f[4]:
+                return float(f[2])
+    return None
+
+
+def dist_setup(n_gpus: int):
+    """(rank, world, local_rank). One process per GPU under torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("QZ_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU arm
+
+class Timer:
+    """Kernel time per call: `reps` calls captured in one CUDA graph on the launching
+    stream, replayed after warm-up, timed with CUDA events on that stream."""
+
+    def __init__(self, stream):
+        import torch
+        self.torch = torch
+        self.stream = stream
+
+    def __call__(self, fn, reps: int, warm: int = 3) -> float:
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            fn()                                       # first call outside capture (sets attributes)
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for _ in range(reps):
+                fn()
+        with torch.cuda.stream(self.stream):
+            for _ in range(warm):
+                g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            s.record(self.stream)
+            g.replay()
+            e.record(self.stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) * 1e3 / reps          # us per call
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import bit_quantized_linear_quantizers_gb300 as qz
+    import synthetic as syn
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    pk = peaks()
+
+    # ---- inputs (seeded, generated once on the host, resident in HBM)
+    _, w = syn.w4a16_decode_inputs(M=1, seed=0)
+    with torch.cuda.stream(stream):
+        qw, sc, _ = qz.qz_quantize_int4_g128(torch.from_numpy(w).to(dev))
+    stream.synchronize()
+    del w
+    weights = [(qw.clone(), sc.clone()) for _ in range(COPIES)]
+    del qw, sc
+    acts, outs, host_a, host_y = {}, {}, {}, {}
+    for M in MS:
+        a_bits, _ = syn.w4a16_decode_inputs(M=M, seed=0, N=128)      # same A recipe; tiny W discarded
+        a_t = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16)
+        acts[M] = a_t.to(dev)
+        outs[M] = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)
+        host_a[M] = a_t.pin_memory()
+        host_y[M] = torch.empty((M, N_DIM), dtype=torch.bfloat16).pin_memory()
+
+    def step():
+        for i in range(COPIES):
+            q, s = weights[i]
+            for M in MS:
+                qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
+
+    def step_e2e():
+        for i in range(COPIES):
+            q, s = weights[i]
+            for M in MS:
+                acts[M].copy_(host_a[M], non_blocking=True)
+                qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
+                host_y[M].copy_(outs[M], non_blocking=True)
+
+    bytes_per_step = COPIES * sum(step_bytes(M) for M in MS)
+    launches_per_step = COPIES * len(MS)
+
+    # ---- the step as one CUDA graph (24 launches, no host overhead between them)
+    with torch.cuda.stream(stream):
+        step()                                         # first calls outside capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+
+    # ---- warm-up, then exactly K timed steps between barriers + synchronize
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = reduce_max(t_ms, world, dev)
+    ms_per_step = t_ms / args.steps
+    value = world * bytes_per_step * args.steps / (t_ms * 1e-3) / 1e9
+
+    # ---- e2e through the public API with pinned host buffers
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    e_steps = max(3, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            step_e2e()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    te_ms = reduce_max(e0.elapsed_time(e1), world, dev)
+    e2e_value = world * bytes_per_step * e_steps / (te_ms * 1e-3) / 1e9
+    h2d = COPIES * sum(M * K_DIM * 2 for M in MS)
+    d2h = COPIES * sum(M * N_DIM * 2 for M in MS)
+
+    # ---- roofline of the dominant kernel (w4a16_kernel): per-M launch timing
+    timer = Timer(stream)
+    per_m = {}
+    it = [0]
+    for M in MS:
+        def one(M=M):
+            q, s = weights[it[0] % COPIES]
+            it[0] += 1
+            qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
+        us = timer(one, reps=200, warm=10)
+        per_m[M] = {"us": round(us, 3), "gbps": round(step_bytes(M) / us / 1e3, 1),
+                    "frac_of_hbm": round(step_bytes(M) / us / 1e3 / pk["hbm_gbs"], 4)}
+    avg_launch_us = t_ms * 1e3 / (args.steps * launches_per_step)
+    achieved = bytes_per_step / launches_per_step / avg_launch_us / 1e3
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": kernel_traffic("w4a16_kernel", "llama_mlp_M16"),
+                "kernel": "w4a16_kernel", "peak_source": pk["source"],
+                "algorithmic_bytes_per_launch": bytes_per_step // launches_per_step,
+                "avg_launch_us": round(avg_launch_us, 3), "per_M": per_m}
+
+    rows = {}
+    if not args.no_rows:
+        rows = secondary_rows(qz, syn, stream, dev, pk)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4xbf16->f32acc", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": list(MS), "K": K_DIM, "N": N_DIM, "weight_copies": COPIES,
+                   "l2": "inputs larger than L2 (8 rotating weight copies, 242 MB)",
+                   "parallelism": f"replicas{world}"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "rows": rows,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def secondary_rows(qz, syn, stream, dev, pk):
+    """The other hot-path rows, each timed on its own (CUDA events, inputs resident)."""
+    import numpy as np
+    import torch
+
+    timer = Timer(stream)
+    rows = {}
+    ws = qz.Workspace(dev)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    fp8_peak = 2.0 * pk["bf16_tflops"]          # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
+    fp4_peak = 6.0 * pk["bf16_tflops"]          # FP4 dense = 6 x bf16 (nominal 13.5 / 2.25 PF)
+
+    # config 3: FP8 1x128 activations, 128x128 weights, block-scaled GEMM
+    a, bt = syn.fp8_block_gemm_inputs(seed=0)
+    a_d, bt_d = bf(a), bf(bt)
+    del a, bt
+    with torch.cuda.stream(stream):
+        qa, sa, _ = qz.qz_quantize_fp8(a_d, qz.FP8_GROUP_1x128, stream=stream)
+        qb, sb, _ = qz.qz_quantize_fp8(bt_d, qz.FP8_BLOCK_128x128, stream=stream)
+    M3, K3 = a_d.shape
+    N3 = bt_d.shape[0]
+    q = {}
+    us = timer(lambda: qz.qz_quantize_fp8(a_d, qz.FP8_GROUP_1x128, codes=qa, scales=sa, stream=stream), 20)
+    by = M3 * K3 * 2 + M3 * K3 + M3 * (K3 // 128) * 4
+    q["fp8_1x128_A_2048x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                       "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    us = timer(lambda: qz.qz_quantize_fp8(bt_d, qz.FP8_BLOCK_128x128, codes=qb, scales=sb, stream=stream), 10)
+    by = N3 * K3 * 2 + N3 * K3 + (N3 // 128) * (K3 // 128) * 4
+    q["fp8_128x128_Bt_14336x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                           "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    try:
+        y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+        us = timer(lambda: qz.qz_gemm_fp8_block(qa, sa, qb, sb, Y=y3, ws=ws, stream=stream), 20)
+        fl = 2.0 * M3 * N3 * K3
+        rows["fp8_block_gemm_2048x14336x4096"] = {"us": round(us, 2), "tflops": round(fl / us / 1e6, 1),
+                                                  "peak_tflops": fp8_peak,
+                                                  "frac": round(fl / us / 1e6 / fp8_peak, 4)}
+    except qz.QZError as e:
+        rows["fp8_block_gemm_2048x14336x4096"] = {"unavailable": str(e)}
+    del a_d, bt_d, qb
+
+    # config 4: NVFP4 / MXFP4 quantize + GEMM
+    a, bt = syn.fp4_gemm_inputs(seed=0)
+    a_d, bt_d = bf(a), bf(bt)
+    del a, bt
+    M4, K4 = a_d.shape
+    N4 = bt_d.shape[0]
+    with torch.cuda.stream(stream):
+        na = qz.qz_quantize_nvfp4(a_d, ws=ws, stream=stream)
+        nb = qz.qz_quantize_nvfp4(bt_d, ws=ws, stream=stream)
+        ma = qz.qz_quantize_mxfp4(a_d, stream=stream)
+        mb = qz.qz_quantize_mxfp4(bt_d, stream=stream)
+    us = timer(lambda: qz.qz_quantize_nvfp4(a_d, codes=na[0], scale_e4m3=na[1], global_scale=na[2], ws=ws,
+                                            stream=stream), 20)
+    by = M4 * K4 * 2 + M4 * K4 // 2 + M4 * K4 // 16 + 4
+    q["nvfp4_A_8192x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                   "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    us = timer(lambda: qz.qz_quantize_mxfp4(a_d, codes=ma[0], scale_e8m0=ma[1], stream=stream), 20)
+    by = M4 * K4 * 2 + M4 * K4 // 2 + M4 * K4 // 32
+    q["mxfp4_A_8192x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                   "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    fl = 2.0 * M4 * N4 * K4
+    y4 = torch.empty((M4, N4), dtype=torch.bfloat16, device=dev)
+    for name, fn in (("nvfp4_gemm_8192x4096x4096",
+                      lambda: qz.qz_gemm_nvfp4(na[0], na[1], na[2], nb[0], nb[1], nb[2], Y=y4, ws=ws,
+                                               stream=stream)),
+                     ("mxfp4_gemm_8192x4096x4096",
+                      lambda: qz.qz_gemm_mxfp4(ma[0], ma[1], mb[0], mb[1], Y=y4, ws=ws, stream=stream))):
+        try:
+            us = timer(fn, 20)
+            rows[name] = {"us": round(us, 2), "tflops": round(fl / us / 1e6, 1), "peak_tflops": fp4_peak,
+                          "frac": round(fl / us / 1e6 / fp4_peak, 4)}
+        except qz.QZError as e:
+            rows[name] = {"unavailable": str(e)}
+    del a_d, bt_d
+
+    # config 1: the six quantizer paths on the 1024 x 1024 fp32 weight (launch-bound: us)
+    x = torch.from_numpy(syn.quant_roundtrip_input(seed=0)).to(dev)
+    c1 = {}
+    for nm, g in (("fp8_per_tensor", 0), ("fp8_per_row", 1), ("fp8_128x128", 2), ("fp8_1x128", 3)):
+        c1[nm] = round(timer(lambda g=g: qz.qz_quantize_fp8(x, g, dequant=True, ws=ws, stream=stream), 50), 2)
+    c1["mxfp4"] = round(timer(lambda: qz.qz_quantize_mxfp4(x, dequant=True, stream=stream), 50), 2)
+    c1["nvfp4"] = round(timer(lambda: qz.qz_quantize_nvfp4(x, dequant=True, ws=ws, stream=stream), 50), 2)
+    c1["int4_g128"] = round(timer(lambda: qz.qz_quantize_int4_g128(x, dequant=True, stream=stream), 50), 2)
+    rows["quantize_roundtrip_1024x1024_f32_us"] = c1
+
+    # config 5: FP8 KV write of K, V bf16 [1, 8, 4096, 128]
+    k, v = syn.kv_cache_inputs(seed=0)
+    k_d, v_d = bf(k), bf(v)
+    kv = qz.qz_kv_write_fp8(k_d, v_d, ws=ws, stream=stream)
+    us = timer(lambda: qz.qz_kv_write_fp8(k_d, v_d, k_codes=kv[0], v_codes=kv[1], k_scale=kv[2],
+                                          v_scale=kv[3], ws=ws, stream=stream), 50)
+    by = 2 * (k.size * 2 + k.size) + 8
+    q["kv_write_fp8_2x8x4096x128_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                           "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    rows["quantizers"] = q
+    rows["qwen3_decode_step"] = qwen3_step(qz, syn, stream, dev, pk, timer, ws)
+    return rows
+
+
+def qwen3_step(qz, syn, stream, dev, pk, timer, ws):
+    """Config 5: one decode step of a random-init Qwen3-0.6B-shaped decoder at 64
+    tokens, all 196 linears in W4A16 as one grouped launch, plus the FP8 KV write."""
+    import numpy as np
+    import torch
+    probs = []
+    wbytes = 0
+    for layer, name, A, w in syn.qwen3_decode_linears(layers=28, tokens=64, seed=0):
+        K, N = w.shape
+        with torch.cuda.stream(stream):
+            qw, sc, _ = qz.qz_quantize_int4_g128(torch.from_numpy(w).to(dev), stream=stream)
+        a_d = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).to(dev)
+        Y = torch.empty((64, N), dtype=torch.bfloat16, device=dev)
+        probs.append((a_d, qw, sc, Y))
+        wbytes += K * N // 2 + (K // 128) * N * 2 + 64 * K * 2 + 64 * N * 2
+    stream.synchronize()
+    us = timer(lambda: qz.qz_gemm_w4a16_grouped(probs, stream=stream), 20)
+    out = {"w4a16_grouped_196_linears_us": round(us, 2), "w4a16_gbps": round(wbytes / us / 1e3, 1),
+           "w4a16_frac_of_hbm": round(wbytes / us / 1e3 / pk["hbm_gbs"], 3)}
+    return out
+
+
+# ---------------------------------------------------------- CPU baseline
+
+_CPU_CACHE = {}
+
+
+def _cpu_inputs():
+    """The oracle's own INT4 quantization of the workload weight (setup, untimed)."""
+    if not _CPU_CACHE:
+        import oracle
+        import synthetic as syn
+        _, w = syn.w4a16_decode_inputs(M=1, seed=0)
+        qw, sc, _ = oracle.quant_int4_g128(w, want_deq=False)
+        acts = {M: syn.w4a16_decode_inputs(M=M, seed=0, N=128)[0] for M in MS}
+        _CPU_CACHE.update(qw=qw, sc=sc, acts=acts)
+    return _CPU_CACHE
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle's W4A16 reference (single-threaded C, FP64 accumulation) timed on
+    this host on a bounded sample: chunks of 64 output columns at every M in
+    {1, 4, 16}, until the time budget is spent. Bytes are counted as for the GPU
+    (the sampled columns' share of each GEMM's algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    c = _cpu_inputs()
+    done_bytes, spent, n_cols = 0.0, 0.0, 0
+    while spent < budget_s and n_cols < N_DIM:
+        cols = np.arange(n_cols, n_cols + 64)
+        for M in MS:
+            ii = np.repeat(np.arange(M), cols.size)
+            jj = np.tile(cols, M)
+            t0 = time.perf_counter()
+            oracle.gemm_w4a16(c["acts"][M], c["qw"], c["sc"], ii, jj)
+            spent += time.perf_counter() - t0
+            done_bytes += step_bytes(M) * cols.size / N_DIM
+        n_cols += cols.size
+    return {"value": round(done_bytes / spent / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_cols} of {N_DIM} output columns at each M in {list(MS)} (K={K_DIM}); "
+                      f"{spent:.1f} s of single-threaded oracle time"}
+
+
+def reference_arm(args, rank, world):
+    """--impl reference: the CPU oracle as it stands, timed on this host's cores, on a
+    bounded sample of the same workload each step. Rank 0 alone runs it."""
+    if rank != 0:
+        return
+    per_step_budget = max(0.5, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(budget_s=per_step_budget / 4)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(budget_s=per_step_budget))
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(v["value"] for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed * 1e3 / args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": list(MS), "K": K_DIM, "N": N_DIM,
+                       "parallelism": "cpu single thread"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": vals[-1]["sample"]},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["qz", "reference"], default="qz")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary per-row measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_setup(args.gpus)
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_arm(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,310 @@
+"""Python binding of libqz, the GB300 (sm_103a) quantizers and quantized GEMMs.
+
+Argument marshalling only: every step of the computation runs in libqz's CUDA
+kernels, behind the C ABI declared in include/qz.h. The functions carry the C
+names. PyTorch supplies device memory (output tensors) and the current CUDA
+stream. There is no CPU path: importing this package fails when libqz.so has
+not been built, and every call raises QZError unless libqz returns QZ_OK.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB, build  # noqa: F401  (build() is the in-tree build step)
+
+__all__ = [
+    "QZError", "lib", "F32", "BF16", "FP8_PER_TENSOR", "FP8_PER_ROW", "FP8_BLOCK_128x128",
+    "FP8_GROUP_1x128", "SCALE_COMPUTE", "SCALE_GIVEN", "qz_workspace_size", "qz_status_string",
+    "qz_device_error", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
+    "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
+    "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_mxfp4", "Workspace",
+]
+
+F32, BF16 = 0, 1
+FP8_PER_TENSOR, FP8_PER_ROW, FP8_BLOCK_128x128, FP8_GROUP_1x128 = 0, 1, 2, 3
+SCALE_COMPUTE, SCALE_GIVEN = 0, 1
+OP_QUANTIZE_FP8, OP_QUANTIZE_NVFP4, OP_KV_WRITE_FP8 = 0, 1, 2
+OP_GEMM_W4A16, OP_GEMM_FP8_BLOCK, OP_GEMM_NVFP4, OP_GEMM_MXFP4 = 3, 4, 5, 6
+
+if not os.path.exists(LIB):
+    raise ImportError(f"libqz.so is not built ({LIB}); run bit_quantized_linear_quantizers_gb300.build() "
+                      "or __graft_entry__.build() first")
+
+lib = ctypes.CDLL(LIB)
+
+_P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+
+
+class _W4A16Problem(ctypes.Structure):
+    _fields_ = [("A", _P), ("qweight", _P), ("scale_bf16", _P), ("Y", _P),
+                ("M", _I), ("N", _I), ("K", _I)]
+
+
+_SIGS = {
+    "qz_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
+    "qz_status_string": (ctypes.c_char_p, [_I]),
+    "qz_device_error": (_I, []),
+    "qz_quantize_fp8": (_I, [_P, _I, _I64, _I64, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
+    "qz_quantize_mxfp4": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "qz_quantize_nvfp4": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qz_quantize_int4_g128": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "qz_kv_write_fp8": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "qz_gemm_w4a16": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "qz_gemm_w4a16_grouped": (_I, [ctypes.POINTER(_W4A16Problem), _I, _P, _SZ, _P]),
+    "qz_gemm_fp8_block": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "qz_gemm_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "qz_gemm_mxfp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class QZError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.qz_status_string(status).decode()}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise QZError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(x: torch.Tensor) -> int:
+    if x.dtype == torch.float32:
+        return F32
+    if x.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"libqz quantizers take float32 or bfloat16 input, got {x.dtype}")
+
+
+def _rows_cols_ld(x: torch.Tensor):
+    if x.dim() != 2 or (x.numel() and x.stride(1) != 1):
+        raise ValueError("expected a 2-D tensor with unit stride in the last dimension")
+    return x.shape[0], x.shape[1], (x.stride(0) if x.shape[0] > 1 else max(x.shape[1], 1))
+
+
+def qz_workspace_size(op: int, d0: int, d1: int = 0, d2: int = 0) -> int:
+    return int(lib.qz_workspace_size(op, d0, d1, d2))
+
+
+def qz_status_string(status: int) -> str:
+    return lib.qz_status_string(status).decode()
+
+
+def qz_device_error() -> int:
+    return int(lib.qz_device_error())
+
+
+class Workspace:
+    """A reusable device scratch buffer (torch-allocated) grown on demand."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+
+def _ws(ws, nbytes, device):
+    if nbytes == 0:
+        return None, 0
+    if ws is None:
+        ws = Workspace(device)
+    buf = ws.get(nbytes) if isinstance(ws, Workspace) else ws
+    return buf, buf.numel()
+
+
+# ------------------------------------------------------------- quantizers
+
+def qz_quantize_fp8(x: torch.Tensor, gran: int, codes=None, scales=None, dequant=False, ws=None,
+                    stream=None):
+    """FP8 E4M3 quantization of a 2-D fp32/bf16 tensor. Returns (codes u8, scales f32,
+    dequant f32 or None). `dequant` may be True (allocate) or an output tensor."""
+    rows, cols, ld = _rows_cols_ld(x)
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    if scales is None:
+        br = min(128, rows) if rows else 1
+        shape = {FP8_PER_TENSOR: (1,), FP8_PER_ROW: (rows,),
+                 FP8_BLOCK_128x128: (rows // br, cols // 128), FP8_GROUP_1x128: (rows, cols // 128)}[gran]
+        scales = torch.empty(shape, dtype=torch.float32, device=dev)
+    if dequant is True:
+        dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    deq = dequant if isinstance(dequant, torch.Tensor) else None
+    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_FP8, rows, cols, gran), dev)
+    _check(lib.qz_quantize_fp8(_ptr(x), _dtype_code(x), rows, cols, ld, gran, _ptr(codes), _ptr(scales),
+                               _ptr(deq), _ptr(buf), nb, _stream(stream)), "qz_quantize_fp8")
+    return codes, scales, deq
+
+
+def qz_quantize_mxfp4(x: torch.Tensor, codes=None, scale_e8m0=None, dequant=False, stream=None):
+    """MXFP4 quantization. Returns (codes u8 [R, C/2], e8m0 u8 [R, C/32], dequant|None)."""
+    rows, cols, ld = _rows_cols_ld(x)
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if scale_e8m0 is None:
+        scale_e8m0 = torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev)
+    if dequant is True:
+        dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    deq = dequant if isinstance(dequant, torch.Tensor) else None
+    _check(lib.qz_quantize_mxfp4(_ptr(x), _dtype_code(x), rows, cols, ld, _ptr(codes), _ptr(scale_e8m0),
+                                 _ptr(deq), _stream(stream)), "qz_quantize_mxfp4")
+    return codes, scale_e8m0, deq
+
+
+def qz_quantize_nvfp4(x: torch.Tensor, codes=None, scale_e4m3=None, global_scale=None,
+                      global_amax_in=None, dequant=False, ws=None, stream=None):
+    """NVFP4 quantization. Returns (codes u8 [R, C/2], block scales u8 (E4M3) [R, C/16],
+    global scale f32 [1], dequant|None)."""
+    rows, cols, ld = _rows_cols_ld(x)
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if scale_e4m3 is None:
+        scale_e4m3 = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+    if global_scale is None:
+        global_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    if dequant is True:
+        dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    deq = dequant if isinstance(dequant, torch.Tensor) else None
+    if global_amax_in is None:
+        buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4, rows, cols), dev)
+    else:
+        buf, nb = None, 0
+    _check(lib.qz_quantize_nvfp4(_ptr(x), _dtype_code(x), rows, cols, ld, _ptr(codes), _ptr(scale_e4m3),
+                                 _ptr(global_scale), _ptr(global_amax_in), _ptr(deq), _ptr(buf), nb,
+                                 _stream(stream)), "qz_quantize_nvfp4")
+    return codes, scale_e4m3, global_scale, deq
+
+
+def qz_quantize_int4_g128(w: torch.Tensor, qweight=None, scale_bf16=None, dequant=False, stream=None):
+    """INT4 g128 of a [K, N] weight. Returns (qweight i32 [K/8, N], scale bf16 [K/128, N],
+    dequant|None)."""
+    K, N, ld = _rows_cols_ld(w)
+    dev = w.device
+    if qweight is None:
+        qweight = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
+    if scale_bf16 is None:
+        scale_bf16 = torch.empty((K // 128, N), dtype=torch.bfloat16, device=dev)
+    if dequant is True:
+        dequant = torch.empty((K, N), dtype=torch.float32, device=dev)
+    deq = dequant if isinstance(dequant, torch.Tensor) else None
+    _check(lib.qz_quantize_int4_g128(_ptr(w), _dtype_code(w), K, N, ld, _ptr(qweight), _ptr(scale_bf16),
+                                     _ptr(deq), _stream(stream)), "qz_quantize_int4_g128")
+    return qweight, scale_bf16, deq
+
+
+def qz_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, k_codes=None, v_codes=None, k_scale=None,
+                    v_scale=None, mode: int = SCALE_COMPUTE, ws=None, stream=None):
+    """FP8 per-tensor KV write of bf16 [B, H, T, D] tensors. Returns (k_codes, v_codes,
+    k_scale, v_scale); in SCALE_GIVEN mode k_scale/v_scale are inputs."""
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16 or k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must be bf16 tensors of the same [B, H, T, D] shape")
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous")
+    B, H, T, D = k.shape
+    dev = k.device
+    if k_codes is None:
+        k_codes = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    if v_codes is None:
+        v_codes = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    if k_scale is None:
+        k_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    if v_scale is None:
+        v_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+    n = B * H * T * D
+    buf, nb = _ws(ws, qz_workspace_size(OP_KV_WRITE_FP8, n) if mode == SCALE_COMPUTE else 0, dev)
+    _check(lib.qz_kv_write_fp8(_ptr(k), _ptr(v), B, H, T, D, _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                               _ptr(v_scale), mode, _ptr(buf), nb, _stream(stream)), "qz_kv_write_fp8")
+    return k_codes, v_codes, k_scale, v_scale
+
+
+# ------------------------------------------------------------------ GEMMs
+
+def qz_gemm_w4a16(A: torch.Tensor, qweight: torch.Tensor, scale_bf16: torch.Tensor, Y=None, ws=None,
+                  stream=None):
+    """Y[M, N] (bf16) = A[M, K] (bf16) @ dequant(INT4 g128 weight)."""
+    M, K = A.shape
+    N = qweight.shape[1]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, M, N, K), A.device)
+    _check(lib.qz_gemm_w4a16(_ptr(A), _ptr(qweight), _ptr(scale_bf16), _ptr(Y), M, N, K, _ptr(buf), nb,
+                             _stream(stream)), "qz_gemm_w4a16")
+    return Y
+
+
+def qz_gemm_w4a16_grouped(problems, ws=None, stream=None):
+    """Run independent W4A16 problems [(A, qweight, scale_bf16, Y), ...] in one launch."""
+    arr = (_W4A16Problem * len(problems))()
+    mmax = kmax = nsum = 0
+    dev = None
+    for i, (A, qw, sc, Y) in enumerate(problems):
+        M, K = A.shape
+        N = qw.shape[1]
+        arr[i] = _W4A16Problem(A.data_ptr(), qw.data_ptr(), sc.data_ptr(), Y.data_ptr(), M, N, K)
+        mmax, kmax, nsum, dev = max(mmax, M), max(kmax, K), nsum + N, A.device
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, mmax, nsum, kmax), dev)
+    _check(lib.qz_gemm_w4a16_grouped(arr, len(problems), _ptr(buf), nb, _stream(stream)),
+           "qz_gemm_w4a16_grouped")
+
+
+def qz_gemm_fp8_block(qA, sA, qB, sB, Y=None, ws=None, stream=None):
+    """Y[M, N] (bf16) from E4M3 qA [M, K] with 1x128 scales sA and E4M3 qB = B^T [N, K]
+    with 128x128 scales sB."""
+    M, K = qA.shape
+    N = qB.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_FP8_BLOCK, M, N, K), qA.device)
+    _check(lib.qz_gemm_fp8_block(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), _ptr(Y), M, N, K, _ptr(buf), nb,
+                                 _stream(stream)), "qz_gemm_fp8_block")
+    return Y
+
+
+def qz_gemm_nvfp4(qA, sA, gA, qB, sB, gB, Y=None, ws=None, stream=None):
+    """Y[M, N] (bf16) from NVFP4 A [M, K] and B^T [N, K] (codes, E4M3 block scales, fp32
+    tensor scale each)."""
+    M, K = qA.shape[0], qA.shape[1] * 2
+    N = qB.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), qA.device)
+    _check(lib.qz_gemm_nvfp4(_ptr(qA), _ptr(sA), _ptr(gA), _ptr(qB), _ptr(sB), _ptr(gB), _ptr(Y), M, N, K,
+                             _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4")
+    return Y
+
+
+def qz_gemm_mxfp4(qA, eA, qB, eB, Y=None, ws=None, stream=None):
+    """Y[M, N] (bf16) from MXFP4 A [M, K] and B^T [N, K] (codes, E8M0 block scales)."""
+    M, K = qA.shape[0], qA.shape[1] * 2
+    N = qB.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_MXFP4, M, N, K), qA.device)
+    _check(lib.qz_gemm_mxfp4(_ptr(qA), _ptr(eA), _ptr(qB), _ptr(eB), _ptr(Y), M, N, K, _ptr(buf), nb,
+                             _stream(stream)), "qz_gemm_mxfp4")
+    return Y

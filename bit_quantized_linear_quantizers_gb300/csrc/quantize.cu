@@ -1,0 +1,561 @@
+// quantize.cu -- quantizer kernels: FP8 E4M3 (per tensor / row / 128x128 /
+// 1x128), MXFP4, NVFP4, INT4 g128, and the FP8 KV-cache write.
+//
+// Each quantizer follows the fake-quant functions of "量化部署实战"
+// (anrans.github.io), section 伪量化实现: reduce |x| to an amax per scale
+// unit, derive the scale, then encode every element as code(x / scale).
+// The kernels emit the codes, the scales and optionally the dequantized fp32
+// tensor. They are HBM-bound: every thread moves 8 consecutive elements with
+// 16- or 32-byte loads, amax reductions use warp shuffles, and codes leave as
+// packed 4- or 8-byte stores.
+//
+// Per-tensor amax (FP8 per tensor, NVFP4's tensor scale, the KV write) is a
+// two-kernel reduction: kernel 1 writes one partial max per CTA into the
+// workspace, kernel 2 reduces those partials in every CTA (a few KB, read from
+// L2) before encoding. No atomics, no zero-initialised workspace.
+#include "qz_internal.cuh"
+
+#include <cuda_fp16.h>
+#include <algorithm>
+
+namespace qz {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// CTA-wide max of a per-thread value; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float* red) {
+    v = warp_max(v, 32);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();                       // `red` may still be in use by a previous call
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; i++) r = fmaxf(r, red[i]);
+    return r;
+}
+
+// FP8 encode of one value with scale s (clamp to +-448, E4M3 RNE).
+__device__ __forceinline__ uint32_t fp8_code(float x, float s) {
+    float y = div_rn(x, s);
+    y = fminf(fmaxf(y, -kFp8Max), kFp8Max);
+    return e4m3_code(y);
+}
+
+__device__ __forceinline__ float fp8_scale(float amax) {
+    return div_rn(fmaxf(amax, kAmaxMin), kFp8Max);
+}
+
+// Encode 8 values; write 8 code bytes (and 8 dequantized floats).
+__device__ __forceinline__ void fp8_encode8(const float v[8], float s, uint8_t* codes, float* deq) {
+    uint32_t c[8];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        float y0 = fminf(fmaxf(div_rn(v[j], s), -kFp8Max), kFp8Max);
+        float y1 = fminf(fmaxf(div_rn(v[j + 1], s), -kFp8Max), kFp8Max);
+        uint32_t p = e4m3x2(y0, y1);
+        c[j] = p & 0xFF;
+        c[j + 1] = p >> 8;
+    }
+    uint2 out;
+    out.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    out.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    *reinterpret_cast<uint2*>(codes) = out;
+    if (deq) {
+        float d[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) d[j] = __fmul_rn(e4m3_value(c[j]), s);
+        reinterpret_cast<float4*>(deq)[0] = make_float4(d[0], d[1], d[2], d[3]);
+        reinterpret_cast<float4*>(deq)[1] = make_float4(d[4], d[5], d[6], d[7]);
+    }
+}
+
+// Encode 8 values to E2M1 with scale s (division exact); returns 8 nibbles,
+// element j at bits 4j..4j+3. Writes dequant if requested.
+__device__ __forceinline__ uint32_t fp4_encode8(const float v[8], float s, float* deq) {
+    uint32_t packed = 0;
+    float d[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        uint32_t c = e2m1_code(div_rn(v[j], s));
+        packed |= c << (4 * j);
+        d[j] = __fmul_rn(e2m1_value(c), s);
+    }
+    if (deq) {
+        reinterpret_cast<float4*>(deq)[0] = make_float4(d[0], d[1], d[2], d[3]);
+        reinterpret_cast<float4*>(deq)[1] = make_float4(d[4], d[5], d[6], d[7]);
+    }
+    return packed;
+}
+
+// Element offset of chunk i (8 elements per chunk when VEC, 1 otherwise).
+template <bool VEC>
+__device__ __forceinline__ int64_t chunk_offset(int64_t i, bool contig, int64_t cpr, int64_t ldx) {
+    constexpr int E = VEC ? 8 : 1;
+    if (contig) return i * E;
+    int64_t r = i / cpr;
+    return r * ldx + (i - r * cpr) * E;
+}
+
+// ------------------------------------------------------ per-tensor amax
+
+// Kernel 1 of a per-tensor reduction: partial[y * gridDim.x + blockIdx.x] =
+// max |x_y| over this CTA's grid-stride share of tensor y (y = blockIdx.y,
+// at most two tensors, for K and V).
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+amax_partial_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t rows, int64_t cols,
+                    int64_t ldx, bool contig, float* __restrict__ partial) {
+    __shared__ float red[kWarps];
+    const T* x = blockIdx.y ? x1 : x0;
+    const int64_t cpr = VEC ? cols / 8 : cols;
+    const int64_t total = rows * cpr;
+    float m = 0.0f;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += stride) {
+        const int64_t off = chunk_offset<VEC>(i, contig, cpr, ldx);
+        if constexpr (VEC) {
+            float v[8];
+            Load8<T>::run(x + off, v);
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+        } else {
+            m = fmaxf(m, fabsf(load1(x + off)));
+        }
+    }
+    m = block_max(m, red);
+    if (threadIdx.x == 0) partial[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = m;
+}
+
+__device__ __forceinline__ float reduce_partials(const float* __restrict__ p, int n, float* red) {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < n; i += kThreads) m = fmaxf(m, __ldcg(p + i));
+    return block_max(m, red);
+}
+
+// Kernel 2 of per-tensor FP8: every CTA reduces the partials to the tensor
+// amax (or reads a given scale), then encodes its grid-stride share.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+fp8_tensor_encode_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t rows, int64_t cols,
+                         int64_t ldx, bool contig, const float* __restrict__ partial, int nparts,
+                         const float* __restrict__ given0, const float* __restrict__ given1,
+                         uint8_t* __restrict__ c0, uint8_t* __restrict__ c1,
+                         float* __restrict__ s0, float* __restrict__ s1,
+                         float* __restrict__ d0, float* __restrict__ d1) {
+    __shared__ float red[kWarps];
+    const int y = blockIdx.y;
+    const T* x = y ? x1 : x0;
+    uint8_t* codes = y ? c1 : c0;
+    float* deq = y ? d1 : d0;
+    float s;
+    if (partial) {
+        s = fp8_scale(reduce_partials(partial + (int64_t)y * nparts, nparts, red));
+        if (blockIdx.x == 0 && threadIdx.x == 0) *(y ? s1 : s0) = s;
+    } else {
+        s = __ldg(y ? given1 : given0);
+    }
+    const int64_t cpr = VEC ? cols / 8 : cols;
+    const int64_t total = rows * cpr;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += stride) {
+        const int64_t off = chunk_offset<VEC>(i, contig, cpr, ldx);
+        if constexpr (VEC) {
+            float v[8];
+            Load8<T>::run(x + off, v);
+            fp8_encode8(v, s, codes + i * 8, deq ? deq + i * 8 : nullptr);
+        } else {
+            const uint32_t c = fp8_code(load1(x + off), s);
+            codes[i] = (uint8_t)c;
+            if (deq) deq[i] = __fmul_rn(e4m3_value(c), s);
+        }
+    }
+}
+
+// ---------------------------------------------------------- per row
+
+// One warp per row: pass 1 reduces the row's amax, pass 2 re-reads the row
+// (from L1/L2) and encodes it.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+fp8_row_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+               uint8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const T* xr = x + r * ldx;
+        float m = 0.0f;
+        if constexpr (VEC) {
+            for (int64_t c = lane * 8; c < cols; c += 256) {
+                float v[8];
+                Load8<T>::run(xr + c, v);
+#pragma unroll
+                for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+            }
+        } else {
+            for (int64_t c = lane; c < cols; c += 32) m = fmaxf(m, fabsf(load1(xr + c)));
+        }
+        const float s = fp8_scale(warp_max(m, 32));
+        if (lane == 0) scales[r] = s;
+        uint8_t* cr = codes + r * cols;
+        float* dr = deq ? deq + r * cols : nullptr;
+        if constexpr (VEC) {
+            for (int64_t c = lane * 8; c < cols; c += 256) {
+                float v[8];
+                Load8<T>::run(xr + c, v);
+                fp8_encode8(v, s, cr + c, dr ? dr + c : nullptr);
+            }
+        } else {
+            for (int64_t c = lane; c < cols; c += 32) {
+                const uint32_t code = fp8_code(load1(xr + c), s);
+                cr[c] = (uint8_t)code;
+                if (dr) dr[c] = __fmul_rn(e4m3_value(code), s);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------- 1 x 128 groups
+
+// 16 threads per 128-element group (8 elements each); a warp covers two
+// groups. Loops run warp-uniformly so the shuffles always see 32 lanes.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+fp8_group_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, bool contig,
+                 uint8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t cpr = cols / 8;
+    const int64_t total = rows * cpr;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    for (int64_t base = wbase; base < total; base += wstride) {
+        const int64_t i = base + lane;
+        const bool ok = i < total;
+        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+        const float s = fp8_scale(warp_max(m, 16));
+        if (ok) {
+            if ((lane & 15) == 0) scales[i >> 4] = s;
+            fp8_encode8(v, s, codes + i * 8, deq ? deq + i * 8 : nullptr);
+        }
+    }
+}
+
+// ----------------------------------------------------- 128 x 128 blocks
+
+// One CTA per (br x 128) block, br = min(128, rows); the block stays in
+// registers (up to 8 chunks of 8 values per thread) between amax and encode.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+fp8_block_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, int br,
+                 uint8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    __shared__ float red[kWarps];
+    const int64_t nbc = cols / 128;
+    const int64_t bi = blockIdx.x / nbc, bj = blockIdx.x % nbc;
+    const int nchunks = br * 16;
+    float v[8][8];
+    float m = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const int j = threadIdx.x + u * kThreads;
+        if (j < nchunks) {
+            const int64_t r = bi * br + (j >> 4), c = bj * 128 + (j & 15) * 8;
+            Load8<T>::run(x + r * ldx + c, v[u]);
+#pragma unroll
+            for (int e = 0; e < 8; e++) m = fmaxf(m, fabsf(v[u][e]));
+        }
+    }
+    const float s = fp8_scale(block_max(m, red));
+    if (threadIdx.x == 0) scales[blockIdx.x] = s;
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const int j = threadIdx.x + u * kThreads;
+        if (j < nchunks) {
+            const int64_t r = bi * br + (j >> 4), c = bj * 128 + (j & 15) * 8;
+            fp8_encode8(v[u], s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MXFP4
+
+// 4 threads per 32-element block. scale = 2^(E-2) with E = floor(log2 amax)
+// read from the exponent field; x / 2^(E-2) is exact as x * 2^(2-E).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, bool contig,
+             uint8_t* __restrict__ codes, uint8_t* __restrict__ e8m0, float* __restrict__ deq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t cpr = cols / 8;
+    const int64_t total = rows * cpr;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    for (int64_t base = wbase; base < total; base += wstride) {
+        const int64_t i = base + lane;
+        const bool ok = i < total;
+        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+        m = fmaxf(warp_max(m, 4), kAmaxMin);
+        const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;   // m is normal
+        const float s = __uint_as_float((uint32_t)(E - 2 + 127) << 23);
+        const float inv = __uint_as_float((uint32_t)(127 + 2 - E) << 23);
+        if (ok) {
+            uint32_t packed = 0;
+            float d[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t c = e2m1_code(__fmul_rn(v[j], inv));
+                packed |= c << (4 * j);
+                d[j] = __fmul_rn(e2m1_value(c), s);
+            }
+            reinterpret_cast<uint32_t*>(codes)[i] = packed;
+            if (deq) {
+                reinterpret_cast<float4*>(deq + i * 8)[0] = make_float4(d[0], d[1], d[2], d[3]);
+                reinterpret_cast<float4*>(deq + i * 8)[1] = make_float4(d[4], d[5], d[6], d[7]);
+            }
+            if ((lane & 3) == 0) e8m0[i >> 2] = (uint8_t)(E - 2 + 127);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ NVFP4
+
+// 2 threads per 16-element block. g comes from the per-tensor partials (or
+// a given amax); the block scale is E4M3(amax16 / 6 / g).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, bool contig,
+             const float* __restrict__ partial, int nparts, const float* __restrict__ amax_in,
+             uint8_t* __restrict__ codes, uint8_t* __restrict__ sb, float* __restrict__ g_out,
+             float* __restrict__ deq) {
+    __shared__ float red[kWarps];
+    const float amax_t = partial ? reduce_partials(partial, nparts, red) : __ldg(amax_in);
+    const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    const int lane = threadIdx.x & 31;
+    const int64_t cpr = cols / 8;
+    const int64_t total = rows * cpr;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    for (int64_t base = wbase; base < total; base += wstride) {
+        const int64_t i = base + lane;
+        const bool ok = i < total;
+        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+        m = warp_max(m, 2);
+        const float t = div_rn(div_rn(m, kFp4Max), g);
+        const uint32_t bcode = e4m3_code(t);                 // saturating, as the clamp-free page
+        const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
+        if (ok) {
+            const uint32_t packed = fp4_encode8(v, s, deq ? deq + i * 8 : nullptr);
+            reinterpret_cast<uint32_t*>(codes)[i] = packed;
+            if ((lane & 1) == 0) sb[i >> 1] = (uint8_t)bcode;
+        }
+    }
+}
+
+// --------------------------------------------------------------- INT4 g128
+
+// One CTA per (group of 128 rows) x (64 columns) tile of w[K, N]: the tile is
+// staged in shared memory, 4 threads reduce each column's amax over 32 rows,
+// then every (k-octet, column) pair packs eight 4-bit codes into one int32.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+int4_g128_kernel(const T* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
+                 int32_t* __restrict__ qweight, uint16_t* __restrict__ scale, float* __restrict__ deq) {
+    __shared__ float tile[128][65];
+    __shared__ float part[4][64];
+    __shared__ float sc[64];
+    const int64_t ncb = N / 64;
+    const int64_t g = blockIdx.x / ncb, n0 = (blockIdx.x % ncb) * 64;
+    // load 128 x 64 (8 chunks of 8 per row; 1024 chunks, 4 per thread)
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        const int j = threadIdx.x + u * kThreads;
+        const int r = j >> 3, c = (j & 7) * 8;
+        float v[8];
+        Load8<T>::run(w + (g * 128 + r) * ldw + n0 + c, v);
+#pragma unroll
+        for (int e = 0; e < 8; e++) tile[r][c + e] = v[e];
+    }
+    __syncthreads();
+    {
+        const int c = threadIdx.x & 63, p = threadIdx.x >> 6;
+        float m = 0.0f;
+        for (int r = p * 32; r < p * 32 + 32; r++) m = fmaxf(m, fabsf(tile[r][c]));
+        part[p][c] = m;
+    }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+        const int c = threadIdx.x;
+        const float m = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
+        const float sf = div_rn(fmaxf(m, kAmaxMin), 7.0f);
+        const __nv_bfloat16 sb = __float2bfloat16_rn(sf);
+        const uint16_t bits = __bfloat16_as_ushort(sb);
+        scale[g * N + n0 + c] = bits;
+        sc[c] = bf16_bits_to_f32(bits);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        const int j = threadIdx.x + u * kThreads;        // 16 octets x 64 columns
+        const int o = j >> 6, c = j & 63;
+        const float s = sc[c];
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float val = tile[o * 8 + e][c];
+            float q = rintf(div_rn(val, s));
+            q = fminf(fmaxf(q, -8.0f), 7.0f);
+            word |= ((uint32_t)(int)q & 0xFu) << (4 * e);
+            if (deq) deq[(g * 128 + o * 8 + e) * N + n0 + c] = __fmul_rn(q, s);
+        }
+        qweight[(g * 16 + o) * N + n0 + c] = (int32_t)word;
+    }
+}
+
+// ---------------------------------------------------------------- helpers
+
+int amax_grid() { return num_sms() * 4; }
+
+int stream_grid(int64_t threads_needed) {
+    const int64_t ctas = (threads_needed + kThreads - 1) / kThreads;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * 8));
+}
+
+bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
+    const size_t es = t == QZ_F32 ? 4 : 2;
+    return is_aligned(x, 16) && ((size_t)ldx * es) % 16 == 0 && cols % 8 == 0;
+}
+
+template <typename T, bool VEC>
+void launch_tensor_amax(const void* x0, const void* x1, int ny, int64_t rows, int64_t cols, int64_t ldx,
+                        bool contig, float* partial, cudaStream_t st) {
+    dim3 grid(amax_grid(), ny);
+    amax_partial_kernel<T, VEC><<<grid, kThreads, 0, st>>>(
+        (const T*)x0, (const T*)x1, rows, cols, ldx, contig, partial);
+}
+
+} // namespace
+
+size_t ws_quantize_fp8_tensor(int64_t, int64_t) { return (size_t)amax_grid() * sizeof(float); }
+size_t ws_quantize_nvfp4(int64_t, int64_t) { return (size_t)amax_grid() * sizeof(float); }
+size_t ws_kv_write(int64_t) { return (size_t)2 * amax_grid() * sizeof(float); }
+
+template <typename T>
+static qz_status fp8_launch_t(const T* x, int64_t rows, int64_t cols, int64_t ldx, qz_fp8_gran gran,
+                              uint8_t* codes, float* scales, float* deq, void* ws, cudaStream_t st,
+                              bool vec) {
+    const bool contig = (ldx == cols);
+    switch (gran) {
+    case QZ_FP8_PER_TENSOR: {
+        float* partial = (float*)ws;
+        const int np = amax_grid();
+        const int64_t work = vec ? rows * cols / 8 : rows * cols;
+        if (vec) {
+            launch_tensor_amax<T, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
+            fp8_tensor_encode_kernel<T, true><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
+                x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
+                scales, deq, deq);
+        } else {
+            launch_tensor_amax<T, false>(x, x, 1, rows, cols, ldx, contig, partial, st);
+            fp8_tensor_encode_kernel<T, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
+                x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
+                scales, deq, deq);
+        }
+        break;
+    }
+    case QZ_FP8_PER_ROW: {
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kWarps - 1) / kWarps,
+                                                                     (int64_t)num_sms() * 8));
+        if (vec) fp8_row_kernel<T, true><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, codes, scales, deq);
+        else fp8_row_kernel<T, false><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, codes, scales, deq);
+        break;
+    }
+    case QZ_FP8_GROUP_1x128:
+        fp8_group_kernel<T><<<stream_grid(rows * cols / 8), kThreads, 0, st>>>(
+            x, rows, cols, ldx, contig, codes, scales, deq);
+        break;
+    case QZ_FP8_BLOCK_128x128: {
+        const int br = (int)std::min<int64_t>(128, rows);
+        const int64_t nblocks = (rows / br) * (cols / 128);
+        fp8_block_kernel<T><<<(unsigned)nblocks, kThreads, 0, st>>>(x, rows, cols, ldx, br, codes,
+                                                                     scales, deq);
+        break;
+    }
+    }
+    return launch_status();
+}
+
+qz_status quantize_fp8_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                              qz_fp8_gran gran, uint8_t* codes, float* scales, float* deq,
+                              void* ws, size_t, cudaStream_t st) {
+    const bool vec = vec_ok(x, ldx, cols, xt);
+    if (xt == QZ_F32) return fp8_launch_t<float>((const float*)x, rows, cols, ldx, gran, codes, scales, deq, ws, st, vec);
+    return fp8_launch_t<uint16_t>((const uint16_t*)x, rows, cols, ldx, gran, codes, scales, deq, ws, st, vec);
+}
+
+qz_status quantize_mxfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t* codes, uint8_t* e8m0, float* deq, cudaStream_t st) {
+    const bool contig = (ldx == cols);
+    const int grid = stream_grid(rows * cols / 8);
+    if (xt == QZ_F32)
+        mxfp4_kernel<float><<<grid, kThreads, 0, st>>>((const float*)x, rows, cols, ldx, contig, codes, e8m0, deq);
+    else
+        mxfp4_kernel<uint16_t><<<grid, kThreads, 0, st>>>((const uint16_t*)x, rows, cols, ldx, contig, codes, e8m0, deq);
+    return launch_status();
+}
+
+qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t* codes, uint8_t* sb, float* g, const float* amax_in,
+                                float* deq, void* ws, size_t, cudaStream_t st) {
+    const bool contig = (ldx == cols);
+    float* partial = amax_in ? nullptr : (float*)ws;
+    const int np = amax_grid();
+    const int grid = stream_grid(rows * cols / 8);
+    if (xt == QZ_F32) {
+        if (partial) launch_tensor_amax<float, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
+        nvfp4_kernel<float><<<grid, kThreads, 0, st>>>((const float*)x, rows, cols, ldx, contig, partial, np,
+                                                       amax_in, codes, sb, g, deq);
+    } else {
+        if (partial) launch_tensor_amax<uint16_t, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
+        nvfp4_kernel<uint16_t><<<grid, kThreads, 0, st>>>((const uint16_t*)x, rows, cols, ldx, contig, partial,
+                                                          np, amax_in, codes, sb, g, deq);
+    }
+    return launch_status();
+}
+
+qz_status quantize_int4_launch(const void* w, qz_dtype wt, int64_t K, int64_t N, int64_t ldw,
+                               int32_t* qweight, uint16_t* scale, float* deq, cudaStream_t st) {
+    const int64_t nblocks = (K / 128) * (N / 64);
+    if (wt == QZ_F32)
+        int4_g128_kernel<float><<<(unsigned)nblocks, kThreads, 0, st>>>((const float*)w, K, N, ldw, qweight, scale, deq);
+    else
+        int4_g128_kernel<uint16_t><<<(unsigned)nblocks, kThreads, 0, st>>>((const uint16_t*)w, K, N, ldw, qweight, scale, deq);
+    return launch_status();
+}
+
+qz_status kv_write_launch(const uint16_t* k, const uint16_t* v, int64_t n, uint8_t* kc, uint8_t* vc,
+                          float* ks, float* vs, qz_scale_mode mode, void* ws, size_t, cudaStream_t st) {
+    const int np = amax_grid();
+    float* partial = (mode == QZ_SCALE_COMPUTE) ? (float*)ws : nullptr;
+    if (partial) launch_tensor_amax<uint16_t, true>(k, v, 2, 1, n, n, true, partial, st);
+    fp8_tensor_encode_kernel<uint16_t, true><<<dim3(stream_grid(n / 8), 2), kThreads, 0, st>>>(
+        k, v, 1, n, n, true, partial, np, ks, vs, kc, vc, ks, vs, nullptr, nullptr);
+    return launch_status();
+}
+
+} // namespace qz

@@ -1,0 +1,268 @@
+// qz_api.cu -- the extern "C" entry points of libqz: host-side validation,
+// workspace sizing and dispatch to the kernels. Nothing here allocates device
+// memory; a call that fails validation enqueues nothing.
+#include "qz_internal.cuh"
+#include "qz_gemm.cuh"
+
+#include <mutex>
+
+namespace qz {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int g_arch_ok[kMaxDevices];   // 0 unknown, 1 sm_103, -1 other
+std::mutex g_mu;
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+} // namespace
+
+int num_sms() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    if (g_sms[d] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+        g_sms[d] = n > 0 ? n : 1;
+    }
+    return g_sms[d];
+}
+
+// The library carries sm_103a code only: refuse other devices up front.
+qz_status device_check() {
+    const int d = current_device();
+    if (d < 0) return QZ_ERR_UNSUPPORTED;
+    if (g_arch_ok[d] == 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int ma = 0, mi = 0;
+        if (cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess) {
+            cudaGetLastError();
+            return QZ_ERR_UNSUPPORTED;
+        }
+        g_arch_ok[d] = (ma == 10 && mi == 3) ? 1 : -1;
+    }
+    return g_arch_ok[d] == 1 ? QZ_OK : QZ_ERR_UNSUPPORTED;
+}
+
+qz_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? QZ_OK : QZ_ERR_CUDA;
+}
+
+bool is_aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+} // namespace qz
+
+using namespace qz;
+
+#define QZ_TRY(expr)                                   \
+    do {                                               \
+        const qz_status _s = (expr);                   \
+        if (_s != QZ_OK) return _s;                    \
+    } while (0)
+
+static size_t elem_size(qz_dtype t) { return t == QZ_F32 ? 4 : 2; }
+static bool dtype_ok(qz_dtype t) { return t == QZ_F32 || t == QZ_BF16; }
+
+extern "C" {
+
+const char* qz_status_string(qz_status s) {
+    switch (s) {
+    case QZ_OK: return "QZ_OK";
+    case QZ_ERR_INVALID_ARG: return "QZ_ERR_INVALID_ARG: null pointer, bad enum or negative size";
+    case QZ_ERR_SHAPE: return "QZ_ERR_SHAPE: size not divisible as required or out of range";
+    case QZ_ERR_ALIGNMENT: return "QZ_ERR_ALIGNMENT: pointer or leading dimension misaligned";
+    case QZ_ERR_UNSUPPORTED: return "QZ_ERR_UNSUPPORTED: no sm_103 device or path unavailable";
+    case QZ_ERR_CUDA: return "QZ_ERR_CUDA: CUDA runtime or launch error";
+    case QZ_ERR_TIMEOUT: return "QZ_ERR_TIMEOUT: a bounded device wait gave up";
+    case QZ_ERR_WORKSPACE: return "QZ_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "QZ_ERR_UNKNOWN";
+}
+
+size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2) {
+    switch (op) {
+    case QZ_OP_QUANTIZE_FP8: return d2 == QZ_FP8_PER_TENSOR ? ws_quantize_fp8_tensor(d0, d1) : 0;
+    case QZ_OP_QUANTIZE_NVFP4: return ws_quantize_nvfp4(d0, d1);
+    case QZ_OP_KV_WRITE_FP8: return ws_kv_write(d0);
+    case QZ_OP_GEMM_W4A16: return ws_gemm_w4a16((int)d0, (int)d1, (int)d2);
+    case QZ_OP_GEMM_FP8_BLOCK: return ws_gemm_fp8_block((int)d0, (int)d1, (int)d2);
+    case QZ_OP_GEMM_NVFP4: return ws_gemm_fp4((int)d0, (int)d1, (int)d2);
+    case QZ_OP_GEMM_MXFP4: return ws_gemm_fp4((int)d0, (int)d1, (int)d2);
+    }
+    return 0;
+}
+
+qz_status qz_device_error(void) { return device_error_read_and_clear(); }
+
+qz_status qz_quantize_fp8(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                          qz_fp8_gran gran, uint8_t* codes, float* scales, float* dequant,
+                          void* ws, size_t ws_bytes, void* stream) {
+    if (!dtype_ok(xt) || gran < QZ_FP8_PER_TENSOR || gran > QZ_FP8_GROUP_1x128) return QZ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ldx < cols) return QZ_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return gran == QZ_FP8_PER_TENSOR ? QZ_ERR_SHAPE : QZ_OK;
+    if (!x || !codes || !scales) return QZ_ERR_INVALID_ARG;
+    const bool vec = is_aligned(x, 16) && ((size_t)ldx * elem_size(xt)) % 16 == 0 && cols % 8 == 0;
+    if (gran == QZ_FP8_BLOCK_128x128 || gran == QZ_FP8_GROUP_1x128) {
+        if (cols % 128) return QZ_ERR_SHAPE;
+        if (gran == QZ_FP8_BLOCK_128x128 && rows > 128 && rows % 128) return QZ_ERR_SHAPE;
+        if (!vec) return QZ_ERR_ALIGNMENT;
+    }
+    if (vec && (!is_aligned(codes, 8) || (dequant && !is_aligned(dequant, 16)))) return QZ_ERR_ALIGNMENT;
+    if (gran == QZ_FP8_PER_TENSOR) {
+        if (!ws) return QZ_ERR_WORKSPACE;
+        if (ws_bytes < ws_quantize_fp8_tensor(rows, cols) || !is_aligned(ws, 4)) return QZ_ERR_WORKSPACE;
+    }
+    QZ_TRY(device_check());
+    return quantize_fp8_launch(x, xt, rows, cols, ldx, gran, codes, scales, dequant, ws, ws_bytes,
+                               (cudaStream_t)stream);
+}
+
+static qz_status fp4_common_checks(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                   int block, const uint8_t* codes, const void* scales, const float* deq) {
+    if (!dtype_ok(xt)) return QZ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ldx < cols) return QZ_ERR_INVALID_ARG;
+    if (cols % block) return QZ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return QZ_OK;
+    if (!x || !codes || !scales) return QZ_ERR_INVALID_ARG;
+    if (!is_aligned(x, 16) || ((size_t)ldx * elem_size(xt)) % 16) return QZ_ERR_ALIGNMENT;
+    if (!is_aligned(codes, 4) || (deq && !is_aligned(deq, 16))) return QZ_ERR_ALIGNMENT;
+    return QZ_OK;
+}
+
+qz_status qz_quantize_mxfp4(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t* codes, uint8_t* scale_e8m0, float* dequant, void* stream) {
+    QZ_TRY(fp4_common_checks(x, xt, rows, cols, ldx, 32, codes, scale_e8m0, dequant));
+    if (rows == 0 || cols == 0) return QZ_OK;
+    QZ_TRY(device_check());
+    return quantize_mxfp4_launch(x, xt, rows, cols, ldx, codes, scale_e8m0, dequant, (cudaStream_t)stream);
+}
+
+qz_status qz_quantize_nvfp4(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t* codes, uint8_t* scale_e4m3, float* global_scale,
+                            const float* global_amax_in, float* dequant,
+                            void* ws, size_t ws_bytes, void* stream) {
+    QZ_TRY(fp4_common_checks(x, xt, rows, cols, ldx, 16, codes, scale_e4m3, dequant));
+    if (rows == 0 || cols == 0) return global_amax_in ? QZ_OK : QZ_ERR_SHAPE;
+    if (!global_scale) return QZ_ERR_INVALID_ARG;
+    if (!global_amax_in) {
+        if (!ws) return QZ_ERR_WORKSPACE;
+        if (ws_bytes < ws_quantize_nvfp4(rows, cols) || !is_aligned(ws, 4)) return QZ_ERR_WORKSPACE;
+    }
+    QZ_TRY(device_check());
+    return quantize_nvfp4_launch(x, xt, rows, cols, ldx, codes, scale_e4m3, global_scale, global_amax_in,
+                                 dequant, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+qz_status qz_quantize_int4_g128(const void* w, qz_dtype wt, int64_t K, int64_t N, int64_t ldw,
+                                int32_t* qweight, uint16_t* scale_bf16, float* dequant, void* stream) {
+    if (!dtype_ok(wt)) return QZ_ERR_INVALID_ARG;
+    if (K < 0 || N < 0 || ldw < N) return QZ_ERR_INVALID_ARG;
+    if (K % 128 || N % 64) return QZ_ERR_SHAPE;
+    if (K == 0 || N == 0) return QZ_OK;
+    if (!w || !qweight || !scale_bf16) return QZ_ERR_INVALID_ARG;
+    if (!is_aligned(w, 16) || ((size_t)ldw * elem_size(wt)) % 16) return QZ_ERR_ALIGNMENT;
+    if (!is_aligned(qweight, 16) || !is_aligned(scale_bf16, 16) || (dequant && !is_aligned(dequant, 16)))
+        return QZ_ERR_ALIGNMENT;
+    QZ_TRY(device_check());
+    return quantize_int4_launch(w, wt, K, N, ldw, qweight, scale_bf16, dequant, (cudaStream_t)stream);
+}
+
+qz_status qz_kv_write_fp8(const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
+                          uint8_t* k_codes, uint8_t* v_codes, float* k_scale, float* v_scale,
+                          qz_scale_mode mode, void* ws, size_t ws_bytes, void* stream) {
+    if (mode != QZ_SCALE_COMPUTE && mode != QZ_SCALE_GIVEN) return QZ_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || T < 0 || D < 0) return QZ_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)B * H * T * D;
+    if (n == 0) return mode == QZ_SCALE_GIVEN ? QZ_OK : QZ_ERR_SHAPE;
+    if (!k || !v || !k_codes || !v_codes || !k_scale || !v_scale) return QZ_ERR_INVALID_ARG;
+    if (n % 8) return QZ_ERR_SHAPE;
+    if (!is_aligned(k, 16) || !is_aligned(v, 16) || !is_aligned(k_codes, 8) || !is_aligned(v_codes, 8))
+        return QZ_ERR_ALIGNMENT;
+    if (mode == QZ_SCALE_COMPUTE) {
+        if (!ws) return QZ_ERR_WORKSPACE;
+        if (ws_bytes < ws_kv_write(n) || !is_aligned(ws, 4)) return QZ_ERR_WORKSPACE;
+    }
+    QZ_TRY(device_check());
+    return kv_write_launch(k, v, n, k_codes, v_codes, k_scale, v_scale, mode, ws, ws_bytes,
+                           (cudaStream_t)stream);
+}
+
+qz_status qz_gemm_w4a16(const uint16_t* A, const int32_t* qweight, const uint16_t* scale_bf16,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+    qz_w4a16_problem p{A, qweight, scale_bf16, Y, M, N, K};
+    return qz_gemm_w4a16_grouped(&p, 1, ws, ws_bytes, stream);
+}
+
+qz_status qz_gemm_w4a16_grouped(const qz_w4a16_problem* problems, int count, void* ws, size_t ws_bytes,
+                                void* stream) {
+    if (!problems || count < 1 || count > kW4A16MaxProblems) return QZ_ERR_INVALID_ARG;
+    int mmax = 0, kmax = 0;
+    int64_t nsum = 0;
+    for (int i = 0; i < count; i++) {
+        const qz_w4a16_problem& p = problems[i];
+        if (!p.A || !p.qweight || !p.scale_bf16 || !p.Y) return QZ_ERR_INVALID_ARG;
+        if (p.M < 1 || p.N < 1 || p.K < 1) return QZ_ERR_INVALID_ARG;
+        if (p.M > 64 || p.K % 128 || p.N % 64) return QZ_ERR_SHAPE;
+        if (!is_aligned(p.A, 16) || !is_aligned(p.qweight, 16) || !is_aligned(p.scale_bf16, 16) ||
+            !is_aligned(p.Y, 16))
+            return QZ_ERR_ALIGNMENT;
+        mmax = p.M > mmax ? p.M : mmax;
+        kmax = p.K > kmax ? p.K : kmax;
+        nsum += p.N;
+    }
+    const size_t need = ws_gemm_w4a16(mmax, (int)nsum, kmax);
+    if (need && (!ws || ws_bytes < need || !is_aligned(ws, 16))) return QZ_ERR_WORKSPACE;
+    QZ_TRY(device_check());
+    return gemm_w4a16_launch(problems, count, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+qz_status qz_gemm_fp8_block(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                            uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+    if (!qA || !sA || !qB || !sB || !Y) return QZ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return QZ_ERR_INVALID_ARG;
+    if (M % kFp8BlockM || N % kFp8BlockN || K % 128) return QZ_ERR_SHAPE;
+    if (!is_aligned(qA, 16) || !is_aligned(qB, 16) || !is_aligned(sA, 16) || !is_aligned(sB, 16) ||
+        !is_aligned(Y, 16))
+        return QZ_ERR_ALIGNMENT;
+    const size_t need = ws_gemm_fp8_block(M, N, K);
+    if (need && (!ws || ws_bytes < need || !is_aligned(ws, 16))) return QZ_ERR_WORKSPACE;
+    QZ_TRY(device_check());
+    return gemm_fp8_block_launch(qA, sA, qB, sB, Y, M, N, K, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+static qz_status fp4_gemm_checks(const void* qA, const void* sA, const void* qB, const void* sB,
+                                 const void* Y, int M, int N, int K, void* ws, size_t ws_bytes) {
+    if (!qA || !sA || !qB || !sB || !Y) return QZ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return QZ_ERR_INVALID_ARG;
+    if (M % kFp4BlockM || N % kFp4BlockN || K % kFp4BlockK) return QZ_ERR_SHAPE;
+    if (!is_aligned(qA, 16) || !is_aligned(qB, 16) || !is_aligned(sA, 16) || !is_aligned(sB, 16) ||
+        !is_aligned(Y, 16))
+        return QZ_ERR_ALIGNMENT;
+    const size_t need = ws_gemm_fp4(M, N, K);
+    if (need && (!ws || ws_bytes < need || !is_aligned(ws, 16))) return QZ_ERR_WORKSPACE;
+    return QZ_OK;
+}
+
+qz_status qz_gemm_nvfp4(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                        const uint8_t* qB, const uint8_t* sB, const float* gB,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+    if (!gA || !gB) return QZ_ERR_INVALID_ARG;
+    QZ_TRY(fp4_gemm_checks(qA, sA, qB, sB, Y, M, N, K, ws, ws_bytes));
+    QZ_TRY(device_check());
+    return gemm_fp4_launch(true, qA, sA, gA, qB, sB, gB, Y, M, N, K, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+    QZ_TRY(fp4_gemm_checks(qA, eA, qB, eB, Y, M, N, K, ws, ws_bytes));
+    QZ_TRY(device_check());
+    return gemm_fp4_launch(false, qA, eA, nullptr, qB, eB, nullptr, Y, M, N, K, ws, ws_bytes,
+                           (cudaStream_t)stream);
+}
+
+} // extern "C"

@@ -1,0 +1,86 @@
+// qz_gemm.cuh -- GEMM launchers and the PTX helpers they share (mbarrier,
+// bulk copies, bounded waits).
+#pragma once
+
+#include "qz_internal.cuh"
+
+namespace qz {
+
+constexpr int kW4A16MaxProblems = 256;
+constexpr int kFp8BlockM = 128, kFp8BlockN = 256;
+constexpr int kFp4BlockM = 128, kFp4BlockN = 256, kFp4BlockK = 256;
+
+size_t ws_gemm_w4a16(int M, int N, int K);
+size_t ws_gemm_fp8_block(int M, int N, int K);
+size_t ws_gemm_fp4(int M, int N, int K);
+
+qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void* ws, size_t ws_bytes,
+                            cudaStream_t st);
+qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                                uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
+qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
+                          const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
+                          int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// Device error words of the GEMM translation units (read and cleared by
+// qz_device_error). Each returns QZ_OK, QZ_ERR_TIMEOUT or QZ_ERR_CUDA.
+qz_status w4a16_error_read_and_clear();
+qz_status fp8_block_error_read_and_clear();
+qz_status fp4_error_read_and_clear();
+qz_status device_error_read_and_clear();
+
+// ------------------------------------------------------------ PTX helpers
+
+// A bounded spin-wait gives up after this many polls (seconds of waiting),
+// records QZ_ERR_TIMEOUT in the translation unit's error word and returns
+// false, so no kernel can hang the GPU on a lost arrival.
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of the mbarrier; false (and *err set) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+    for (uint32_t i = 0; i < kWaitLimit; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicExch(err, (unsigned int)QZ_ERR_TIMEOUT);
+    return false;
+}
+
+// 1-D bulk copy global -> shared through the TMA unit, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+} // namespace qz

@@ -1,0 +1,126 @@
+// qz_internal.cuh -- device codecs and host helpers shared by the libqz kernels.
+//
+// Number formats ("量化部署实战", 格式速查; "量化：让每一步搬更少的字节",
+// 新一代低位格式):
+//   E4M3 (fn): 1 sign, 4 exponent (bias 7), 3 mantissa bits, max 448, no inf.
+//   E2M1: 1 sign, 2 exponent, 1 mantissa bit: +-{0, .5, 1, 1.5, 2, 3, 4, 6}.
+//   E8M0: an 8-bit biased exponent (bias 127), a pure power of two.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "../../include/qz.h"
+
+namespace qz {
+
+// The clamp floor of the fake-quant functions: the fp32 value nearest 1e-12.
+constexpr float kAmaxMin = 1e-12f;
+constexpr float kFp8Max = 448.0f;
+constexpr float kFp4Max = 6.0f;
+
+// ---------------------------------------------------------------- device
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
+    return __uint_as_float(b16 << 16);
+}
+
+// Widen eight consecutive input elements (fp32 or bf16) to fp32.
+template <typename T> struct Load8;
+template <> struct Load8<float> {
+    static __device__ __forceinline__ void run(const float* p, float v[8]) {
+        float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+template <> struct Load8<uint16_t> {
+    static __device__ __forceinline__ void run(const uint16_t* p, float v[8]) {
+        uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+        uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+
+__device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const uint16_t* p) { return bf16_bits_to_f32(__ldg(p)); }
+
+// x / s rounded once (IEEE round to nearest even): the codes depend on it.
+__device__ __forceinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
+
+// Two fp32 -> two E4M3 bytes, round to nearest even, saturating to +-448
+// (the hardware conversion). Returns lo | hi << 8.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Value of one E4M3 byte as fp32 (exact; via the hardware E4M3 -> f16 conversion).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    uint32_t h2;
+    uint16_t in = (uint16_t)(code & 0xFF);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// E4M3 code of one fp32 already clamped to +-448.
+__device__ __forceinline__ uint32_t e4m3_code(float y) { return e4m3x2(y, 0.0f) & 0xFF; }
+
+// E2M1 code of y: the nearest grid magnitude, an exact midpoint going to the
+// smaller magnitude (first index of the minimum distance), sign bit = (y < 0).
+// Magnitudes above 6 give code 7 (the clamp to +-6 of the fake-quant).
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+    float a = fabsf(y);
+    uint32_t m = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) +
+                 (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
+    return m | (y < 0.0f ? 8u : 0u);
+}
+
+// Value of a 4-bit E2M1 code (sign bit 3) as fp32; code 8 gives -0.0.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    uint32_t m = c & 7u, e = m >> 1, f = m & 1u;
+    float v = (m < 2u) ? 0.5f * (float)f : __uint_as_float(((e + 126u) << 23) | (f << 22));
+    return (c & 8u) ? -v : v;
+}
+
+__device__ __forceinline__ float warp_max(float v, int width) {
+    for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------ host
+
+int num_sms();                         // SM count of the current device (cached)
+qz_status launch_status();             // cudaGetLastError -> qz_status
+bool is_aligned(const void* p, size_t a);
+
+} // namespace qz
+
+// Internal launchers (quantize.cu).
+namespace qz {
+size_t ws_quantize_fp8_tensor(int64_t rows, int64_t cols);
+size_t ws_quantize_nvfp4(int64_t rows, int64_t cols);
+size_t ws_kv_write(int64_t n);
+
+qz_status quantize_fp8_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                              qz_fp8_gran gran, uint8_t* codes, float* scales, float* deq,
+                              void* ws, size_t ws_bytes, cudaStream_t st);
+qz_status quantize_mxfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t* codes, uint8_t* e8m0, float* deq, cudaStream_t st);
+qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                uint8_t* codes, uint8_t* sb, float* g, const float* amax_in,
+                                float* deq, void* ws, size_t ws_bytes, cudaStream_t st);
+qz_status quantize_int4_launch(const void* w, qz_dtype wt, int64_t K, int64_t N, int64_t ldw,
+                               int32_t* qweight, uint16_t* scale, float* deq, cudaStream_t st);
+qz_status kv_write_launch(const uint16_t* k, const uint16_t* v, int64_t n, uint8_t* kc, uint8_t* vc,
+                          float* ks, float* vs, qz_scale_mode mode, void* ws, size_t ws_bytes,
+                          cudaStream_t st);
+} // namespace qz

@@ -1,0 +1,233 @@
+/*
+ * qz.h -- C ABI of libqz: low-bit quantizers and quantized linear layers for
+ * one GB300 (sm_103a) GPU.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership: every data pointer is a DEVICE pointer owned by the caller. The
+ *   library never allocates or frees device memory. Scratch that a call needs
+ *   comes from a caller buffer `ws` of at least qz_workspace_size(...) bytes.
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream). Every call only enqueues work on that stream and returns
+ *   without synchronising; outputs are valid in stream order. A workspace must
+ *   not be shared by calls that may run concurrently.
+ * Layout: row-major, leading dimension in elements. Packed 4-bit codes put
+ *   the even-index element in the low nibble of each byte. bf16 data is passed
+ *   as uint16_t bit patterns. Scales use the row-major layouts given per call.
+ * Errors: every call returns a qz_status. Arguments are validated on the host
+ *   before anything is enqueued, so a rejected call launches nothing and
+ *   leaves every output untouched. No call aborts, throws or prints.
+ *   QZ_ERR_CUDA reports a launch or runtime error seen right after enqueueing.
+ * Numerics: the codes and scales of every quantizer are defined by the fake-
+ *   quant functions of "量化部署实战" (anrans.github.io), section 伪量化实现,
+ *   computed in IEEE fp32 (bf16 inputs are widened exactly to fp32 first):
+ *   E4M3 rounds to nearest even and saturates at +-448; E2M1 rounds to the
+ *   nearest of +-{0, .5, 1, 1.5, 2, 3, 4, 6} with exact ties going to the
+ *   smaller magnitude; the clamp floor 1e-12 is the fp32 value nearest 1e-12.
+ *   NaN or infinite inputs are outside the contract (no fault, undefined codes).
+ */
+#ifndef QZ_H
+#define QZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qz_status {
+    QZ_OK = 0,
+    QZ_ERR_INVALID_ARG = 1,   /* null pointer, unknown enum value, negative size */
+    QZ_ERR_SHAPE = 2,         /* size not divisible as required, or out of the supported range */
+    QZ_ERR_ALIGNMENT = 3,     /* pointer or leading dimension not aligned as required */
+    QZ_ERR_UNSUPPORTED = 4,   /* no usable sm_103 device, or the path is not available */
+    QZ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+    QZ_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (see qz_device_error) */
+    QZ_ERR_WORKSPACE = 7      /* ws is NULL or smaller than qz_workspace_size() */
+} qz_status;
+
+typedef enum qz_dtype { QZ_F32 = 0, QZ_BF16 = 1 } qz_dtype;
+
+typedef enum qz_fp8_gran {
+    QZ_FP8_PER_TENSOR = 0,    /* one scale for the tensor                      scales[1]             */
+    QZ_FP8_PER_ROW = 1,       /* one scale per row (output channel / token)    scales[rows]          */
+    QZ_FP8_BLOCK_128x128 = 2, /* one scale per (br x 128) block, br=min(128,rows) scales[rows/br][cols/128] */
+    QZ_FP8_GROUP_1x128 = 3    /* one scale per row per 128 columns             scales[rows][cols/128] */
+} qz_fp8_gran;
+
+typedef enum qz_scale_mode {
+    QZ_SCALE_COMPUTE = 0,     /* scale = max(amax, 1e-12) / 448 from the data written   */
+    QZ_SCALE_GIVEN = 1        /* use the caller's (calibrated) scale, read from device  */
+} qz_scale_mode;
+
+typedef enum qz_op {
+    QZ_OP_QUANTIZE_FP8 = 0,   /* d0 = rows, d1 = cols, d2 = granularity   */
+    QZ_OP_QUANTIZE_NVFP4 = 1, /* d0 = rows, d1 = cols                      */
+    QZ_OP_KV_WRITE_FP8 = 2,   /* d0 = elements per tensor (B*H*T*D)        */
+    QZ_OP_GEMM_W4A16 = 3,     /* d0 = M, d1 = N, d2 = K                    */
+    QZ_OP_GEMM_FP8_BLOCK = 4, /* d0 = M, d1 = N, d2 = K                    */
+    QZ_OP_GEMM_NVFP4 = 5,     /* d0 = M, d1 = N, d2 = K                    */
+    QZ_OP_GEMM_MXFP4 = 6      /* d0 = M, d1 = N, d2 = K                    */
+} qz_op;
+
+/* Bytes of workspace the call `op` needs for the given sizes (0 if none).
+ * Returns 0 for an unknown op. Sizes that the call itself would reject still
+ * return a (harmless) value. Workspace contents need no initialisation. */
+size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2);
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* qz_status_string(qz_status s);
+
+/* Reads and clears the library's device-side error word on the current
+ * device (set when a bounded wait inside a GEMM kernel gives up). Returns
+ * QZ_ERR_TIMEOUT if it was set, QZ_OK if not, QZ_ERR_CUDA if the read failed.
+ * Synchronises with the legacy default stream. */
+qz_status qz_device_error(void);
+
+/* ------------------------------------------------------------ quantizers */
+
+/* FP8 E4M3 quantization of x[rows, cols] (leading dim ldx >= cols) at one of
+ * four scale granularities ("量化部署实战", 伪量化实现: fp8_per_tensor,
+ * fp8_per_row, fp8_blockwise with (128,128) for weights and (1,128) for
+ * activations; 格式速查: FP8 E4M3 row):
+ *   scale = max(amax_unit, 1e-12) / 448;  code = E4M3(clamp(x / scale, +-448))
+ *   dequant = E4M3value(code) * scale    (fp32, one rounding)
+ * codes:   [rows, cols] bytes, dense.
+ * scales:  fp32, shape per qz_fp8_gran.
+ * dequant: nullable; fp32 [rows, cols], dense.
+ * ws:      PER_TENSOR needs qz_workspace_size(QZ_OP_QUANTIZE_FP8, rows, cols, 0)
+ *          bytes; the other granularities need none (ws may be NULL).
+ * Shapes:  BLOCK_128x128 needs cols % 128 == 0 and rows % min(128, rows) == 0;
+ *          GROUP_1x128 needs cols % 128 == 0. rows == 0 or cols == 0 is a no-op
+ *          returning QZ_OK, except PER_TENSOR (amax undefined) -> QZ_ERR_SHAPE.
+ * Alignment: x 16-byte aligned with ldx*elemsize % 16 == 0 and cols % 8 == 0
+ *          give the vector path; PER_TENSOR and PER_ROW also accept any other
+ *          x/ldx/cols (scalar path). BLOCK/GROUP require the vector conditions
+ *          (QZ_ERR_ALIGNMENT), and codes/dequant must then be 8/16-byte aligned. */
+qz_status qz_quantize_fp8(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                          qz_fp8_gran gran, uint8_t* codes, float* scales, float* dequant,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* MXFP4 quantization, one power-of-two (E8M0) scale per 32 consecutive
+ * elements of a row ("量化部署实战", 伪量化实现: mxfp4; "量化：让每一步搬更少的
+ * 字节", 新一代低位格式: MXFP4):
+ *   E = floor(log2(max(amax32, 1e-12))) (exact, from the exponent field)
+ *   scale = 2^(E-2); scale_e8m0 = E - 2 + 127
+ *   code = E2M1(clamp(x / scale, +-6));  dequant = E2M1value(code) * scale
+ * codes: [rows, cols/2] bytes (even element in the low nibble).
+ * scale_e8m0: [rows, cols/32] bytes. dequant: nullable fp32 [rows, cols].
+ * Shapes: cols % 32 == 0. Alignment: x 16 B, ldx*elemsize % 16 == 0, codes 4 B,
+ * dequant 16 B. rows == 0 is a no-op. No workspace. */
+qz_status qz_quantize_mxfp4(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t* codes, uint8_t* scale_e8m0, float* dequant, void* stream);
+
+/* NVFP4 quantization, one E4M3 scale per 16 consecutive elements of a row
+ * plus one fp32 scale per tensor ("量化部署实战", 伪量化实现: nvfp4;
+ * 格式速查: NVFP4 row), in the page's order:
+ *   g = max(amax_tensor, 1e-12) / (448 * 6)         -> *global_scale
+ *   b = E4M3(amax16 / 6 / g)                         -> scale_e4m3
+ *   s = max(E4M3value(b), 1e-12) * g
+ *   code = E2M1(clamp(x / s, +-6));  dequant = E2M1value(code) * s
+ * global_amax_in: nullable device pointer; when given, its value replaces the
+ *   computed tensor amax (calibrated or shared across slices) and no
+ *   workspace is needed.
+ * codes: [rows, cols/2]; scale_e4m3: [rows, cols/16]; global_scale: 1 fp32.
+ * ws: qz_workspace_size(QZ_OP_QUANTIZE_NVFP4, rows, cols, 0) bytes when
+ *   global_amax_in is NULL. Shapes: cols % 16 == 0; rows == 0 -> QZ_ERR_SHAPE
+ *   unless global_amax_in is given (then a no-op). Alignment as MXFP4. */
+qz_status qz_quantize_nvfp4(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t* codes, uint8_t* scale_e4m3, float* global_scale,
+                            const float* global_amax_in, float* dequant,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Symmetric INT4 weight quantization with one bf16 scale per group of 128
+ * along K, for a row-major weight w[K, N] (leading dim ldw >= N)
+ * ("量化部署实战", 格式速查: W4A16 row, integers -8..7 with a scale per 128;
+ * "量化：让每一步搬更少的字节", 量化在做什么: q = round(x / s), x^ = q * s;
+ * "LLM 推理优化 · 量化学习笔记" 5.1: q = clamp(round(x / s), qmin, qmax)):
+ *   s = bf16_rne(max(amax_group, 1e-12) / 7);  q = clamp(rint(w / s), -8, 7)
+ * qweight: int32 [K/8, N]; element k of column n sits in bits 4*(k%8)..+3 of
+ *   qweight[k/8][n], two's complement.
+ * scale_bf16: [K/128, N] bf16 bits. dequant: nullable fp32 [K, N] = q * s.
+ * Shapes: K % 128 == 0, N % 64 == 0. Alignment: w 16 B, ldw*elemsize % 16 == 0,
+ * qweight and dequant 16 B, scale_bf16 16 B. K == 0 or N == 0 is a no-op. */
+qz_status qz_quantize_int4_g128(const void* w, qz_dtype wt, int64_t K, int64_t N, int64_t ldw,
+                                int32_t* qweight, uint16_t* scale_bf16, float* dequant,
+                                void* stream);
+
+/* FP8 KV-cache write: per-tensor E4M3 quantization of K and of V, each with
+ * its own scale ("量化部署实战", 伪量化实现: FP8KVCache.update applies
+ * fp8_per_tensor to k and to v; KV Cache 量化: calibrated offline scales).
+ * k, v: bf16 [B, H, T, D] contiguous (n = B*H*T*D elements each).
+ * k_codes, v_codes: n bytes each. k_scale, v_scale: one fp32 each (device).
+ * mode COMPUTE: scales = max(amax, 1e-12) / 448 written to k_scale/v_scale;
+ *   needs qz_workspace_size(QZ_OP_KV_WRITE_FP8, n, 0, 0) bytes.
+ * mode GIVEN: k_scale/v_scale are read (must be finite and > 0); no workspace.
+ * Alignment: k, v 16 B; codes 8 B. n == 0 -> QZ_ERR_SHAPE (COMPUTE), no-op (GIVEN). */
+qz_status qz_kv_write_fp8(const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
+                          uint8_t* k_codes, uint8_t* v_codes, float* k_scale, float* v_scale,
+                          qz_scale_mode mode, void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- GEMMs */
+
+/* W4A16 GEMM ("量化：让每一步搬更少的字节", 路线一: one kernel that fuses the
+ * INT4 unpack, the dequantization and the matrix product):
+ *   Y[m, n] = bf16_rne( sum_g s[g, n] * sum_{k in g} A[m, k] * q[k, n] )
+ * accumulated in fp32. A: bf16 [M, K] row-major. qweight, scale_bf16: the
+ * layouts written by qz_quantize_int4_g128. Y: bf16 [M, N].
+ * Shapes: 1 <= M <= 64, K % 128 == 0, N % 64 == 0.
+ * Alignment: all pointers 16 B. ws: qz_workspace_size(QZ_OP_GEMM_W4A16, M, N, K). */
+qz_status qz_gemm_w4a16(const uint16_t* A, const int32_t* qweight, const uint16_t* scale_bf16,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+/* One W4A16 problem of a grouped launch (all pointers device, layouts as in
+ * qz_gemm_w4a16). */
+typedef struct qz_w4a16_problem {
+    const uint16_t* A;
+    const int32_t* qweight;
+    const uint16_t* scale_bf16;
+    uint16_t* Y;
+    int M, N, K;
+} qz_w4a16_problem;
+
+/* Runs `count` independent W4A16 problems in one launch (a decoder step's
+ * linears, whose inputs are all ready). Each problem obeys the rules of
+ * qz_gemm_w4a16. count <= 256. ws: qz_workspace_size(QZ_OP_GEMM_W4A16, Mmax,
+ * sum of N, Kmax) bytes suffices. */
+qz_status qz_gemm_w4a16_grouped(const qz_w4a16_problem* problems, int count,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* FP8 block-scaled GEMM ("量化部署实战", 练习 2: inside each 128-wide K block
+ * the tensor cores multiply-accumulate FP8, then the partial sum is multiplied
+ * by that block's activation and weight scales and added into the fp32 result):
+ *   Y[i, j] = bf16_rne( sum_kb sA[i, kb] * sB[j/128, kb] * sum_{k in kb} qA[i,k] * qB[j,k] )
+ * qA: E4M3 [M, K] (1x128 groups, as written by qz_quantize_fp8 GROUP_1x128);
+ * sA: fp32 [M, K/128]. qB: E4M3 [N, K] = B^T, K-major (128x128 blocks, as
+ * written by qz_quantize_fp8 BLOCK_128x128 on B^T); sB: fp32 [N/128, K/128].
+ * Y: bf16 [M, N]. Shapes: M % 128 == 0, N % 256 == 0, K % 128 == 0, K >= 128.
+ * Alignment: all pointers 16 B. */
+qz_status qz_gemm_fp8_block(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                            uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+/* NVFP4 GEMM (Blackwell FP4 tensor cores; "量化部署实战", 格式速查: NVFP4):
+ *   Y[i, j] = bf16_rne( gA * gB * sum_b sA[i,b] * sB[j,b] * sum_{k in b} qA[i,k] * qB[j,k] )
+ * qA: [M, K/2] packed E2M1, sA: E4M3 [M, K/16], gA: fp32 device scalar;
+ * qB, sB, gB likewise for B^T [N, K]; layouts as written by qz_quantize_nvfp4.
+ * Y: bf16 [M, N]. Shapes: M % 128 == 0, N % 256 == 0, K % 256 == 0.
+ * Alignment: all pointers 16 B. */
+qz_status qz_gemm_nvfp4(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                        const uint8_t* qB, const uint8_t* sB, const float* gB,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+/* MXFP4 GEMM: Y[i, j] = bf16_rne( sum_b 2^(eA[i,b]-127) * 2^(eB[j,b]-127) *
+ * sum_{k in b} qA[i,k] * qB[j,k] ), blocks of 32 along K. Layouts as written by
+ * qz_quantize_mxfp4 on A [M, K] and B^T [N, K]. Shapes and alignment as NVFP4. */
+qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
+                        uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QZ_H */

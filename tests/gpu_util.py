@@ -1,0 +1,42 @@
+"""Helpers shared by the GPU parity tests: host <-> device transfers of the
+seeded inputs and bit-level comparisons. No quantization arithmetic here."""
+import numpy as np
+import torch
+
+
+def dev_f32(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_u8(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, np.uint8)).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    """Device tensor -> numpy, keeping bit patterns (bf16 -> uint16)."""
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def bits32(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, np.float32).view(np.uint32)
+
+
+def assert_same_bytes(gpu: np.ndarray, ref: np.ndarray, what: str):
+    gpu, ref = np.asarray(gpu), np.asarray(ref)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    if gpu.dtype == np.float32:
+        gpu, ref = bits32(gpu), bits32(ref)
+    bad = np.argwhere(gpu != ref)
+    assert bad.size == 0, f"{what}: {len(bad)} mismatches, first at {bad[:5].tolist()}: " \
+                          f"gpu {gpu[tuple(bad[0])]!r} ref {ref[tuple(bad[0])]!r}"
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -1,0 +1,122 @@
+"""The C ABI on the host (no GPU needed): libqz.so loads, exports every function
+include/qz.h declares, sizes workspaces, and rejects invalid calls during host
+validation, before anything could reach a GPU. Every call below carries at least
+one invalid argument, so none of them can launch a kernel on any machine."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "qz.h")
+
+
+def _lib():
+    from bit_quantized_linear_quantizers_gb300 import _build
+    _build.build()
+    return ctypes.CDLL(_build.LIB)
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qz_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4", "qz_quantize_int4_g128",
+                     "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_fp8_block", "qz_gemm_nvfp4",
+                     "qz_gemm_mxfp4", "qz_workspace_size", "qz_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+@pytest.fixture(scope="module")
+def qz():
+    import bit_quantized_linear_quantizers_gb300 as q
+    return q
+
+
+def test_status_strings(qz):
+    assert qz.qz_status_string(0) == "QZ_OK"
+    for s in range(1, 8):
+        assert qz.qz_status_string(s).startswith("QZ_ERR_")
+
+
+def test_workspace_sizes(qz):
+    assert qz.qz_workspace_size(qz.OP_QUANTIZE_FP8, 1024, 1024, qz.FP8_PER_TENSOR) > 0
+    assert qz.qz_workspace_size(qz.OP_QUANTIZE_FP8, 1024, 1024, qz.FP8_PER_ROW) == 0
+    assert qz.qz_workspace_size(qz.OP_KV_WRITE_FP8, 1 << 22) >= 2 * 4
+    assert qz.qz_workspace_size(qz.OP_GEMM_W4A16, 16, 14336, 4096) == 0
+    assert qz.qz_workspace_size(99, 1, 1, 1) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)        # aligned, never dereferenced: validation fails first
+ODD = ctypes.c_void_p(0x10001)
+NULL = None
+
+
+@pytest.mark.parametrize("args,expect", [
+    # x, dtype, rows, cols, ldx, gran, codes, scales, deq, ws, ws_bytes, stream
+    ((FAKE, 0, 4, 128, 128, 9, FAKE, FAKE, NULL, NULL, 0, NULL), 1),        # bad granularity
+    ((FAKE, 7, 4, 128, 128, 1, FAKE, FAKE, NULL, NULL, 0, NULL), 1),        # bad dtype
+    ((FAKE, 0, 4, 128, 64, 1, FAKE, FAKE, NULL, NULL, 0, NULL), 1),         # ldx < cols
+    ((NULL, 0, 4, 128, 128, 1, FAKE, FAKE, NULL, NULL, 0, NULL), 1),        # null x
+    ((FAKE, 0, 4, 100, 100, 3, FAKE, FAKE, NULL, NULL, 0, NULL), 2),        # 1x128 needs cols % 128
+    ((FAKE, 0, 200, 128, 128, 2, FAKE, FAKE, NULL, NULL, 0, NULL), 2),      # 128x128 needs rows % 128
+    ((ODD, 0, 4, 128, 128, 3, FAKE, FAKE, NULL, NULL, 0, NULL), 3),         # misaligned x, group path
+    ((FAKE, 0, 4, 128, 128, 0, FAKE, FAKE, NULL, NULL, 0, NULL), 7),        # per-tensor without ws
+    ((FAKE, 0, 0, 128, 128, 0, FAKE, FAKE, NULL, NULL, 0, NULL), 2),        # empty per-tensor
+])
+def test_quantize_fp8_validation(qz, args, expect):
+    assert qz.lib.qz_quantize_fp8(*args) == expect
+
+
+def test_empty_inputs_are_noops(qz):
+    # rows == 0: nothing to do, no device touched (pointers are fake)
+    assert qz.lib.qz_quantize_fp8(FAKE, 0, 0, 128, 128, 1, FAKE, FAKE, NULL, NULL, 0, NULL) == 0
+    assert qz.lib.qz_quantize_mxfp4(FAKE, 0, 0, 64, 64, FAKE, FAKE, NULL, NULL) == 0
+    assert qz.lib.qz_quantize_int4_g128(FAKE, 0, 0, 64, 64, FAKE, FAKE, NULL, NULL) == 0
+    assert qz.lib.qz_kv_write_fp8(FAKE, FAKE, 0, 8, 16, 128, FAKE, FAKE, FAKE, FAKE, 1, NULL, 0, NULL) == 0
+
+
+def test_fp4_and_int4_validation(qz):
+    L = qz.lib
+    assert L.qz_quantize_mxfp4(FAKE, 0, 4, 48, 48, FAKE, FAKE, NULL, NULL) == 2          # cols % 32
+    assert L.qz_quantize_mxfp4(FAKE, 0, 4, 64, 63, FAKE, FAKE, NULL, NULL) == 1          # ldx < cols
+    assert L.qz_quantize_mxfp4(ODD, 0, 4, 64, 64, FAKE, FAKE, NULL, NULL) == 3
+    assert L.qz_quantize_nvfp4(FAKE, 0, 4, 24, 24, FAKE, FAKE, FAKE, NULL, NULL, NULL, 0, NULL) == 2
+    assert L.qz_quantize_nvfp4(FAKE, 0, 4, 32, 32, FAKE, FAKE, FAKE, NULL, NULL, NULL, 0, NULL) == 7
+    assert L.qz_quantize_nvfp4(FAKE, 0, 4, 32, 32, FAKE, FAKE, NULL, NULL, NULL, FAKE, 1 << 20, NULL) == 1
+    assert L.qz_quantize_int4_g128(FAKE, 0, 100, 64, 64, FAKE, FAKE, NULL, NULL) == 2    # K % 128
+    assert L.qz_quantize_int4_g128(FAKE, 0, 128, 40, 40, FAKE, FAKE, NULL, NULL) == 2    # N % 64
+    assert L.qz_kv_write_fp8(FAKE, FAKE, 1, 8, 16, 128, FAKE, FAKE, FAKE, FAKE, 5, NULL, 0, NULL) == 1
+    assert L.qz_kv_write_fp8(FAKE, FAKE, 1, 8, 16, 128, FAKE, FAKE, FAKE, FAKE, 0, NULL, 0, NULL) == 7
+    assert L.qz_kv_write_fp8(ODD, FAKE, 1, 8, 16, 128, FAKE, FAKE, FAKE, FAKE, 1, NULL, 0, NULL) == 3
+
+
+def test_gemm_validation(qz):
+    L = qz.lib
+    # A, qweight, scale, Y, M, N, K, ws, ws_bytes, stream
+    assert L.qz_gemm_w4a16(FAKE, FAKE, FAKE, FAKE, 65, 128, 128, NULL, 0, NULL) == 2     # M > 64
+    assert L.qz_gemm_w4a16(FAKE, FAKE, FAKE, FAKE, 4, 100, 128, NULL, 0, NULL) == 2      # N % 64
+    assert L.qz_gemm_w4a16(FAKE, FAKE, FAKE, FAKE, 4, 128, 96, NULL, 0, NULL) == 2       # K % 128
+    assert L.qz_gemm_w4a16(NULL, FAKE, FAKE, FAKE, 4, 128, 128, NULL, 0, NULL) == 1
+    assert L.qz_gemm_w4a16(ODD, FAKE, FAKE, FAKE, 4, 128, 128, NULL, 0, NULL) == 3
+    assert L.qz_gemm_w4a16(FAKE, FAKE, FAKE, FAKE, 0, 128, 128, NULL, 0, NULL) == 1
+    assert L.qz_gemm_w4a16_grouped(None, 0, NULL, 0, NULL) == 1
+    assert L.qz_gemm_fp8_block(FAKE, FAKE, FAKE, FAKE, FAKE, 100, 256, 128, NULL, 0, NULL) == 2
+    assert L.qz_gemm_fp8_block(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 100, NULL, 0, NULL) == 2
+    assert L.qz_gemm_fp8_block(FAKE, FAKE, NULL, FAKE, FAKE, 128, 256, 128, NULL, 0, NULL) == 1
+    assert L.qz_gemm_nvfp4(FAKE, FAKE, NULL, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 1
+    assert L.qz_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 200, 256, NULL, 0, NULL) == 2
+    assert L.qz_gemm_mxfp4(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 100, NULL, 0, NULL) == 2
+    assert L.qz_gemm_mxfp4(ODD, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 3
