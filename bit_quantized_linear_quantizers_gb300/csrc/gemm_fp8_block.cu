@@ -1,0 +1,221 @@
+// gemm_fp8_block.cu -- block-scaled FP8 GEMM for prefill on tcgen05:
+//   Y[i, j] = bf16( sum_kb sA[i, kb] * sB[j/128, kb] * sum_{k in kb} qA[i,k] qB[j,k] )
+// with E4M3 operands, 1x128 activation scales and 128x128 weight scales
+// ("量化部署实战", 练习 2: inside each 128-deep K block the tensor cores
+// multiply-accumulate FP8, the partial sum is then multiplied by that block's
+// activation and weight scales and added into the fp32 result).
+//
+// The fp32 block scales are not powers of two, so they cannot ride in the
+// tensor core's own block-scale path (E8M0 / UE4M3). Instead each 128-deep K
+// block is an independent tcgen05 MMA chain into a TMEM accumulator, and the
+// epilogue warps promote it on the CUDA cores: acc += P_kb * (sA * sB).
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//  warp 0      TMA producer: 128x128 A and 256x128 B boxes (128-byte swizzle)
+//              into a 4-stage shared-memory ring, mbarrier complete_tx.
+//  warp 1      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4
+//              (M=128, N=256, K=32) per K block into one of two TMEM
+//              accumulators (2 x 256 columns), committed to the stage's
+//              "empty" barrier and the accumulator's "full" barrier.
+//  warps 2-9   promotion + epilogue: each thread owns one output row and 128
+//              columns; per K block it loads its partial sums from TMEM
+//              (tcgen05.ld), multiplies by sA*sB and adds into fp32 registers,
+//              then frees the accumulator; at the end of the tile it rounds
+//              to bf16 and stores.
+// The MMA of K block kb+1 runs while block kb is being promoted.
+#include "qz_tc.cuh"
+
+#include <algorithm>
+
+namespace qz {
+
+namespace {
+
+__device__ unsigned int g_fp8_err;
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int A_BYTES = BM * BK;                  // 16 KB
+constexpr int B_BYTES = BN * BK;                  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+
+__global__ void __launch_bounds__(THREADS, 1)
+fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const float* __restrict__ sA, const float* __restrict__ sB, uint16_t* __restrict__ Y,
+                      int M, int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+    auto full = [&](int s) { return smem_u32(bars + s); };
+    auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+    auto tfull = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+    auto tempty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = M / BM, tiles = mt * (N / BN), nkb = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), EPI_WARPS);
+        }
+        fence_barrier_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+                for (int kb = 0; kb < nkb; kb++, it++) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(empty(s), ph ^ 1, &g_fp8_err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full(s), STAGE_BYTES);
+                    tma_load_2d(sbase + s * STAGE_BYTES, &tmA, kb * BK, m0, full(s));
+                    tma_load_2d(sbase + s * STAGE_BYTES + A_BYTES, &tmB, kb * BK, n0, full(s));
+                }
+            }
+            // every issued copy has landed before the CTA may exit
+            for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; j++)
+                mbar_wait(full(j % STAGES), (j / STAGES) & 1, &g_fp8_err);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, ac = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < nkb; kb++, it++, ac++) {
+                    const int b = ac & 1;
+                    if (!mbar_wait(tempty(b), ((ac >> 1) & 1) ^ 1, &g_fp8_err)) { ok = false; break; }
+                    tc_fence_after();
+                    const int s = it % STAGES;
+                    if (!mbar_wait(full(s), (it / STAGES) & 1, &g_fp8_err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(sbase + s * STAGE_BYTES);
+                    const uint64_t bd = sdesc_k_sw128(sbase + s * STAGE_BYTES + A_BYTES);
+                    const uint32_t d = tmem_base + b * BN;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 32; ks++)                 // K = 32 bytes per MMA
+                        mma_f8f6f4(d, ad + (uint64_t)(ks * 2), bd + (uint64_t)(ks * 2), IDESC, ks > 0);
+                    tc_commit(empty(s));
+                    tc_commit(tfull(b));
+                }
+            }
+            // the last accumulators are complete before TMEM is released
+            if (ac > 0) mbar_wait(tfull((ac - 1) & 1), ((ac - 1) >> 1) & 1, &g_fp8_err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------ promotion + epilogue warps
+        const int q = warp & 3;                   // TMEM lane quarter of this warp
+        const int h = (warp - 2) >> 2;            // column half of the 256-wide tile
+        const int r = q * 32 + lane;              // row within the tile
+        uint32_t ac = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+            const float* sa_row = sA + (size_t)(m0 + r) * nkb;
+            const float* sb_row = sB + (size_t)(n0 / 128 + h) * nkb;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+            float scale_next = __ldg(sa_row) * __ldg(sb_row);
+            for (int kb = 0; kb < nkb; kb++, ac++) {
+                const float scale = scale_next;
+                if (kb + 1 < nkb) scale_next = __ldg(sa_row + kb + 1) * __ldg(sb_row + kb + 1);
+                const int b = ac & 1;
+                if (!mbar_wait(tfull(b), (ac >> 1) & 1, &g_fp8_err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) acc[c * 32 + i] = fmaf(__uint_as_float(v[i]), scale, acc[c * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty(b));
+            }
+            if (!ok) break;
+            uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * 128);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                uint4 o;
+                uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    __nv_bfloat162 p = __floats2bfloat162_rn(acc[j * 8 + 2 * e], acc[j * 8 + 2 * e + 1]);
+                    w[e] = *reinterpret_cast<uint32_t*>(&p);
+                }
+                yrow[j] = o;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+} // namespace
+
+size_t ws_gemm_fp8_block(int, int, int) { return 0; }
+
+qz_status fp8_block_error_read_and_clear() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fp8_err, sizeof(v)) != cudaSuccess) return QZ_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_fp8_err, &z, sizeof(z)) != cudaSuccess) return QZ_ERR_CUDA;
+    return v ? QZ_ERR_TIMEOUT : QZ_OK;
+}
+
+qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                                uint16_t* Y, int M, int N, int K, void*, size_t, cudaStream_t st) {
+    CUtensorMap ta, tb;
+    if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM)) return QZ_ERR_CUDA;
+    if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN)) return QZ_ERR_CUDA;
+    static int attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(fp8_block_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return QZ_ERR_CUDA;
+        attr_set[dev] = 1;
+    }
+    const int tiles = (M / BM) * (N / BN);
+    const int grid = std::min(tiles, num_sms());
+    fp8_block_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, M, N, K);
+    return launch_status();
+}
+
+} // namespace qz

@@ -72,19 +72,19 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Byte b of an offset-binary word (two 4-bit codes u = q + 8) -> bf16x2
-// (q_even, q_odd). The low nibble lands in the low bf16's mantissa (value
-// 128 + u), the high nibble 4 bits higher in the high bf16 (128 + 16u); one
-// fma per half, (x * 1 - 136) and (x / 16 - 16), gives q exactly.
+// Byte B of an offset-binary word u (two 4-bit codes u = q + 8 per byte) ->
+// bf16x2 (q_even, q_odd). The even code comes from byte B of u, the odd code
+// from byte B of u >> 4 (u4); each lands in mantissa bits 0-3 of its bf16
+// half (value 128 + u), and one fma (x * 1 - 136) gives q exactly.
 template <int B>
-__device__ __forceinline__ uint32_t nib_pair(uint32_t u) {
-    const uint32_t r = __byte_perm(u, 0u, B * 0x1111u);
+__device__ __forceinline__ uint32_t nib_pair(uint32_t u, uint32_t u4) {
+    const uint32_t r = __byte_perm(u, u4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
     uint32_t v;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(r), "r"(0x00F0000Fu), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43004300u));
     uint32_t out;
-    const uint32_t mul = 0x3D803F80u;    // bf16x2 (lo 1.0, hi 0.0625)
-    const uint32_t add = 0xC180C308u;    // bf16x2 (lo -136.0, hi -16.0)
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out) : "r"(v), "r"(mul), "r"(add));
+    const uint32_t one = 0x3F803F80u;    // bf16x2 (1.0, 1.0)
+    const uint32_t add = 0xC308C308u;    // bf16x2 (-136.0, -136.0)
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out) : "r"(v), "r"(one), "r"(add));
     return out;
 }
 
@@ -178,8 +178,11 @@ w4a16_kernel(const __grid_constant__ Params P, int nt_max, int ns) {
                         const uint32_t* wr = w + (size_t)(4 * j + t) * (nt_max + WPAD) + warp * 16 + g;
                         const uint32_t u0 = wr[0] ^ 0x88888888u;         // column n
                         const uint32_t u1 = wr[8] ^ 0x88888888u;         // column n + 8
-                        const uint32_t f0[4] = {nib_pair<0>(u0), nib_pair<0>(u1), nib_pair<1>(u0), nib_pair<1>(u1)};
-                        const uint32_t f1[4] = {nib_pair<2>(u0), nib_pair<2>(u1), nib_pair<3>(u0), nib_pair<3>(u1)};
+                        const uint32_t v0 = u0 >> 4, v1 = u1 >> 4;
+                        const uint32_t f0[4] = {nib_pair<0>(u0, v0), nib_pair<0>(u1, v1), nib_pair<1>(u0, v0),
+                                                nib_pair<1>(u1, v1)};
+                        const uint32_t f1[4] = {nib_pair<2>(u0, v0), nib_pair<2>(u1, v1), nib_pair<3>(u0, v0),
+                                                nib_pair<3>(u1, v1)};
 #pragma unroll
                         for (int mb = 0; mb < MB; mb++) {
                             const uint4 b = *reinterpret_cast<const uint4*>(a + (mb * 8 + g) * AROW + (32 * j + 8 * t) * 2);

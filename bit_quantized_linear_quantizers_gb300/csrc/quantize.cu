@@ -49,44 +49,52 @@ __device__ __forceinline__ float fp8_scale(float amax) {
     return div_rn(fmaxf(amax, kAmaxMin), kFp8Max);
 }
 
-// Encode 8 values; write 8 code bytes (and 8 dequantized floats).
-__device__ __forceinline__ void fp8_encode8(const float v[8], float s, uint8_t* codes, float* deq) {
-    uint32_t c[8];
+// Encode 8 values with scale d.s; write 8 code bytes (and 8 dequantized
+// floats). The quotients are correctly rounded (Recip), the E4M3 conversion
+// is the hardware's round-to-nearest-even, saturating at +-448 (the clamp).
+__device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, uint8_t* codes, float* deq) {
+    float y[8];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
-        float y0 = fminf(fmaxf(div_rn(v[j], s), -kFp8Max), kFp8Max);
-        float y1 = fminf(fmaxf(div_rn(v[j + 1], s), -kFp8Max), kFp8Max);
-        uint32_t p = e4m3x2(y0, y1);
-        c[j] = p & 0xFF;
-        c[j + 1] = p >> 8;
+        y[j] = v[j];
+        y[j + 1] = v[j + 1];
+        div2(y[j], y[j + 1], d);
+        y[j] = sign_of(y[j], v[j]);
+        y[j + 1] = sign_of(y[j + 1], v[j + 1]);
     }
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) p[j] = e4m3x2(y[2 * j], y[2 * j + 1]);
     uint2 out;
-    out.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-    out.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    out.x = __byte_perm(p[0], p[1], 0x5410);
+    out.y = __byte_perm(p[2], p[3], 0x5410);
     *reinterpret_cast<uint2*>(codes) = out;
     if (deq) {
-        float d[8];
+        float o[8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) d[j] = __fmul_rn(e4m3_value(c[j]), s);
-        reinterpret_cast<float4*>(deq)[0] = make_float4(d[0], d[1], d[2], d[3]);
-        reinterpret_cast<float4*>(deq)[1] = make_float4(d[4], d[5], d[6], d[7]);
+        for (int j = 0; j < 8; j++) o[j] = __fmul_rn(e4m3_value((j & 1) ? (p[j >> 1] >> 8) : p[j >> 1]), d.s);
+        reinterpret_cast<float4*>(deq)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(deq)[1] = make_float4(o[4], o[5], o[6], o[7]);
     }
 }
 
-// Encode 8 values to E2M1 with scale s (division exact); returns 8 nibbles,
-// element j at bits 4j..4j+3. Writes dequant if requested.
-__device__ __forceinline__ uint32_t fp4_encode8(const float v[8], float s, float* deq) {
-    uint32_t packed = 0;
-    float d[8];
+// Encode 8 values to E2M1 with scale d.s (correctly rounded quotients);
+// returns 8 nibbles, element j at bits 4j..4j+3; writes dequant if asked.
+__device__ __forceinline__ uint32_t fp4_encode8(const float v[8], const Recip& d, float* deq) {
+    float y[8];
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        uint32_t c = e2m1_code(div_rn(v[j], s));
-        packed |= c << (4 * j);
-        d[j] = __fmul_rn(e2m1_value(c), s);
+    for (int j = 0; j < 8; j += 2) {
+        y[j] = v[j];
+        y[j + 1] = v[j + 1];
+        div2(y[j], y[j + 1], d);
     }
+    const uint32_t packed = e2m1x8(y);
     if (deq) {
-        reinterpret_cast<float4*>(deq)[0] = make_float4(d[0], d[1], d[2], d[3]);
-        reinterpret_cast<float4*>(deq)[1] = make_float4(d[4], d[5], d[6], d[7]);
+        float o[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) o[j] = __fmul_rn(e2m1_value(packed >> (4 * j)), d.s);
+        reinterpret_cast<float4*>(deq)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(deq)[1] = make_float4(o[4], o[5], o[6], o[7]);
     }
     return packed;
 }
@@ -100,11 +108,15 @@ __device__ __forceinline__ int64_t chunk_offset(int64_t i, bool contig, int64_t 
     return r * ldx + (i - r * cpr) * E;
 }
 
+// Loads per thread kept in flight by the streaming kernels.
+constexpr int U = 4;
+
 // ------------------------------------------------------ per-tensor amax
 
 // Kernel 1 of a per-tensor reduction: partial[y * gridDim.x + blockIdx.x] =
 // max |x_y| over this CTA's grid-stride share of tensor y (y = blockIdx.y,
-// at most two tensors, for K and V).
+// at most two tensors, for K and V). U chunks per thread are loaded before
+// any is reduced.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 amax_partial_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t rows, int64_t cols,
@@ -115,15 +127,25 @@ amax_partial_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t 
     const int64_t total = rows * cpr;
     float m = 0.0f;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += stride) {
-        const int64_t off = chunk_offset<VEC>(i, contig, cpr, ldx);
+    for (int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; i0 < total; i0 += U * stride) {
         if constexpr (VEC) {
-            float v[8];
-            Load8<T>::run(x + off, v);
+            float v[U][8];
 #pragma unroll
-            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+            for (int u = 0; u < U; u++) {
+                const int64_t i = i0 + u * stride;
+                if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
+                else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++)
+#pragma unroll
+                for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
         } else {
-            m = fmaxf(m, fabsf(load1(x + off)));
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t i = i0 + u * stride;
+                if (i < total) m = fmaxf(m, fabsf(load1(x + chunk_offset<false>(i, contig, cpr, ldx))));
+            }
         }
     }
     m = block_max(m, red);
@@ -137,48 +159,82 @@ __device__ __forceinline__ float reduce_partials(const float* __restrict__ p, in
 }
 
 // Kernel 2 of per-tensor FP8: every CTA reduces the partials to the tensor
-// amax (or reads a given scale), then encodes its grid-stride share.
-template <typename T, bool VEC>
+// amax (or reads a caller-given scale, GIVEN), then encodes its grid-stride
+// share. A given scale may make x / s overflow, so that path divides exactly
+// per element and clamps as the fake-quant does.
+template <typename T, bool VEC, bool GIVEN>
 __global__ void __launch_bounds__(kThreads)
 fp8_tensor_encode_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t rows, int64_t cols,
                          int64_t ldx, bool contig, const float* __restrict__ partial, int nparts,
-                         const float* __restrict__ given0, const float* __restrict__ given1,
-                         uint8_t* __restrict__ c0, uint8_t* __restrict__ c1,
-                         float* __restrict__ s0, float* __restrict__ s1,
-                         float* __restrict__ d0, float* __restrict__ d1) {
+                         const float* given0, const float* given1, uint8_t* __restrict__ c0,
+                         uint8_t* __restrict__ c1, float* s0, float* s1, float* __restrict__ d0,
+                         float* __restrict__ d1) {
     __shared__ float red[kWarps];
     const int y = blockIdx.y;
     const T* x = y ? x1 : x0;
     uint8_t* codes = y ? c1 : c0;
     float* deq = y ? d1 : d0;
     float s;
-    if (partial) {
+    if (!GIVEN) {
         s = fp8_scale(reduce_partials(partial + (int64_t)y * nparts, nparts, red));
         if (blockIdx.x == 0 && threadIdx.x == 0) *(y ? s1 : s0) = s;
     } else {
         s = __ldg(y ? given1 : given0);
     }
+    const Recip d(s);
     const int64_t cpr = VEC ? cols / 8 : cols;
     const int64_t total = rows * cpr;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += stride) {
-        const int64_t off = chunk_offset<VEC>(i, contig, cpr, ldx);
+    for (int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; i0 < total; i0 += 2 * stride) {
         if constexpr (VEC) {
-            float v[8];
-            Load8<T>::run(x + off, v);
-            fp8_encode8(v, s, codes + i * 8, deq ? deq + i * 8 : nullptr);
+            float v[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int64_t i = i0 + u * stride;
+                if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int64_t i = i0 + u * stride;
+                if (i >= total) continue;
+                if (GIVEN) {
+                    uint8_t cb[8];
+                    float o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const uint32_t c = fp8_code(v[u][j], s);
+                        cb[j] = (uint8_t)c;
+                        o[j] = __fmul_rn(e4m3_value(c), s);
+                    }
+                    uint2 w;
+                    w.x = cb[0] | (cb[1] << 8) | (cb[2] << 16) | ((uint32_t)cb[3] << 24);
+                    w.y = cb[4] | (cb[5] << 8) | (cb[6] << 16) | ((uint32_t)cb[7] << 24);
+                    *reinterpret_cast<uint2*>(codes + i * 8) = w;
+                    if (deq) {
+                        reinterpret_cast<float4*>(deq + i * 8)[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        reinterpret_cast<float4*>(deq + i * 8)[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    }
+                } else {
+                    fp8_encode8(v[u], d, codes + i * 8, deq ? deq + i * 8 : nullptr);
+                }
+            }
         } else {
-            const uint32_t c = fp8_code(load1(x + off), s);
-            codes[i] = (uint8_t)c;
-            if (deq) deq[i] = __fmul_rn(e4m3_value(c), s);
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int64_t i = i0 + u * stride;
+                if (i >= total) continue;
+                const uint32_t c = fp8_code(load1(x + chunk_offset<false>(i, contig, cpr, ldx)), s);
+                codes[i] = (uint8_t)c;
+                if (deq) deq[i] = __fmul_rn(e4m3_value(c), s);
+            }
         }
     }
 }
 
 // ---------------------------------------------------------- per row
 
-// One warp per row: pass 1 reduces the row's amax, pass 2 re-reads the row
-// (from L1/L2) and encodes it.
+// One warp per row: pass 1 reduces the row's amax (U loads in flight per
+// lane), pass 2 re-reads the row (from L1/L2) and encodes it.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 fp8_row_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
@@ -190,11 +246,17 @@ fp8_row_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
         const T* xr = x + r * ldx;
         float m = 0.0f;
         if constexpr (VEC) {
-            for (int64_t c = lane * 8; c < cols; c += 256) {
-                float v[8];
-                Load8<T>::run(xr + c, v);
+            for (int64_t c0 = lane * 8; c0 < cols; c0 += U * 256) {
+                float v[U][8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+                for (int u = 0; u < U; u++) {
+                    if (c0 + u * 256 < cols) Load8<T>::run(xr + c0 + u * 256, v[u]);
+                    else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; u++)
+#pragma unroll
+                    for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
             }
         } else {
             for (int64_t c = lane; c < cols; c += 32) m = fmaxf(m, fabsf(load1(xr + c)));
@@ -204,10 +266,17 @@ fp8_row_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
         uint8_t* cr = codes + r * cols;
         float* dr = deq ? deq + r * cols : nullptr;
         if constexpr (VEC) {
-            for (int64_t c = lane * 8; c < cols; c += 256) {
-                float v[8];
-                Load8<T>::run(xr + c, v);
-                fp8_encode8(v, s, cr + c, dr ? dr + c : nullptr);
+            const Recip d(s);
+            for (int64_t c0 = lane * 8; c0 < cols; c0 += 2 * 256) {
+                float v[2][8];
+#pragma unroll
+                for (int u = 0; u < 2; u++)
+                    if (c0 + u * 256 < cols) Load8<T>::run(xr + c0 + u * 256, v[u]);
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                    const int64_t c = c0 + u * 256;
+                    if (c < cols) fp8_encode8(v[u], d, cr + c, dr ? dr + c : nullptr);
+                }
             }
         } else {
             for (int64_t c = lane; c < cols; c += 32) {
@@ -222,7 +291,8 @@ fp8_row_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
 // ------------------------------------------------------- 1 x 128 groups
 
 // 16 threads per 128-element group (8 elements each); a warp covers two
-// groups. Loops run warp-uniformly so the shuffles always see 32 lanes.
+// groups per step and takes two steps at once. Loops run warp-uniformly so
+// the shuffles always see 32 lanes.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fp8_group_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, bool contig,
@@ -230,20 +300,27 @@ fp8_group_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
     for (int64_t base = wbase; base < total; base += wstride) {
-        const int64_t i = base + lane;
-        const bool ok = i < total;
-        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
-        float m = 0.0f;
+        float v[2][8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
-        const float s = fp8_scale(warp_max(m, 16));
-        if (ok) {
-            if ((lane & 15) == 0) scales[i >> 4] = s;
-            fp8_encode8(v, s, codes + i * 8, deq ? deq + i * 8 : nullptr);
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
+            else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+            const float s = fp8_scale(warp_max(m, 16));
+            if (i < total) {
+                if ((lane & 15) == 0) scales[i >> 4] = s;
+                fp8_encode8(v[u], Recip(s), codes + i * 8, deq ? deq + i * 8 : nullptr);
+            }
         }
     }
 }
@@ -251,7 +328,32 @@ fp8_group_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld
 // ----------------------------------------------------- 128 x 128 blocks
 
 // One CTA per (br x 128) block, br = min(128, rows); the block stays in
-// registers (up to 8 chunks of 8 values per thread) between amax and encode.
+// registers in its input format (up to 8 chunks per thread) between the
+// amax reduction and the encode.
+template <typename T> struct Raw8;
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = __ldg(reinterpret_cast<const float4*>(p));
+        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void unpack(float v[8]) const {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+template <> struct Raw8<uint16_t> {
+    uint4 a;
+    __device__ __forceinline__ void load(const uint16_t* p) { a = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ void unpack(float v[8]) const {
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fp8_block_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, int br,
@@ -260,26 +362,34 @@ fp8_block_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld
     const int64_t nbc = cols / 128;
     const int64_t bi = blockIdx.x / nbc, bj = blockIdx.x % nbc;
     const int nchunks = br * 16;
-    float v[8][8];
+    Raw8<T> raw[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const int j = threadIdx.x + u * kThreads;
+        if (j < nchunks) raw[u].load(x + (bi * br + (j >> 4)) * ldx + bj * 128 + (j & 15) * 8);
+    }
     float m = 0.0f;
 #pragma unroll
     for (int u = 0; u < 8; u++) {
         const int j = threadIdx.x + u * kThreads;
         if (j < nchunks) {
-            const int64_t r = bi * br + (j >> 4), c = bj * 128 + (j & 15) * 8;
-            Load8<T>::run(x + r * ldx + c, v[u]);
+            float v[8];
+            raw[u].unpack(v);
 #pragma unroll
-            for (int e = 0; e < 8; e++) m = fmaxf(m, fabsf(v[u][e]));
+            for (int e = 0; e < 8; e++) m = fmaxf(m, fabsf(v[e]));
         }
     }
     const float s = fp8_scale(block_max(m, red));
     if (threadIdx.x == 0) scales[blockIdx.x] = s;
+    const Recip d(s);
 #pragma unroll
     for (int u = 0; u < 8; u++) {
         const int j = threadIdx.x + u * kThreads;
         if (j < nchunks) {
             const int64_t r = bi * br + (j >> 4), c = bj * 128 + (j & 15) * 8;
-            fp8_encode8(v[u], s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
+            float v[8];
+            raw[u].unpack(v);
+            fp8_encode8(v, d, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
         }
     }
 }
@@ -295,35 +405,41 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
     for (int64_t base = wbase; base < total; base += wstride) {
-        const int64_t i = base + lane;
-        const bool ok = i < total;
-        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
-        float m = 0.0f;
+        float v[2][8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
-        m = fmaxf(warp_max(m, 4), kAmaxMin);
-        const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;   // m is normal
-        const float s = __uint_as_float((uint32_t)(E - 2 + 127) << 23);
-        const float inv = __uint_as_float((uint32_t)(127 + 2 - E) << 23);
-        if (ok) {
-            uint32_t packed = 0;
-            float d[8];
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
+            else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+        }
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t c = e2m1_code(__fmul_rn(v[j], inv));
-                packed |= c << (4 * j);
-                d[j] = __fmul_rn(e2m1_value(c), s);
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+            m = fmaxf(warp_max(m, 4), kAmaxMin);
+            const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;   // m is normal
+            const float sc = __uint_as_float((uint32_t)(E - 2 + 127) << 23);
+            const float inv = __uint_as_float((uint32_t)(127 + 2 - E) << 23);
+            if (i < total) {
+                float y[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) y[j] = __fmul_rn(v[u][j], inv);
+                const uint32_t packed = e2m1x8(y);
+                reinterpret_cast<uint32_t*>(codes)[i] = packed;
+                if (deq) {
+                    float o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) o[j] = __fmul_rn(e2m1_value(packed >> (4 * j)), sc);
+                    reinterpret_cast<float4*>(deq + i * 8)[0] = make_float4(o[0], o[1], o[2], o[3]);
+                    reinterpret_cast<float4*>(deq + i * 8)[1] = make_float4(o[4], o[5], o[6], o[7]);
+                }
+                if ((lane & 3) == 0) e8m0[i >> 2] = (uint8_t)(E - 2 + 127);
             }
-            reinterpret_cast<uint32_t*>(codes)[i] = packed;
-            if (deq) {
-                reinterpret_cast<float4*>(deq + i * 8)[0] = make_float4(d[0], d[1], d[2], d[3]);
-                reinterpret_cast<float4*>(deq + i * 8)[1] = make_float4(d[4], d[5], d[6], d[7]);
-            }
-            if ((lane & 3) == 0) e8m0[i >> 2] = (uint8_t)(E - 2 + 127);
         }
     }
 }
@@ -342,29 +458,39 @@ nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
     const float amax_t = partial ? reduce_partials(partial, nparts, red) : __ldg(amax_in);
     const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    const Recip dg(g);
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
     for (int64_t base = wbase; base < total; base += wstride) {
-        const int64_t i = base + lane;
-        const bool ok = i < total;
-        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (ok) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v);
-        float m = 0.0f;
+        float v[2][8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
-        m = warp_max(m, 2);
-        const float t = div_rn(div_rn(m, kFp4Max), g);
-        const uint32_t bcode = e4m3_code(t);                 // saturating, as the clamp-free page
-        const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
-        if (ok) {
-            const uint32_t packed = fp4_encode8(v, s, deq ? deq + i * 8 : nullptr);
-            reinterpret_cast<uint32_t*>(codes)[i] = packed;
-            if ((lane & 1) == 0) sb[i >> 1] = (uint8_t)bcode;
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
+            else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t i = base + u * 32 + lane;
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+            m = warp_max(m, 2);
+            // t = (amax16 / 6) / g, both divisions correctly rounded
+            const float t = div_rn(div_rn(m, kFp4Max), g);
+            const uint32_t bcode = e4m3_code(t);                 // saturating, as the clamp-free page
+            const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
+            if (i < total) {
+                const uint32_t packed = fp4_encode8(v[u], Recip(s), deq ? deq + i * 8 : nullptr);
+                reinterpret_cast<uint32_t*>(codes)[i] = packed;
+                if ((lane & 1) == 0) sb[i >> 1] = (uint8_t)bcode;
+            }
         }
     }
+    (void)dg;
 }
 
 // --------------------------------------------------------------- INT4 g128
@@ -467,12 +593,12 @@ static qz_status fp8_launch_t(const T* x, int64_t rows, int64_t cols, int64_t ld
         const int64_t work = vec ? rows * cols / 8 : rows * cols;
         if (vec) {
             launch_tensor_amax<T, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-            fp8_tensor_encode_kernel<T, true><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
+            fp8_tensor_encode_kernel<T, true, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
                 x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
                 scales, deq, deq);
         } else {
             launch_tensor_amax<T, false>(x, x, 1, rows, cols, ldx, contig, partial, st);
-            fp8_tensor_encode_kernel<T, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
+            fp8_tensor_encode_kernel<T, false, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
                 x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
                 scales, deq, deq);
         }
@@ -552,9 +678,15 @@ qz_status kv_write_launch(const uint16_t* k, const uint16_t* v, int64_t n, uint8
                           float* ks, float* vs, qz_scale_mode mode, void* ws, size_t, cudaStream_t st) {
     const int np = amax_grid();
     float* partial = (mode == QZ_SCALE_COMPUTE) ? (float*)ws : nullptr;
-    if (partial) launch_tensor_amax<uint16_t, true>(k, v, 2, 1, n, n, true, partial, st);
-    fp8_tensor_encode_kernel<uint16_t, true><<<dim3(stream_grid(n / 8), 2), kThreads, 0, st>>>(
-        k, v, 1, n, n, true, partial, np, ks, vs, kc, vc, ks, vs, nullptr, nullptr);
+    const dim3 grid(stream_grid(n / 8), 2);
+    if (partial) {
+        launch_tensor_amax<uint16_t, true>(k, v, 2, 1, n, n, true, partial, st);
+        fp8_tensor_encode_kernel<uint16_t, true, false><<<grid, kThreads, 0, st>>>(
+            k, v, 1, n, n, true, partial, np, nullptr, nullptr, kc, vc, ks, vs, nullptr, nullptr);
+    } else {
+        fp8_tensor_encode_kernel<uint16_t, true, true><<<grid, kThreads, 0, st>>>(
+            k, v, 1, n, n, true, nullptr, np, ks, vs, kc, vc, nullptr, nullptr, nullptr, nullptr);
+    }
     return launch_status();
 }
 

@@ -49,6 +49,14 @@ qz_status device_check() {
     return g_arch_ok[d] == 1 ? QZ_OK : QZ_ERR_UNSUPPORTED;
 }
 
+qz_status device_error_read_and_clear() {
+    qz_status s = w4a16_error_read_and_clear();
+    if (s != QZ_OK) return s;
+    s = fp8_block_error_read_and_clear();
+    if (s != QZ_OK) return s;
+    return fp4_error_read_and_clear();
+}
+
 qz_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? QZ_OK : QZ_ERR_CUDA;
 }

@@ -34,7 +34,7 @@ qz_status device_error_read_and_clear();
 // A bounded spin-wait gives up after this many polls (seconds of waiting),
 // records QZ_ERR_TIMEOUT in the translation unit's error word and returns
 // false, so no kernel can hang the GPU on a lost arrival.
-constexpr uint32_t kWaitLimit = 1u << 26;
+constexpr uint32_t kWaitLimit = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);

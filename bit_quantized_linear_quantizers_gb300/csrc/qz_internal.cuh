@@ -55,6 +55,78 @@ __device__ __forceinline__ float load1(const uint16_t* p) { return bf16_bits_to_
 // x / s rounded once (IEEE round to nearest even): the codes depend on it.
 __device__ __forceinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
 
+// Correctly rounded quotients x / s for a whole scale unit, from r = RN(1/s):
+// q0 = RN(x * r) is within one ulp of x / s, the remainder x - q0 * s is then
+// exact (one fma), and the correction RN(q0 + rem * r) is the correctly
+// rounded quotient (Markstein's theorem: P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990). The preconditions hold whenever the quotient can map to a
+// non-zero code: the scales are >= 1e-12 / 2688 and the quotient and the
+// remainder stay normal. An exactly zero x comes back as +0; callers that
+// keep the sign of zero restore it (sign_of).
+struct Recip {
+    float s, r;
+    __device__ __forceinline__ explicit Recip(float s_) {
+        s = s_;
+        r = __fdiv_rn(1.0f, s_);
+    }
+};
+
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long d, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+
+// Two quotients at once with packed fp32x2 arithmetic.
+__device__ __forceinline__ void div2(float& a, float& b, const Recip& d) {
+    const unsigned long long x = f2_pack(a, b), r = f2_pack(d.r, d.r), ns = f2_pack(-d.s, -d.s);
+    unsigned long long q0, rem, q1;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(r));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rem) : "l"(q0), "l"(ns), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(rem), "l"(r), "l"(q0));
+    f2_unpack(q1, a, b);
+}
+
+// y with the sign bit of x (a non-zero quotient already has it; fixes -0).
+__device__ __forceinline__ float sign_of(float y, float x) {
+    return __uint_as_float(__float_as_uint(y) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Eight E2M1 codes (element j in bits 4j..4j+3) of quotients y[8]: the
+// hardware conversion (round to nearest even, saturating to 6) agrees with
+// the nearest-value rule except at an exact midpoint, where the rule takes the
+// smaller magnitude. Midpoints (0.25 .. 5) carry at most two mantissa bits, so
+// lanes whose quotients all have non-zero low mantissa bits skip the exact
+// recount.
+__device__ __forceinline__ uint32_t e2m1x8(const float y[8]) {
+    uint32_t w = 0;
+    bool maybe_tie = false;
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        uint16_t b;
+        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
+            : "=h"(b) : "f"(y[j + 1]), "f"(y[j]));
+        w |= (uint32_t)(b & 0xFF) << (4 * j);
+        maybe_tie |= (__float_as_uint(y[j]) & 0x1FFFFFu) == 0u;
+        maybe_tie |= (__float_as_uint(y[j + 1]) & 0x1FFFFFu) == 0u;
+    }
+    if (maybe_tie) {
+        w = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const float a = fabsf(y[j]);
+            const uint32_t m = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) + (a > 2.5f) +
+                               (a > 3.5f) + (a > 5.0f);
+            w |= (m | (y[j] < 0.0f ? 8u : 0u)) << (4 * j);
+        }
+    }
+    return w;
+}
+
 // Two fp32 -> two E4M3 bytes, round to nearest even, saturating to +-448
 // (the hardware conversion). Returns lo | hi << 8.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {

@@ -1,0 +1,145 @@
+// qz_tc.cuh -- Blackwell (sm_103a) tensor-core plumbing shared by the
+// tcgen05 GEMMs: tensor memory allocation, MMA issue and commit, TMEM loads,
+// TMA tensor copies, shared-memory matrix descriptors and host-side tensor
+// map encoding. Inline PTX only; no CUTLASS.
+#pragma once
+
+#include "qz_gemm.cuh"
+
+#include <cuda.h>
+
+namespace qz {
+
+// ------------------------------------------------------------ TMEM
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// D (TMEM, fp32) (+)= A (smem desc) x B (smem desc), kind::f8f6f4.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// D (TMEM, fp32) (+)= A x B with hardware block scaling, E2M1 operands:
+// NVFP4 = kind::mxf4nvf4 with one UE4M3 scale per 16 (scale_vec::4X),
+// MXFP4 = kind::mxf4 with one UE8M0 scale per 32 (scale_vec::2X). The scale
+// factors are read from TMEM at sfa / sfb.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+}
+
+// Copy 32 rows x 16 bytes (512 contiguous bytes of shared memory) into TMEM
+// lanes 0-31, 4 columns, replicated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled K-major source whose 8-row x
+// 16-byte core matrices are stored contiguously (128 B apart along M).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 16;                  // leading byte offset
+    d |= (uint64_t)(128 >> 4) << 32;                  // stride byte offset: 8 rows x 16 B
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    return d;                                         // swizzle: none
+}
+
+// Instruction descriptor of the block-scaled FP4 kinds (E2M1 x E2M1 -> fp32),
+// scale type UE4M3 (nv) or UE8M0 (mx), scale-factor byte selectors sf_id.
+__host__ __device__ constexpr uint32_t idesc_fp4(bool ue8m0, uint32_t M, uint32_t N, uint32_t sf_id_a,
+                                                 uint32_t sf_id_b) {
+    return (sf_id_b << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
+           ((M >> 4) << 24) | (sf_id_a << 29);
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32*(w%4) .. +31); must be followed by tmem_wait_ld before use.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+                   "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+                   "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------- TMA
+
+// 2-D tiled TMA load of box (x = inner coordinate, y = outer) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with the 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle
+// atoms stacked along M/N (stride 1024 B). The tile base must be 1024-byte
+// aligned; a K offset inside the 128-byte row is added to the start address.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);         // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                           // descriptor version (fixed 0b001)
+    d |= (uint64_t)2 << 61;                           // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor, dense kinds (f16 / f8f6f4): fp32 accumulator,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_dense(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N) {
+    return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// ------------------------------------------------------------ host
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+} // namespace qz

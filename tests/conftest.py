@@ -10,6 +10,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libqz.so")
+    # build the library and the oracle once (in-tree, incremental) before collection
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def pytest_collection_modifyitems(config, items):

@@ -40,3 +40,19 @@ def assert_same_bytes(gpu: np.ndarray, ref: np.ndarray, what: str):
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def half_ulp_bf16(y_ref: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at the exact value: the error of rounding it to the bf16 output
+    (8 significant bits: ulp = 2^(floor(log2|y|) - 7))."""
+    y = np.abs(np.asarray(y_ref, np.float64))
+    _, e = np.frexp(y)                     # y = m * 2^e, m in [0.5, 1)
+    return np.where(y > 0, np.ldexp(1.0, e - 9), 0.0)
+
+
+def gemm_tolerance(y_ref: np.ndarray, bound: np.ndarray, rel: float = 1e-3) -> np.ndarray:
+    """Acceptance bound of a bf16-output GEMM against the exact FP64 reference:
+    rel * sum_k |a*b| (the accumulation error allowed) plus half a bf16 ulp of the
+    exact result (the rounding of the output to bf16, which alone exceeds the first
+    term wherever |y| approaches sum_k |a*b|)."""
+    return rel * np.asarray(bound, np.float64) + half_ulp_bf16(y_ref)

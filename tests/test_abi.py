@@ -14,9 +14,9 @@ HEADER = os.path.join(ROOT, "include", "qz.h")
 
 
 def _lib():
-    from bit_quantized_linear_quantizers_gb300 import _build
-    _build.build()
-    return ctypes.CDLL(_build.LIB)
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    return ctypes.CDLL(b.build())
 
 
 def declared_functions():

@@ -1,0 +1,130 @@
+"""GPU parity of the NVFP4 and MXFP4 GEMMs (tcgen05 block-scaled FP4) against the
+oracle's FP64 reference: |y_gpu - y_ref| <= 1e-3 * sum_k |a_ik * b_kj| plus half
+a bf16 ulp of y_ref (the rounding of the bf16 output), on the exactly dequantized
+operands (E2M1 x block scale (x tensor scale)). Operands come
+from the oracle's quantizers; integer cases with unit scales must be exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from gpu_util import bf16_bits_to_f64, gemm_tolerance, host
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def qz():
+    import bit_quantized_linear_quantizers_gb300 as q
+    return q
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def check(y_bits, y_ref, bound, what):
+    y = bf16_bits_to_f64(y_bits)
+    ok = np.abs(y - y_ref) <= gemm_tolerance(y_ref, bound, REL)
+    bad = np.argwhere(~ok)
+    assert ok.all(), f"{what}: {len(bad)} outside 1e-3*sum|ab| + half a bf16 ulp; first {bad[:3].tolist()}"
+
+
+def inputs(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    a[:, rng.choice(K, max(1, K // 200), replace=False)] *= np.float32(30)
+    bt = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    return syn.to_bf16_bits(a), syn.to_bf16_bits(bt)
+
+
+def nv_run(qz, a, bt):
+    ca, sa, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+    cb, sb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+    y = host(qz.qz_gemm_nvfp4(dev(ca), dev(sa), dev(np.float32([ga])), dev(cb), dev(sb), dev(np.float32([gb]))))
+    return y, (ca, sa, ga, cb, sb, gb)
+
+
+def mx_run(qz, a, bt):
+    ca, ea, _ = oracle.quant_mxfp4(a, want_deq=False)
+    cb, eb, _ = oracle.quant_mxfp4(bt, want_deq=False)
+    y = host(qz.qz_gemm_mxfp4(dev(ca), dev(ea), dev(cb), dev(eb)))
+    return y, (ca, ea, cb, eb)
+
+
+def pack(codes):
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+def test_fp4_gemm_integer_exact(qz, fmt):
+    """Unit scales and E2M1 codes of small integers: an exact integer matmul."""
+    rng = np.random.default_rng(1)
+    M, N, K = 128, 256, 256
+    mag = np.array([0, 2, 4, 5, 6, 7])                    # 0, 1, 2, 3, 4, 6
+    ca = (rng.choice(mag, (M, K)) | (rng.integers(0, 2, (M, K)) << 3)).astype(np.uint8)
+    cb = (rng.choice(mag, (N, K)) | (rng.integers(0, 2, (N, K)) << 3)).astype(np.uint8)
+    va = np.vectorize(oracle.e2m1_decode)(ca)
+    vb = np.vectorize(oracle.e2m1_decode)(cb)
+    ref = (va @ vb.T).astype(np.float32)
+    if fmt == "nv":
+        one = 0x38
+        y = host(qz.qz_gemm_nvfp4(dev(pack(ca)), dev(np.full((M, K // 16), one, np.uint8)),
+                                  dev(np.float32([1.0])), dev(pack(cb)), dev(np.full((N, K // 16), one, np.uint8)),
+                                  dev(np.float32([1.0]))))
+    else:
+        y = host(qz.qz_gemm_mxfp4(dev(pack(ca)), dev(np.full((M, K // 32), 127, np.uint8)),
+                                  dev(pack(cb)), dev(np.full((N, K // 32), 127, np.uint8))))
+    assert np.array_equal(bf16_bits_to_f64(y), bf16_bits_to_f64(syn.to_bf16_bits(ref)))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256)])
+def test_nvfp4_gemm(qz, M, N, K):
+    a, bt = inputs(M, N, K, seed=M + N + K)
+    y, ops = nv_run(qz, a, bt)
+    y_ref, bound = oracle.gemm_nvfp4(*ops)
+    check(y, y_ref, bound, f"nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256)])
+def test_mxfp4_gemm(qz, M, N, K):
+    a, bt = inputs(M, N, K, seed=M + N + K + 1)
+    y, ops = mx_run(qz, a, bt)
+    y_ref, bound = oracle.gemm_mxfp4(*ops)
+    check(y, y_ref, bound, f"mxfp4 {M}x{N}x{K}")
+
+
+def test_fp4_gemm_scales_per_block(qz):
+    """Distinct scales per (row, block) on both operands: a scale read from the wrong
+    block or row shows up as a large error."""
+    rng = np.random.default_rng(9)
+    M, N, K = 256, 512, 512
+    ca = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    cb = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    ea = rng.integers(120, 135, (M, K // 32)).astype(np.uint8)
+    eb = rng.integers(120, 135, (N, K // 32)).astype(np.uint8)
+    y = host(qz.qz_gemm_mxfp4(dev(pack(ca)), dev(ea), dev(pack(cb)), dev(eb)))
+    y_ref, bound = oracle.gemm_mxfp4(pack(ca), ea, pack(cb), eb)
+    check(y, y_ref, bound, "mx per-block scales")
+    sa = rng.integers(0x20, 0x60, (M, K // 16)).astype(np.uint8)          # UE4M3 in [2^-4, 2^4)
+    sb = rng.integers(0x20, 0x60, (N, K // 16)).astype(np.uint8)
+    y = host(qz.qz_gemm_nvfp4(dev(pack(ca)), dev(sa), dev(np.float32([0.5])), dev(pack(cb)), dev(sb),
+                              dev(np.float32([3.0]))))
+    y_ref, bound = oracle.gemm_nvfp4(pack(ca), sa, 0.5, pack(cb), sb, 3.0)
+    check(y, y_ref, bound, "nv per-block scales")
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+def test_fp4_gemm_full_size_sampled(qz, fmt):
+    """Config 4 at full size (M=8192, N=4096, K=4096) in the bench's launch
+    configuration, operands from the oracle's quantizers, sampled outputs."""
+    a, bt = syn.fp4_gemm_inputs(seed=0)
+    y, ops = (nv_run if fmt == "nv" else mx_run)(qz, a, bt)
+    rng = np.random.default_rng(3)
+    ii, jj = rng.integers(0, a.shape[0], 3000), rng.integers(0, bt.shape[0], 3000)
+    ref = oracle.gemm_nvfp4 if fmt == "nv" else oracle.gemm_mxfp4
+    y_ref, bound = ref(*ops, ii, jj)
+    check(y[ii, jj], y_ref, bound, f"{fmt} full size")

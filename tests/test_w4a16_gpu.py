@@ -1,7 +1,8 @@
 """GPU parity of the W4A16 GEMM against the oracle's FP64 reference.
 
-Acceptance (the GEMM tolerance): |y_gpu - y_ref| <= 1e-3 * sum_k |a_ik * b_kj|, on
-the exactly dequantized operands. The INT4 weights fed to both sides come from
+Acceptance (the GEMM tolerance): |y_gpu - y_ref| <= 1e-3 * sum_k |a_ik * b_kj| plus
+half a bf16 ulp of y_ref (the rounding of the bf16 output), on the exactly
+dequantized operands. The INT4 weights fed to both sides come from
 the oracle's quantizer, never from the GPU. Shapes cover ragged token counts
 (M = 1..64), several tiles, the half-depth last K stage (K % 256 == 128), the
 full Llama-3.1-8B MLP size (sampled outputs) and a grouped launch."""
@@ -10,7 +11,7 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_util import bf16_bits_to_f64, dev_bf16, host
+from gpu_util import bf16_bits_to_f64, gemm_tolerance, dev_bf16, host
 
 import torch
 
@@ -41,9 +42,9 @@ def activations(M, K, seed):
 
 def check(y_gpu_bits, y_ref, bound, what):
     y = bf16_bits_to_f64(y_gpu_bits)
-    ok = np.abs(y - y_ref) <= REL * bound
+    ok = np.abs(y - y_ref) <= gemm_tolerance(y_ref, bound, REL)
     bad = np.argwhere(~ok)
-    assert ok.all(), f"{what}: {len(bad)} outside 1e-3*sum|ab|, first {bad[:3].tolist()}"
+    assert ok.all(), f"{what}: {len(bad)} outside 1e-3*sum|ab| + half a bf16 ulp, first {bad[:3].tolist()}"
 
 
 def run(qz, A, qw, sc):
