@@ -29,6 +29,7 @@
 #include "qz_tc.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace qz {
 
@@ -271,6 +272,40 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
     else
         fp4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, wsA, wsB, gA, gB, Y, M, N, K);
     return launch_status();
+}
+
+} // namespace qz
+
+// ------------------------------------------------ allocation-free NVFP4 GEMM
+//
+// Scratch of qz_gemm_nvfp4_noalloc: a fixed device array defined here, so
+// callers that cannot allocate still get the re-laid scale factors somewhere.
+// In host code the symbol is only a host-side stand-in; its device address is
+// looked up once per device (with that device current) and cached.
+static __device__ __align__(256) uint8_t qz_nvfp4_noalloc_scratch[QZ_NVFP4_NOALLOC_SCRATCH_BYTES];
+
+namespace qz {
+
+namespace {
+void* g_noalloc_ptr[64];
+std::mutex g_noalloc_mu;
+} // namespace
+
+qz_status nvfp4_noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QZ_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, qz_nvfp4_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return QZ_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return QZ_OK;
 }
 
 } // namespace qz

@@ -273,4 +273,24 @@ qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB,
                            (cudaStream_t)stream);
 }
 
+// Same computation as qz_gemm_nvfp4; the scratch is the library's fixed array
+// (see nvfp4_noalloc_scratch) instead of a caller workspace. No allocation.
+qz_status qz_gemm_nvfp4_noalloc(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                                const uint8_t* qB, const uint8_t* sB, const float* gB,
+                                uint16_t* Y, int M, int N, int K, void* stream) {
+    if (!gA || !gB || !qA || !sA || !qB || !sB || !Y) return QZ_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return QZ_ERR_INVALID_ARG;
+    if (M % kFp4BlockM || N % kFp4BlockN || K % kFp4BlockK) return QZ_ERR_SHAPE;
+    if (!is_aligned(qA, 16) || !is_aligned(qB, 16) || !is_aligned(sA, 16) || !is_aligned(sB, 16) ||
+        !is_aligned(Y, 16))
+        return QZ_ERR_ALIGNMENT;
+    const size_t need = ws_gemm_fp4(M, N, K);
+    if (need > QZ_NVFP4_NOALLOC_SCRATCH_BYTES) return QZ_ERR_SHAPE;   // beyond the fixed scratch
+    QZ_TRY(device_check());
+    void* scratch = nullptr;
+    QZ_TRY(nvfp4_noalloc_scratch(&scratch));
+    return gemm_fp4_launch(true, qA, sA, gA, qB, sB, gB, Y, M, N, K, scratch, QZ_NVFP4_NOALLOC_SCRATCH_BYTES,
+                           (cudaStream_t)stream);
+}
+
 } // extern "C"

@@ -28,6 +28,11 @@ qz_status w4a16_error_read_and_clear();
 qz_status fp8_block_error_read_and_clear();
 qz_status fp4_error_read_and_clear();
 qz_status device_error_read_and_clear();
+qz_status device_check();
+
+// Device address of the fixed scratch array of qz_gemm_nvfp4_noalloc on the
+// current device (looked up on first use per device).
+qz_status nvfp4_noalloc_scratch(void** out);
 
 // ------------------------------------------------------------ PTX helpers
 

@@ -226,6 +226,33 @@ qz_status qz_gemm_nvfp4(const uint8_t* qA, const uint8_t* sA, const float* gA,
 qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
                         uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
 
+/* NVFP4 GEMM that allocates nothing and takes no workspace. (The surveyed
+ * pages have no counterpart: this is an interface convenience of this library.)
+ * Some callers cannot call cudaMalloc or hand this library a workspace: runtimes
+ * whose device memory is planned once at start-up and parcelled out by their own
+ * arena (plug-ins get no allocator), and latency-critical loops that must not
+ * risk cudaMalloc/cudaFree synchronising the device or failing mid-step. This
+ * call computes exactly what qz_gemm_nvfp4 computes, with the same arguments
+ * minus ws/ws_bytes; its scratch (the scale factors re-laid for the tensor
+ * cores) lives in a fixed device array of QZ_NVFP4_NOALLOC_SCRATCH_BYTES that
+ * the library defines, which every GPU that loads the library holds until the
+ * process exits.
+ * Limit: round_up(M*K/16, 1024) + round_up(N*K/16, 1024) must not exceed
+ *   QZ_NVFP4_NOALLOC_SCRATCH_BYTES (4 MiB: e.g. M + N <= 16384 at K = 4096);
+ *   larger sizes return QZ_ERR_SHAPE and launch nothing.
+ * Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture on the device.
+ * Sharing: every call uses the same array and leaves its last contents there;
+ *   nothing in it needs to start at zero (each call writes every byte it later
+ *   reads). Calls whose executions overlap on the GPU (different streams, no
+ *   ordering between them) race on the array and must be serialised by the
+ *   caller. Other rules, layouts and errors: as qz_gemm_nvfp4. */
+#define QZ_NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+qz_status qz_gemm_nvfp4_noalloc(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                                const uint8_t* qB, const uint8_t* sB, const float* gB,
+                                uint16_t* Y, int M, int N, int K, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
