@@ -163,14 +163,15 @@ class Timer:
         self.stream = stream
 
     def __call__(self, fn, reps: int, warm: int = 3) -> float:
+        """fn(i) runs call i; rows rotate i over input copies whose total exceeds L2."""
         torch = self.torch
         with torch.cuda.stream(self.stream):
-            fn()                                       # first call outside capture (sets attributes)
+            fn(0)                                      # first call outside capture (sets attributes)
         self.stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
-            for _ in range(reps):
-                fn()
+            for i in range(reps):
+                fn(i)
         with torch.cuda.stream(self.stream):
             for _ in range(warm):
                 g.replay()
@@ -281,11 +282,9 @@ def gpu_arm(args, rank, world, local_rank):
     # ---- roofline of the dominant kernel (w4a16_kernel): per-M launch timing
     timer = Timer(stream)
     per_m = {}
-    it = [0]
     for M in MS:
-        def one(M=M):
-            q, s = weights[it[0] % COPIES]
-            it[0] += 1
+        def one(i, M=M):
+            q, s = weights[i % COPIES]
             qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
         us = timer(one, reps=200, warm=10)
         per_m[M] = {"us": round(us, 3), "gbps": round(step_bytes(M) / us / 1e3, 1),
@@ -301,7 +300,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     rows = {}
     if not args.no_rows:
-        rows = secondary_rows(qz, syn, stream, dev, pk)
+        rows = secondary_rows(qz, syn, stream, dev, pk, set(args.rows.split(",")))
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -323,8 +322,10 @@ def gpu_arm(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
-def secondary_rows(qz, syn, stream, dev, pk):
-    """The other hot-path rows, each timed on its own (CUDA events, inputs resident)."""
+def secondary_rows(qz, syn, stream, dev, pk, which):
+    """The other hot-path rows, each timed on its own (CUDA events, inputs resident).
+    `which` selects among fp8 (config 3), fp4 (config 4), roundtrip (config 1), kv and
+    qwen (config 5)."""
     import numpy as np
     import torch
 
@@ -338,92 +339,148 @@ def secondary_rows(qz, syn, stream, dev, pk):
     fp8_peak = 2.0 * pk["bf16_tflops"]          # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
     fp4_peak = 6.0 * pk["bf16_tflops"]          # FP4 dense = 6 x bf16 (nominal 13.5 / 2.25 PF)
 
+    q = {}
+    if "fp8" in which:
+        fp8_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp8_peak)
+    if "fp4" in which:
+        fp4_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp4_peak)
+    if "roundtrip" in which:
+        roundtrip_rows(qz, syn, dev, timer, ws, rows, stream)
+    if "kv" in which:
+        kv_rows(qz, syn, stream, pk, timer, ws, bf, q)
+    if q:
+        rows["quantizers"] = q
+    if "qwen" in which:
+        rows["qwen3_decode_step"] = qwen3_step(qz, syn, stream, dev, pk, timer, ws)
+    return rows
+
+
+def copies_for(nbytes: int, l2_bytes: int = 126 << 20) -> int:
+    """Copies of an input of nbytes needed for the copies together to exceed 2 x L2."""
+    return max(2, -(-2 * l2_bytes // max(1, nbytes)))
+
+
+def fp8_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp8_peak):
+    import torch
     # config 3: FP8 1x128 activations, 128x128 weights, block-scaled GEMM
     a, bt = syn.fp8_block_gemm_inputs(seed=0)
     a_d, bt_d = bf(a), bf(bt)
     del a, bt
-    with torch.cuda.stream(stream):
-        qa, sa, _ = qz.qz_quantize_fp8(a_d, qz.FP8_GROUP_1x128, stream=stream)
-        qb, sb, _ = qz.qz_quantize_fp8(bt_d, qz.FP8_BLOCK_128x128, stream=stream)
     M3, K3 = a_d.shape
     N3 = bt_d.shape[0]
-    q = {}
-    us = timer(lambda: qz.qz_quantize_fp8(a_d, qz.FP8_GROUP_1x128, codes=qa, scales=sa, stream=stream), 20)
+    na = copies_for(a_d.numel() * 3)
+    A = [a_d] + [a_d.clone() for _ in range(na - 1)]
+    outa = [qz.qz_quantize_fp8(x, qz.FP8_GROUP_1x128, stream=stream)[:2] for x in A]
+    us = timer(lambda i: qz.qz_quantize_fp8(A[i % na], qz.FP8_GROUP_1x128, codes=outa[i % na][0],
+                                            scales=outa[i % na][1], stream=stream), 4 * na)
     by = M3 * K3 * 2 + M3 * K3 + M3 * (K3 // 128) * 4
     q["fp8_1x128_A_2048x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
                                        "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
-    us = timer(lambda: qz.qz_quantize_fp8(bt_d, qz.FP8_BLOCK_128x128, codes=qb, scales=sb, stream=stream), 10)
+    nb = copies_for(bt_d.numel() * 3)
+    B = [bt_d] + [bt_d.clone() for _ in range(nb - 1)]
+    outb = [qz.qz_quantize_fp8(x, qz.FP8_BLOCK_128x128, stream=stream)[:2] for x in B]
+    us = timer(lambda i: qz.qz_quantize_fp8(B[i % nb], qz.FP8_BLOCK_128x128, codes=outb[i % nb][0],
+                                            scales=outb[i % nb][1], stream=stream), 4 * nb)
     by = N3 * K3 * 2 + N3 * K3 + (N3 // 128) * (K3 // 128) * 4
     q["fp8_128x128_Bt_14336x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
                                            "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    del A, B
     try:
-        y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
-        us = timer(lambda: qz.qz_gemm_fp8_block(qa, sa, qb, sb, Y=y3, ws=ws, stream=stream), 20)
+        # GEMM operands rotate over copies (A + B codes exceed 2 x L2 together)
+        ng = copies_for(M3 * K3 + N3 * K3 + M3 * N3 * 2)
+        ops = [(outa[i % len(outa)][0], outa[i % len(outa)][1], outb[i % len(outb)][0], outb[i % len(outb)][1])
+               for i in range(ng)]
+        ys = [torch.empty((M3, N3), dtype=torch.bfloat16, device=dev) for _ in range(ng)]
+        us = timer(lambda i: qz.qz_gemm_fp8_block(*ops[i % ng], Y=ys[i % ng], ws=ws, stream=stream), 4 * ng)
         fl = 2.0 * M3 * N3 * K3
         rows["fp8_block_gemm_2048x14336x4096"] = {"us": round(us, 2), "tflops": round(fl / us / 1e6, 1),
                                                   "peak_tflops": fp8_peak,
                                                   "frac": round(fl / us / 1e6 / fp8_peak, 4)}
     except qz.QZError as e:
         rows["fp8_block_gemm_2048x14336x4096"] = {"unavailable": str(e)}
-    del a_d, bt_d, qb
 
+
+def fp4_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp4_peak):
+    import torch
     # config 4: NVFP4 / MXFP4 quantize + GEMM
     a, bt = syn.fp4_gemm_inputs(seed=0)
     a_d, bt_d = bf(a), bf(bt)
     del a, bt
     M4, K4 = a_d.shape
     N4 = bt_d.shape[0]
-    with torch.cuda.stream(stream):
-        na = qz.qz_quantize_nvfp4(a_d, ws=ws, stream=stream)
-        nb = qz.qz_quantize_nvfp4(bt_d, ws=ws, stream=stream)
-        ma = qz.qz_quantize_mxfp4(a_d, stream=stream)
-        mb = qz.qz_quantize_mxfp4(bt_d, stream=stream)
-    us = timer(lambda: qz.qz_quantize_nvfp4(a_d, codes=na[0], scale_e4m3=na[1], global_scale=na[2], ws=ws,
-                                            stream=stream), 20)
+    na = copies_for(a_d.numel() * 2)
+    A = [a_d] + [a_d.clone() for _ in range(na - 1)]
+    nvA = [qz.qz_quantize_nvfp4(x, ws=ws, stream=stream)[:3] for x in A]
+    mxA = [qz.qz_quantize_mxfp4(x, stream=stream)[:2] for x in A]
+    nvB = qz.qz_quantize_nvfp4(bt_d, ws=ws, stream=stream)[:3]
+    mxB = qz.qz_quantize_mxfp4(bt_d, stream=stream)[:2]
+    us = timer(lambda i: qz.qz_quantize_nvfp4(A[i % na], codes=nvA[i % na][0], scale_e4m3=nvA[i % na][1],
+                                              global_scale=nvA[i % na][2], ws=ws, stream=stream), 4 * na)
     by = M4 * K4 * 2 + M4 * K4 // 2 + M4 * K4 // 16 + 4
     q["nvfp4_A_8192x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
                                    "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
-    us = timer(lambda: qz.qz_quantize_mxfp4(a_d, codes=ma[0], scale_e8m0=ma[1], stream=stream), 20)
+    us = timer(lambda i: qz.qz_quantize_mxfp4(A[i % na], codes=mxA[i % na][0], scale_e8m0=mxA[i % na][1],
+                                              stream=stream), 4 * na)
     by = M4 * K4 * 2 + M4 * K4 // 2 + M4 * K4 // 32
     q["mxfp4_A_8192x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
                                    "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    del A
     fl = 2.0 * M4 * N4 * K4
-    y4 = torch.empty((M4, N4), dtype=torch.bfloat16, device=dev)
+    # the na copies of A's codes (plus B and the output) exceed 2 x L2 together
+    ys = [torch.empty((M4, N4), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     for name, fn in (("nvfp4_gemm_8192x4096x4096",
-                      lambda: qz.qz_gemm_nvfp4(na[0], na[1], na[2], nb[0], nb[1], nb[2], Y=y4, ws=ws,
-                                               stream=stream)),
+                      lambda i: qz.qz_gemm_nvfp4(*nvA[i % na], *nvB, Y=ys[i % 2], ws=ws, stream=stream)),
                      ("mxfp4_gemm_8192x4096x4096",
-                      lambda: qz.qz_gemm_mxfp4(ma[0], ma[1], mb[0], mb[1], Y=y4, ws=ws, stream=stream))):
+                      lambda i: qz.qz_gemm_mxfp4(*mxA[i % na], *mxB, Y=ys[i % 2], ws=ws, stream=stream))):
         try:
-            us = timer(fn, 20)
+            us = timer(fn, 4 * na)
             rows[name] = {"us": round(us, 2), "tflops": round(fl / us / 1e6, 1), "peak_tflops": fp4_peak,
                           "frac": round(fl / us / 1e6 / fp4_peak, 4)}
         except qz.QZError as e:
             rows[name] = {"unavailable": str(e)}
     del a_d, bt_d
 
-    # config 1: the six quantizer paths on the 1024 x 1024 fp32 weight (launch-bound: us)
-    x = torch.from_numpy(syn.quant_roundtrip_input(seed=0)).to(dev)
+
+def roundtrip_rows(qz, syn, dev, timer, ws, rows, stream):
+    import torch
+    # config 1: the six quantizer paths on the 1024 x 1024 fp32 weight (4 MiB, launch-bound: us);
+    # 128 copies rotate so that each call reads its input from HBM
+    x0 = torch.from_numpy(syn.quant_roundtrip_input(seed=0)).to(dev)
+    n = copies_for(x0.numel() * 4)
+    X = [x0] + [x0.clone() for _ in range(n - 1)]
     c1 = {}
     for nm, g in (("fp8_per_tensor", 0), ("fp8_per_row", 1), ("fp8_128x128", 2), ("fp8_1x128", 3)):
-        c1[nm] = round(timer(lambda g=g: qz.qz_quantize_fp8(x, g, dequant=True, ws=ws, stream=stream), 50), 2)
-    c1["mxfp4"] = round(timer(lambda: qz.qz_quantize_mxfp4(x, dequant=True, stream=stream), 50), 2)
-    c1["nvfp4"] = round(timer(lambda: qz.qz_quantize_nvfp4(x, dequant=True, ws=ws, stream=stream), 50), 2)
-    c1["int4_g128"] = round(timer(lambda: qz.qz_quantize_int4_g128(x, dequant=True, stream=stream), 50), 2)
+        outs = [qz.qz_quantize_fp8(x, g, dequant=True, ws=ws, stream=stream) for x in X]
+        c1[nm] = round(timer(lambda i, g=g, outs=outs: qz.qz_quantize_fp8(
+            X[i % n], g, codes=outs[i % n][0], scales=outs[i % n][1], dequant=outs[i % n][2], ws=ws,
+            stream=stream), 2 * n), 2)
+    outs = [qz.qz_quantize_mxfp4(x, dequant=True, stream=stream) for x in X]
+    c1["mxfp4"] = round(timer(lambda i: qz.qz_quantize_mxfp4(
+        X[i % n], codes=outs[i % n][0], scale_e8m0=outs[i % n][1], dequant=outs[i % n][2], stream=stream), 2 * n), 2)
+    outs = [qz.qz_quantize_nvfp4(x, dequant=True, ws=ws, stream=stream) for x in X]
+    c1["nvfp4"] = round(timer(lambda i: qz.qz_quantize_nvfp4(
+        X[i % n], codes=outs[i % n][0], scale_e4m3=outs[i % n][1], global_scale=outs[i % n][2],
+        dequant=outs[i % n][3], ws=ws, stream=stream), 2 * n), 2)
+    outs = [qz.qz_quantize_int4_g128(x, dequant=True, stream=stream) for x in X]
+    c1["int4_g128"] = round(timer(lambda i: qz.qz_quantize_int4_g128(
+        X[i % n], qweight=outs[i % n][0], scale_bf16=outs[i % n][1], dequant=outs[i % n][2], stream=stream),
+        2 * n), 2)
     rows["quantize_roundtrip_1024x1024_f32_us"] = c1
 
-    # config 5: FP8 KV write of K, V bf16 [1, 8, 4096, 128]
+
+def kv_rows(qz, syn, stream, pk, timer, ws, bf, q):
+    # config 5: FP8 KV write of K, V bf16 [1, 8, 4096, 128] (8 MiB each), rotating copies
     k, v = syn.kv_cache_inputs(seed=0)
     k_d, v_d = bf(k), bf(v)
-    kv = qz.qz_kv_write_fp8(k_d, v_d, ws=ws, stream=stream)
-    us = timer(lambda: qz.qz_kv_write_fp8(k_d, v_d, k_codes=kv[0], v_codes=kv[1], k_scale=kv[2],
-                                          v_scale=kv[3], ws=ws, stream=stream), 50)
+    n = copies_for(k.size * 2 * 3)
+    KV = [(k_d, v_d)] + [(k_d.clone(), v_d.clone()) for _ in range(n - 1)]
+    outs = [qz.qz_kv_write_fp8(a, b, ws=ws, stream=stream) for a, b in KV]
+    us = timer(lambda i: qz.qz_kv_write_fp8(*KV[i % n], k_codes=outs[i % n][0], v_codes=outs[i % n][1],
+                                            k_scale=outs[i % n][2], v_scale=outs[i % n][3], ws=ws,
+                                            stream=stream), 2 * n)
     by = 2 * (k.size * 2 + k.size) + 8
     q["kv_write_fp8_2x8x4096x128_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
                                            "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
-    rows["quantizers"] = q
-    rows["qwen3_decode_step"] = qwen3_step(qz, syn, stream, dev, pk, timer, ws)
-    return rows
 
 
 def qwen3_step(qz, syn, stream, dev, pk, timer, ws):
@@ -442,7 +499,7 @@ def qwen3_step(qz, syn, stream, dev, pk, timer, ws):
         probs.append((a_d, qw, sc, Y))
         wbytes += K * N // 2 + (K // 128) * N * 2 + 64 * K * 2 + 64 * N * 2
     stream.synchronize()
-    us = timer(lambda: qz.qz_gemm_w4a16_grouped(probs, stream=stream), 20)
+    us = timer(lambda i: qz.qz_gemm_w4a16_grouped(probs, stream=stream), 20)
     out = {"w4a16_grouped_196_linears_us": round(us, 2), "w4a16_gbps": round(wbytes / us / 1e3, 1),
            "w4a16_frac_of_hbm": round(wbytes / us / 1e3 / pk["hbm_gbs"], 3)}
     return out
@@ -521,6 +578,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qz", "reference"], default="qz")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary per-row measurements")
+    ap.add_argument("--rows", default="fp8,fp4,roundtrip,kv,qwen",
+                    help="secondary rows to measure (comma list of fp8, fp4, roundtrip, kv, qwen)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)

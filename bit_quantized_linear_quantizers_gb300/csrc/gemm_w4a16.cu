@@ -9,12 +9,18 @@
 //  * swap A and B: the MMA computes Y^T = W^T A^T, so 16 weight columns fill
 //    the MMA's 16-row side and up to 8 tokens its 8-wide side; M <= 64 tokens
 //    take MT/8 MMAs per weight fragment (mma.m16n8k16, bf16 in, fp32 out).
-//  * one CTA per tile of NT weight columns and the whole K range: NT is
-//    chosen so that the tile count is about the SM count (no split-K and no
-//    scratch memory); grouped launches run many problems' tiles in one grid.
-//  * a producer warp stages 256-deep K slices of the weights, the
-//    activations and the scales into shared memory with TMA bulk copies
-//    (cp.async.bulk) completing on mbarriers; NT/16 MMA warps consume them.
+//  * persistent CTAs (at most one per SM) walk a list of tiles of NT weight
+//    columns x the whole K range; NT is chosen so that a single problem has
+//    about one tile per SM (no split-K across CTAs, no scratch memory), and
+//    grouped launches (a decoder step's linears) stream all problems' tiles
+//    through one warm pipeline. Two MMA warps share each 16-column slice,
+//    one per 128-deep scale group of every stage, and add their sums in
+//    shared memory at the end of the tile.
+//  * a producer thread stages 256-deep K slices through an mbarrier ring with
+//    2-D tensor TMA: the packed weights as 32-column x 32-row boxes (4 KB,
+//    128-byte swizzle), the activations as one 256 x MT box (rows beyond M
+//    and K beyond the end read as zero) and the scales as one NT x 2 box --
+//    a handful of large copies per stage, so the copy engine keeps HBM busy.
 //  * the INT4 codes are exact integers in bf16, so each 128-deep group is
 //    multiplied exactly and the fp32 group sum is scaled by its bf16 scale
 //    (folding the scale into bf16 weights would round).
@@ -22,7 +28,7 @@
 //    thread (g, t) takes the whole packed word of k-octet t, so one 32-bit
 //    shared load feeds two MMA k-steps, and the matching activations are 8
 //    consecutive bf16 (one 16-byte load).
-#include "qz_gemm.cuh"
+#include "qz_tc.cuh"
 
 #include <cuda_bf16.h>
 #include <algorithm>
@@ -34,35 +40,42 @@ namespace {
 __device__ unsigned int g_w4a16_err;
 
 constexpr int KT = 256;                 // K per pipeline stage (two scale groups)
-constexpr int WPAD = 8;                 // words of padding per weight row (bank spread)
-constexpr int AROW = KT * 2 + 64;       // bytes per activation row in shared memory
-constexpr int NTMAX = 128;
+constexpr int NTMAX = 128;              // widest tile (16 MMA warps)
+
+// Widest tile for an MT-token kernel: more tokens need more accumulator
+// registers, so fewer (wider-register) MMA warps.
+__host__ __device__ constexpr int ntmax_for(int mt) { return mt <= 16 ? 128 : 64; }
+constexpr int PER_LAUNCH = 56;          // problems per launch (kernel parameter space: 32 KB)
+constexpr int WBOX = 4096;              // one 32-column x 32-row weight box
 
 struct Prob {
-    const uint16_t* A;
-    const uint32_t* q;
-    const uint16_t* s;
+    CUtensorMap tmW;                    // qweight [K/8][N] int32, box 32 x 32, 128-byte swizzle
+    CUtensorMap tmA;                    // A [M][K] bf16, box 256 x MT
+    CUtensorMap tmS;                    // scale [K/128][N] bf16, box NT x 2
     uint16_t* Y;
     int M, N, K;
-    int nt;          // tile width (columns), multiple of 16
-    int cta_begin;   // first CTA index of this problem
+    int tile_begin;                     // first tile index of this problem
 };
 
 struct Params {
+    Prob p[PER_LAUNCH];
     int count;
-    Prob p[kW4A16MaxProblems];
+    int total_tiles;
 };
 
 struct Layout {
-    int nt, mt, ns;
-    uint32_t w_bytes, a_bytes, s_bytes, stage_bytes;
-    __host__ __device__ Layout(int nt_, int mt_, int ns_) : nt(nt_), mt(mt_), ns(ns_) {
-        w_bytes = 32u * (uint32_t)(nt + WPAD) * 4u;
-        a_bytes = (uint32_t)mt * AROW;
-        s_bytes = 2u * NTMAX * 2u;
-        stage_bytes = w_bytes + a_bytes + s_bytes;
+    uint32_t w_bytes, a_bytes, s_bytes, stage_bytes, y_pitch, y_bytes;
+    __host__ __device__ Layout(int nt, int mt) {
+        w_bytes = (uint32_t)(nt / 32) * WBOX;
+        a_bytes = (uint32_t)mt * KT * 2u;
+        s_bytes = ((uint32_t)nt * 4u + 127u) & ~127u;
+        stage_bytes = (w_bytes + a_bytes + s_bytes + 1023u) & ~1023u;
+        y_pitch = (uint32_t)nt + 4u;                      // fp32 words per staged output row
+        y_bytes = ((uint32_t)mt * y_pitch * 4u + 1023u) & ~1023u;
     }
-    __host__ __device__ uint32_t smem_bytes() const { return (uint32_t)ns * stage_bytes + 2u * ns * 8u; }
+    __host__ __device__ uint32_t smem_bytes(int ns) const {
+        return (uint32_t)ns * stage_bytes + y_bytes + 2u * ns * 8u + 1024u;
+    }
 };
 
 __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
@@ -72,15 +85,17 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Byte B of an offset-binary word u (two 4-bit codes u = q + 8 per byte) ->
-// bf16x2 (q_even, q_odd). The even code comes from byte B of u, the odd code
-// from byte B of u >> 4 (u4); each lands in mantissa bits 0-3 of its bf16
-// half (value 128 + u), and one fma (x * 1 - 136) gives q exactly.
+// Byte B of a packed word w (two's-complement 4-bit codes, element 2B in
+// the low nibble of byte B) -> bf16x2 (q_even, q_odd). The even code comes
+// from byte B of w, the odd one from byte B of w4 = w >> 4; one lop3 keeps
+// each code in mantissa bits 0-3 of its half, flips its sign bit (u = q + 8)
+// and sets the exponent of 128, so the half holds 128 + u exactly; one fma
+// (x * 1 - 136) leaves q.
 template <int B>
-__device__ __forceinline__ uint32_t nib_pair(uint32_t u, uint32_t u4) {
-    const uint32_t r = __byte_perm(u, u4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t w4) {
+    const uint32_t r = __byte_perm(w, w4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
     uint32_t v;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43084308u));
     uint32_t out;
     const uint32_t one = 0x3F803F80u;    // bf16x2 (1.0, 1.0)
     const uint32_t add = 0xC308C308u;    // bf16x2 (-136.0, -136.0)
@@ -88,31 +103,25 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t u, uint32_t u4) {
     return out;
 }
 
+// Word at (row r, column c) of a 32 x 32-word box written by TMA with the
+// 128-byte swizzle (16-byte chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t wbox_word(const uint8_t* box, int r, int c) {
+    return *reinterpret_cast<const uint32_t*>(box + r * 128 + ((((c >> 2) ^ (r & 7)) << 4) | ((c & 3) << 2)));
+}
+
 template <int MT>
-__global__ void __launch_bounds__((NTMAX / 16 + 1) * 32)
-w4a16_kernel(const __grid_constant__ Params P, int nt_max, int ns) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__((2 * ntmax_for(MT) / 16 + 1) * 32, 1)
+w4a16_kernel(const __grid_constant__ Params P, int nt, int ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int MB = MT / 8;                       // 8-token MMA blocks
-    const int nwarps_c = nt_max / 16;                // consumer warps
+    const int nslice = nt / 16;                      // 16-column MMA slices
+    const int nwarps_c = 2 * nslice;                 // MMA warps: one per slice and scale group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Layout L(nt, MT);
 
-    // ---- locate problem and tile
-    int lo = 0, hi = P.count - 1;
-    while (lo < hi) {                                // last problem with cta_begin <= blockIdx.x
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.p[mid].cta_begin <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-    }
-    const Prob& pr = P.p[lo];
-    const int tile = blockIdx.x - pr.cta_begin;
-    const int n0 = tile * pr.nt;
-    const int ntv = min(pr.nt, pr.N - n0);           // valid columns (multiple of 16)
-    const int nstage = (pr.K + KT - 1) / KT;
-    const Layout L(nt_max, MT, ns);
-
-    uint8_t* sW = smem;
-    uint8_t* sA = smem + L.w_bytes;
-    uint8_t* sS = sA + L.a_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)ns * L.stage_bytes);
+    float* ybuf = reinterpret_cast<float*>(smem + (size_t)ns * L.stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)ns * L.stage_bytes + L.y_bytes);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + ns);
 
     if (threadIdx.x == 0) {
@@ -123,75 +132,129 @@ w4a16_kernel(const __grid_constant__ Params P, int nt_max, int ns) {
         fence_barrier_init();
     }
     __syncthreads();
+    // Programmatic dependent launch: the next kernel on the stream may start as
+    // soon as SMs free up; this kernel waits for the previous one (griddepcontrol
+    // .wait, producer below) only before loading activations, so its first weight
+    // stages stream in while the previous kernel finishes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    bool ok = true;
+    auto find = [&](int tile) {                      // last problem with tile_begin <= tile
+        int lo = 0, hi = P.count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.p[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+
     if (warp == nwarps_c) {
-        // ------------------------------------------------ producer warp
-        const uint32_t wrow = (uint32_t)ntv * 4u, srow = (uint32_t)ntv * 2u;
-        const int mrows = min(pr.M, MT);
-        for (int s = 0; s < nstage && ok; s++) {
-            const int k0 = s * KT;
-            const int kl = min(KT, pr.K - k0);               // 256, or 128 for the last stage
-            const uint32_t bytes = (uint32_t)(kl / 8) * wrow + (uint32_t)mrows * kl * 2u + (uint32_t)(kl / 128) * srow;
-            const int slot = s % ns;
-            if (s >= ns) ok = mbar_wait(empty0 + 8 * slot, ((s / ns) - 1) & 1, &g_w4a16_err);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const uint32_t full = full0 + 8 * slot;
-            if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-            __syncwarp();
-            const uint32_t st = smem_u32(smem) + slot * L.stage_bytes;
-            if (lane < kl / 8)
-                bulk_g2s(st + lane * (uint32_t)(nt_max + WPAD) * 4u,
-                         pr.q + (size_t)(k0 / 8 + lane) * pr.N + n0, wrow, full);
-            for (int r = lane; r < mrows; r += 32)
-                bulk_g2s(st + L.w_bytes + r * AROW, pr.A + (size_t)r * pr.K + k0, (uint32_t)kl * 2u, full);
-            if (lane < kl / 128)
-                bulk_g2s(st + L.w_bytes + L.a_bytes + lane * NTMAX * 2u,
-                         pr.s + (size_t)(k0 / 128 + lane) * pr.N + n0, srow, full);
+        // ------------------------------------------------ producer (one thread)
+        if (lane == 0) {
+            const uint32_t bytes = L.w_bytes + L.a_bytes + (uint32_t)nt * 4u;
+            uint32_t it = 0;
+            bool ok = true, waited = false;
+            for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+                const Prob& pr = P.p[find(tile)];
+                const int n0 = (tile - pr.tile_begin) * nt;
+                const int nstage = (pr.K + KT - 1) / KT;
+                prefetch_tmap(&pr.tmW);
+                prefetch_tmap(&pr.tmA);
+                prefetch_tmap(&pr.tmS);
+                // first tile: weights and scales of the first ring's worth of stages
+                // before the dependency wait, activations after it
+                const int early = waited ? 0 : min(nstage, ns);
+                for (int s = 0; s < early; s++) {
+                    const uint32_t full = full0 + 8 * s;
+                    const uint32_t st = smem_u32(smem) + s * L.stage_bytes;
+                    mbar_arrive_expect_tx(full, bytes);
+                    for (int b = 0; b < nt / 32; b++)
+                        tma_load_2d(st + b * WBOX, &pr.tmW, n0 + 32 * b, s * (KT / 8), full);
+                    tma_load_2d(st + L.w_bytes + L.a_bytes, &pr.tmS, n0, s * (KT / 128), full);
+                }
+                if (!waited) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    waited = true;
+                }
+                for (int s = 0; s < early; s++)
+                    tma_load_2d(smem_u32(smem) + s * L.stage_bytes + L.w_bytes, &pr.tmA, s * KT, 0, full0 + 8 * s);
+                it += early;
+                for (int s = early; s < nstage; s++, it++) {
+                    const int slot = it % ns;
+                    if (it >= (uint32_t)ns && !mbar_wait(empty0 + 8 * slot, ((it / ns) - 1) & 1, &g_w4a16_err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = full0 + 8 * slot;
+                    const uint32_t st = smem_u32(smem) + slot * L.stage_bytes;
+                    mbar_arrive_expect_tx(full, bytes);
+                    for (int b = 0; b < nt / 32; b++)
+                        tma_load_2d(st + b * WBOX, &pr.tmW, n0 + 32 * b, s * (KT / 8), full);
+                    tma_load_2d(st + L.w_bytes, &pr.tmA, s * KT, 0, full);
+                    tma_load_2d(st + L.w_bytes + L.a_bytes, &pr.tmS, n0, s * (KT / 128), full);
+                }
+            }
+            // every issued copy has landed before the CTA may exit
+            for (uint32_t j = it > (uint32_t)ns ? it - ns : 0; j < it; j++)
+                mbar_wait(full0 + 8 * (j % ns), (j / ns) & 1, &g_w4a16_err);
         }
     } else {
         // ------------------------------------------------- MMA warps
         const int g = lane >> 2, t = lane & 3;
-        const bool active = warp * 16 < ntv;
-        float acc[MB][4];
+        const int slice = warp % nslice, half = warp / nslice;   // half = scale group in each stage
+        const int c0 = 16 * (slice & 1) + g;
+        // swizzled byte offsets of columns c0 and c0 + 8 in rows with (row & 7) = 4 * par + t
+        uint32_t off[2][2];
 #pragma unroll
-        for (int mb = 0; mb < MB; mb++) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.0f;
+        for (int par = 0; par < 2; par++)
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int c = c0 + 8 * h;
+                off[par][h] = ((((uint32_t)c >> 2) ^ (uint32_t)(4 * par + t)) << 4) | (((uint32_t)c & 3u) << 2);
+            }
+        const uint32_t wrow = (uint32_t)(slice >> 1) * WBOX + (uint32_t)(16 * half + t) * 128u;
+        const uint32_t arow = (uint32_t)g * (KT * 2) + (uint32_t)(128 * half + 8 * t) * 2u;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+            const Prob& pr = P.p[find(tile)];
+            const int n0 = (tile - pr.tile_begin) * nt;
+            const int ntv = min(nt, pr.N - n0);          // valid columns (multiple of 32)
+            const bool active = slice * 16 < ntv;
+            const int nstage = (pr.K + KT - 1) / KT;
+            float acc[MB][4];
+#pragma unroll
+            for (int mb = 0; mb < MB; mb++) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.0f;
 
-        for (int s = 0; s < nstage; s++) {
-            const int slot = s % ns;
-            if (!mbar_wait(full0 + 8 * slot, (s / ns) & 1, &g_w4a16_err)) { ok = false; break; }
-            const int ngrp = min(KT, pr.K - s * KT) / 128;
-            if (active) {
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(sW + (size_t)slot * L.stage_bytes);
-                const uint8_t* a = sA + (size_t)slot * L.stage_bytes;
-                const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + (size_t)slot * L.stage_bytes);
-#pragma unroll
-                for (int grp = 0; grp < 2; grp++) {
-                    if (grp >= ngrp) break;
+            for (int s = 0; s < nstage; s++, it++) {
+                const int slot = it % ns;
+                if (!mbar_wait(full0 + 8 * slot, (it / ns) & 1, &g_w4a16_err)) { ok = false; break; }
+                if (active) {
+                    const uint8_t* st = smem + (size_t)slot * L.stage_bytes;
+                    const uint8_t* wb = st + wrow;
+                    const uint8_t* a = st + L.w_bytes + arow;
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + L.w_bytes + L.a_bytes);
                     float ag[MB][4];
 #pragma unroll
                     for (int mb = 0; mb < MB; mb++) ag[mb][0] = ag[mb][1] = ag[mb][2] = ag[mb][3] = 0.0f;
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        const int j = grp * 4 + c;                       // 32-deep chunk in the stage
-                        const uint32_t* wr = w + (size_t)(4 * j + t) * (nt_max + WPAD) + warp * 16 + g;
-                        const uint32_t u0 = wr[0] ^ 0x88888888u;         // column n
-                        const uint32_t u1 = wr[8] ^ 0x88888888u;         // column n + 8
-                        const uint32_t v0 = u0 >> 4, v1 = u1 >> 4;
-                        const uint32_t f0[4] = {nib_pair<0>(u0, v0), nib_pair<0>(u1, v1), nib_pair<1>(u0, v0),
-                                                nib_pair<1>(u1, v1)};
-                        const uint32_t f1[4] = {nib_pair<2>(u0, v0), nib_pair<2>(u1, v1), nib_pair<3>(u0, v0),
-                                                nib_pair<3>(u1, v1)};
+                    for (int c = 0; c < 4; c++) {                    // 32-deep chunks of this group
+                        const uint8_t* rowp = wb + c * 512;          // k-octet row 16*half + 4c + t
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(rowp + off[c & 1][0]);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(rowp + off[c & 1][1]);
+                        const uint32_t x0 = w0 >> 4, x1 = w1 >> 4;
+                        const uint32_t f0[4] = {nib_pair<0>(w0, x0), nib_pair<0>(w1, x1), nib_pair<1>(w0, x0),
+                                                nib_pair<1>(w1, x1)};
+                        const uint32_t f1[4] = {nib_pair<2>(w0, x0), nib_pair<2>(w1, x1), nib_pair<3>(w0, x0),
+                                                nib_pair<3>(w1, x1)};
 #pragma unroll
                         for (int mb = 0; mb < MB; mb++) {
-                            const uint4 b = *reinterpret_cast<const uint4*>(a + (mb * 8 + g) * AROW + (32 * j + 8 * t) * 2);
-                            mma_bf16(ag[mb], f0, b.x, b.y);
-                            mma_bf16(ag[mb], f1, b.z, b.w);
+                            const uint4 bv = *reinterpret_cast<const uint4*>(a + mb * 8 * (KT * 2) + c * 64);
+                            mma_bf16(ag[mb], f0, bv.x, bv.y);
+                            mma_bf16(ag[mb], f1, bv.z, bv.w);
                         }
                     }
-                    const float s0 = bf16_bits_to_f32(sc[grp * NTMAX + warp * 16 + g]);
-                    const float s1 = bf16_bits_to_f32(sc[grp * NTMAX + warp * 16 + g + 8]);
+                    const float s0 = bf16_bits_to_f32(sc[half * nt + slice * 16 + g]);
+                    const float s1 = bf16_bits_to_f32(sc[half * nt + slice * 16 + g + 8]);
 #pragma unroll
                     for (int mb = 0; mb < MB; mb++) {
                         acc[mb][0] = fmaf(s0, ag[mb][0], acc[mb][0]);
@@ -200,34 +263,52 @@ w4a16_kernel(const __grid_constant__ Params P, int nt_max, int ns) {
                         acc[mb][3] = fmaf(s1, ag[mb][3], acc[mb][3]);
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-        }
-        // ---- epilogue: stage the tile as bf16 [MT][NT] in shared memory (stage 0)
-        // after every warp has finished reading the pipeline buffers.
-        asm volatile("bar.sync 1, %0;" ::"r"(nwarps_c * 32) : "memory");
-        if (active && ok) {
-            __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(smem);
-            const int n = warp * 16 + g;
+            // ---- tile epilogue: group-0 warps store their sums, group-1 warps add
+            // theirs, then all MMA warps write the bf16 tile (rows < M, valid columns).
+            const int n = slice * 16 + g;
+            if (half == 0 && active && ok) {
 #pragma unroll
-            for (int mb = 0; mb < MB; mb++) {
-                const int m = mb * 8 + 2 * t;
-                ys[m * nt_max + n] = __float2bfloat16_rn(acc[mb][0]);
-                ys[(m + 1) * nt_max + n] = __float2bfloat16_rn(acc[mb][1]);
-                ys[m * nt_max + n + 8] = __float2bfloat16_rn(acc[mb][2]);
-                ys[(m + 1) * nt_max + n + 8] = __float2bfloat16_rn(acc[mb][3]);
+                for (int mb = 0; mb < MB; mb++) {
+                    const int m = mb * 8 + 2 * t;
+                    ybuf[m * L.y_pitch + n] = acc[mb][0];
+                    ybuf[(m + 1) * L.y_pitch + n] = acc[mb][1];
+                    ybuf[m * L.y_pitch + n + 8] = acc[mb][2];
+                    ybuf[(m + 1) * L.y_pitch + n + 8] = acc[mb][3];
+                }
             }
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(nwarps_c * 32) : "memory");
-        if (ok) {
-            const int vec_per_row = ntv / 8;                 // 16-byte vectors per output row
-            const int mrows = min(pr.M, MT);
-            for (int i = threadIdx.x; i < mrows * vec_per_row; i += nwarps_c * 32) {
-                const int m = i / vec_per_row, v = i - m * vec_per_row;
-                const uint4 val = *reinterpret_cast<const uint4*>(smem + ((size_t)m * nt_max + v * 8) * 2);
-                *reinterpret_cast<uint4*>(pr.Y + (size_t)m * pr.N + n0 + v * 8) = val;
+            asm volatile("bar.sync 1, %0;" ::"r"(nwarps_c * 32) : "memory");
+            if (half == 1 && active && ok) {
+#pragma unroll
+                for (int mb = 0; mb < MB; mb++) {
+                    const int m = mb * 8 + 2 * t;
+                    ybuf[m * L.y_pitch + n] += acc[mb][0];
+                    ybuf[(m + 1) * L.y_pitch + n] += acc[mb][1];
+                    ybuf[m * L.y_pitch + n + 8] += acc[mb][2];
+                    ybuf[(m + 1) * L.y_pitch + n + 8] += acc[mb][3];
+                }
             }
+            asm volatile("bar.sync 1, %0;" ::"r"(nwarps_c * 32) : "memory");
+            if (ok) {
+                const int vec_per_row = ntv / 8;             // 16-byte output vectors per row
+                const int mrows = min(pr.M, MT);
+                for (int i = threadIdx.x; i < mrows * vec_per_row; i += nwarps_c * 32) {
+                    const int m = i / vec_per_row, v = i - m * vec_per_row;
+                    const float4 lo4 = *reinterpret_cast<const float4*>(ybuf + m * L.y_pitch + v * 8);
+                    const float4 hi4 = *reinterpret_cast<const float4*>(ybuf + m * L.y_pitch + v * 8 + 4);
+                    uint4 o;
+                    __nv_bfloat162 b0 = __floats2bfloat162_rn(lo4.x, lo4.y), b1 = __floats2bfloat162_rn(lo4.z, lo4.w);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(hi4.x, hi4.y), b3 = __floats2bfloat162_rn(hi4.z, hi4.w);
+                    o.x = *reinterpret_cast<uint32_t*>(&b0);
+                    o.y = *reinterpret_cast<uint32_t*>(&b1);
+                    o.z = *reinterpret_cast<uint32_t*>(&b2);
+                    o.w = *reinterpret_cast<uint32_t*>(&b3);
+                    *reinterpret_cast<uint4*>(pr.Y + (size_t)m * pr.N + n0 + v * 8) = o;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(nwarps_c * 32) : "memory");
         }
     }
 }
@@ -235,15 +316,13 @@ w4a16_kernel(const __grid_constant__ Params P, int nt_max, int ns) {
 int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
 template <int MT>
-qz_status launch_mt(const Params& P, int total_ctas, int nt_max, cudaStream_t st) {
-    const int sms = num_sms();
-    // Few large tiles (about one per SM): deep pipeline, one CTA per SM.
-    // Many tiles: two CTAs per SM so one CTA's epilogue overlaps another's loads.
-    const int budget = total_ctas <= sms ? 200 * 1024 : 110 * 1024;
-    int ns = (int)(budget / Layout(nt_max, MT, 1).stage_bytes);
+qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
+    // One persistent CTA per SM (or per tile, if fewer), ring as deep as fits.
+    const Layout L(nt, MT);
+    const uint32_t budget = 200u * 1024u;
+    int ns = (int)((budget - 1024u - L.y_bytes) / (L.stage_bytes + 16u));
     ns = std::max(2, std::min(ns, 8));
-    const Layout L(nt_max, MT, ns);
-    const int smem = (int)L.smem_bytes();
+    const int smem = (int)L.smem_bytes(ns);
     static int smem_set[64];                       // per device: largest size opted in so far
     int dev = 0;
     cudaGetDevice(&dev);
@@ -253,9 +332,46 @@ qz_status launch_mt(const Params& P, int total_ctas, int nt_max, cudaStream_t st
             return QZ_ERR_CUDA;
         smem_set[dev] = smem;
     }
-    const int threads = (nt_max / 16 + 1) * 32;
-    w4a16_kernel<MT><<<total_ctas, threads, smem, st>>>(P, nt_max, ns);
+    const int threads = (2 * (nt / 16) + 1) * 32;
+    const int grid = std::min(P.total_tiles, num_sms());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w4a16_kernel<MT>, P, nt, ns) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
+}
+
+qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
+    Params P;                                     // the kernel parameter block (copied at launch)
+    int total = 0;
+    P.count = count;
+    for (int i = 0; i < count; i++) {
+        const qz_w4a16_problem& q = problems[i];
+        Prob& p = P.p[i];
+        if (!encode_tmap_2d(&p.tmW, q.qweight, 4, (uint64_t)q.N, (uint64_t)q.K / 8, (uint64_t)q.N * 4, 32, 32, true) ||
+            !encode_tmap_2d(&p.tmA, q.A, 2, (uint64_t)q.K, (uint64_t)q.M, (uint64_t)q.K * 2, KT, (uint32_t)mt, false) ||
+            !encode_tmap_2d(&p.tmS, q.scale_bf16, 2, (uint64_t)q.N, (uint64_t)q.K / 128, (uint64_t)q.N * 2,
+                            (uint32_t)nt, 2, false))
+            return QZ_ERR_CUDA;
+        p.Y = q.Y;
+        p.M = q.M; p.N = q.N; p.K = q.K;
+        p.tile_begin = total;
+        total += (q.N + nt - 1) / nt;
+    }
+    P.total_tiles = total;
+    switch (mt) {
+    case 8: return launch_mt<8>(P, nt, st);
+    case 16: return launch_mt<16>(P, nt, st);
+    case 32: return launch_mt<32>(P, nt, st);
+    default: return launch_mt<64>(P, nt, st);
+    }
 }
 
 } // namespace
@@ -270,37 +386,23 @@ qz_status w4a16_error_read_and_clear() {
 }
 
 qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, size_t, cudaStream_t st) {
-    Params P;          // the kernel parameter block (copied at launch)
     const int sms = num_sms();
     int mmax = 0;
     for (int i = 0; i < count; i++) mmax = std::max(mmax, problems[i].M);
-    // Tile width: with one problem, the smallest multiple of 16 giving at
-    // most one tile per SM (capped at 128 columns); grouped problems use 128.
-    int nt_max = NTMAX;
+    // Tile width: with one problem, the smallest multiple of 32 giving at most
+    // one tile per SM (capped at the widest tile for M); grouped problems use
+    // the widest tile.
+    const int mt = choose_mt(mmax);
+    int nt = ntmax_for(mt);
     if (count == 1) {
         const int N = problems[0].N;
-        nt_max = std::min(NTMAX, 16 * (int)((N + 16LL * sms - 1) / (16LL * sms)));
+        nt = std::min(nt, 32 * (int)((N + 32LL * sms - 1) / (32LL * sms)));
     }
-    int total = 0;
-    P.count = count;
-    for (int i = 0; i < count; i++) {
-        const qz_w4a16_problem& q = problems[i];
-        Prob& p = P.p[i];
-        p.A = q.A;
-        p.q = reinterpret_cast<const uint32_t*>(q.qweight);
-        p.s = q.scale_bf16;
-        p.Y = q.Y;
-        p.M = q.M; p.N = q.N; p.K = q.K;
-        p.nt = nt_max;
-        p.cta_begin = total;
-        total += (q.N + nt_max - 1) / nt_max;
+    for (int i = 0; i < count; i += PER_LAUNCH) {
+        const qz_status s = launch_chunk(problems + i, std::min(PER_LAUNCH, count - i), nt, mt, st);
+        if (s != QZ_OK) return s;
     }
-    switch (choose_mt(mmax)) {
-    case 8: return launch_mt<8>(P, total, nt_max, st);
-    case 16: return launch_mt<16>(P, total, nt_max, st);
-    case 32: return launch_mt<32>(P, total, nt_max, st);
-    default: return launch_mt<64>(P, total, nt_max, st);
-    }
+    return QZ_OK;
 }
 
 } // namespace qz

@@ -25,6 +25,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+// Programmatic dependent launch: the amax kernel lets its dependent (the
+// encoder) start once every CTA has stored its partial; the encoder waits for
+// the amax kernel's results before reading the partials (a no-op when it was
+// launched without a programmatic dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // CTA-wide max of a per-thread value; every thread gets the result.
 __device__ __forceinline__ float block_max(float v, float* red) {
     v = warp_max(v, 32);
@@ -46,7 +53,7 @@ __device__ __forceinline__ uint32_t fp8_code(float x, float s) {
 }
 
 __device__ __forceinline__ float fp8_scale(float amax) {
-    return div_rn(fmaxf(amax, kAmaxMin), kFp8Max);
+    return div1(fmaxf(amax, kAmaxMin), Recip(kFp8Max));     // max(amax, 1e-12) / 448, correctly rounded
 }
 
 // Encode 8 values with scale d.s; write 8 code bytes (and 8 dequantized
@@ -55,13 +62,7 @@ __device__ __forceinline__ float fp8_scale(float amax) {
 __device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, uint8_t* codes, float* deq) {
     float y[8];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        y[j] = v[j];
-        y[j + 1] = v[j + 1];
-        div2(y[j], y[j + 1], d);
-        y[j] = sign_of(y[j], v[j]);
-        y[j + 1] = sign_of(y[j + 1], v[j + 1]);
-    }
+    for (int j = 0; j < 8; j++) y[j] = sign_of(div1(v[j], d), v[j]);
     uint32_t p[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) p[j] = e4m3x2(y[2 * j], y[2 * j + 1]);
@@ -80,15 +81,12 @@ __device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, ui
 
 // Encode 8 values to E2M1 with scale d.s (correctly rounded quotients);
 // returns 8 nibbles, element j at bits 4j..4j+3; writes dequant if asked.
+// Warp-collective (the tie screen votes): all 32 lanes call it together.
 __device__ __forceinline__ uint32_t fp4_encode8(const float v[8], const Recip& d, float* deq) {
     float y[8];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        y[j] = v[j];
-        y[j + 1] = v[j + 1];
-        div2(y[j], y[j + 1], d);
-    }
-    const uint32_t packed = e2m1x8(y);
+    for (int j = 0; j < 8; j++) y[j] = div1(v[j], d);
+    const uint32_t packed = e2m1x8_screened(y);     // quotients by an arbitrary scale: ties are rare
     if (deq) {
         float o[8];
 #pragma unroll
@@ -108,8 +106,10 @@ __device__ __forceinline__ int64_t chunk_offset(int64_t i, bool contig, int64_t 
     return r * ldx + (i - r * cpr) * E;
 }
 
-// Loads per thread kept in flight by the streaming kernels.
+// Loads per thread kept in flight by the streaming kernels (amax pass, and the
+// warp-uniform encoders: chunks of 8 elements per lane per iteration).
 constexpr int U = 4;
+constexpr int UQ = 4;
 
 // ------------------------------------------------------ per-tensor amax
 
@@ -150,9 +150,11 @@ amax_partial_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t 
     }
     m = block_max(m, red);
     if (threadIdx.x == 0) partial[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = m;
+    pdl_trigger();
 }
 
 __device__ __forceinline__ float reduce_partials(const float* __restrict__ p, int n, float* red) {
+    pdl_wait();
     float m = 0.0f;
     for (int i = threadIdx.x; i < n; i += kThreads) m = fmaxf(m, __ldcg(p + i));
     return block_max(m, red);
@@ -300,18 +302,18 @@ fp8_group_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ld
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * (32 * UQ);
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * UQ;
     for (int64_t base = wbase; base < total; base += wstride) {
-        float v[2][8];
+        float v[UQ][8];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
             else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             float m = 0.0f;
 #pragma unroll
@@ -405,18 +407,18 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * (32 * UQ);
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * UQ;
     for (int64_t base = wbase; base < total; base += wstride) {
-        float v[2][8];
+        float v[UQ][8];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
             else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             float m = 0.0f;
 #pragma unroll
@@ -428,8 +430,8 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
             if (i < total) {
                 float y[8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) y[j] = __fmul_rn(v[u][j], inv);
-                const uint32_t packed = e2m1x8(y);
+                for (int j = 0; j < 8; j++) y[j] = __fadd_rn(__fmul_rn(v[u][j], inv), 0.0f);
+                const uint32_t packed = e2m1x8_fix(e2m1x8_rne(y), y);
                 reinterpret_cast<uint32_t*>(codes)[i] = packed;
                 if (deq) {
                     float o[8];
@@ -458,39 +460,41 @@ nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
     const float amax_t = partial ? reduce_partials(partial, nparts, red) : __ldg(amax_in);
     const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
-    const Recip dg(g);
+    const Recip dg(g), d6(kFp4Max);
     const int lane = threadIdx.x & 31;
     const int64_t cpr = cols / 8;
     const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 64;
-    const int64_t wstride = (int64_t)gridDim.x * kThreads * 2;
+    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * (32 * UQ);
+    const int64_t wstride = (int64_t)gridDim.x * kThreads * UQ;
     for (int64_t base = wbase; base < total; base += wstride) {
-        float v[2][8];
+        float v[UQ][8];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
             else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < UQ; u++) {
             const int64_t i = base + u * 32 + lane;
             float m = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
             m = warp_max(m, 2);
-            // t = (amax16 / 6) / g, both divisions correctly rounded
-            const float t = div_rn(div_rn(m, kFp4Max), g);
+            // t = (amax16 / 6) / g, both quotients correctly rounded
+            const float t = div1(div1(m, d6), dg);
             const uint32_t bcode = e4m3_code(t);                 // saturating, as the clamp-free page
             const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
-            if (i < total) {
-                const uint32_t packed = fp4_encode8(v[u], Recip(s), deq ? deq + i * 8 : nullptr);
+            // every lane encodes (the tie screen votes across the warp); lanes
+            // past the end hold zeros and store nothing
+            const bool live = i < total;
+            const uint32_t packed = fp4_encode8(v[u], Recip(s), (deq && live) ? deq + i * 8 : nullptr);
+            if (live) {
                 reinterpret_cast<uint32_t*>(codes)[i] = packed;
                 if ((lane & 1) == 0) sb[i >> 1] = (uint8_t)bcode;
             }
         }
     }
-    (void)dg;
 }
 
 // --------------------------------------------------------------- INT4 g128
@@ -557,9 +561,26 @@ int4_g128_kernel(const T* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
 
 int amax_grid() { return num_sms() * 4; }
 
+// Launch `kernel` so that it may start while the previous kernel on the stream
+// finishes (it must call pdl_wait before consuming that kernel's results).
+template <typename... KArgs, typename... Args>
+void launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 int stream_grid(int64_t threads_needed) {
     const int64_t ctas = (threads_needed + kThreads - 1) / kThreads;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * 8));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * 4));   // one wave of resident CTAs
 }
 
 bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
@@ -591,16 +612,17 @@ static qz_status fp8_launch_t(const T* x, int64_t rows, int64_t cols, int64_t ld
         float* partial = (float*)ws;
         const int np = amax_grid();
         const int64_t work = vec ? rows * cols / 8 : rows * cols;
+        const float* none = nullptr;
         if (vec) {
             launch_tensor_amax<T, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-            fp8_tensor_encode_kernel<T, true, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
-                x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
-                scales, deq, deq);
+            launch_dependent(fp8_tensor_encode_kernel<T, true, false>, dim3(stream_grid(work), 1), dim3(kThreads), st,
+                             x, x, rows, cols, ldx, contig, (const float*)partial, np, none, none, codes, codes,
+                             scales, scales, deq, deq);
         } else {
             launch_tensor_amax<T, false>(x, x, 1, rows, cols, ldx, contig, partial, st);
-            fp8_tensor_encode_kernel<T, false, false><<<dim3(stream_grid(work), 1), kThreads, 0, st>>>(
-                x, x, rows, cols, ldx, contig, partial, np, nullptr, nullptr, codes, codes, scales,
-                scales, deq, deq);
+            launch_dependent(fp8_tensor_encode_kernel<T, false, false>, dim3(stream_grid(work), 1), dim3(kThreads),
+                             st, x, x, rows, cols, ldx, contig, (const float*)partial, np, none, none, codes,
+                             codes, scales, scales, deq, deq);
         }
         break;
     }
@@ -652,14 +674,15 @@ qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_
     float* partial = amax_in ? nullptr : (float*)ws;
     const int np = amax_grid();
     const int grid = stream_grid(rows * cols / 8);
+    const float* cpart = partial;
     if (xt == QZ_F32) {
         if (partial) launch_tensor_amax<float, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-        nvfp4_kernel<float><<<grid, kThreads, 0, st>>>((const float*)x, rows, cols, ldx, contig, partial, np,
-                                                       amax_in, codes, sb, g, deq);
+        launch_dependent(nvfp4_kernel<float>, dim3(grid), dim3(kThreads), st, (const float*)x, rows, cols, ldx,
+                         contig, cpart, np, amax_in, codes, sb, g, deq);
     } else {
         if (partial) launch_tensor_amax<uint16_t, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-        nvfp4_kernel<uint16_t><<<grid, kThreads, 0, st>>>((const uint16_t*)x, rows, cols, ldx, contig, partial,
-                                                          np, amax_in, codes, sb, g, deq);
+        launch_dependent(nvfp4_kernel<uint16_t>, dim3(grid), dim3(kThreads), st, (const uint16_t*)x, rows, cols,
+                         ldx, contig, cpart, np, amax_in, codes, sb, g, deq);
     }
     return launch_status();
 }
@@ -680,9 +703,11 @@ qz_status kv_write_launch(const uint16_t* k, const uint16_t* v, int64_t n, uint8
     float* partial = (mode == QZ_SCALE_COMPUTE) ? (float*)ws : nullptr;
     const dim3 grid(stream_grid(n / 8), 2);
     if (partial) {
+        const float* none = nullptr;
+        float* nod = nullptr;
         launch_tensor_amax<uint16_t, true>(k, v, 2, 1, n, n, true, partial, st);
-        fp8_tensor_encode_kernel<uint16_t, true, false><<<grid, kThreads, 0, st>>>(
-            k, v, 1, n, n, true, partial, np, nullptr, nullptr, kc, vc, ks, vs, nullptr, nullptr);
+        launch_dependent(fp8_tensor_encode_kernel<uint16_t, true, false>, grid, dim3(kThreads), st, k, v, (int64_t)1,
+                         n, n, true, (const float*)partial, np, none, none, kc, vc, ks, vs, nod, nod);
     } else {
         fp8_tensor_encode_kernel<uint16_t, true, true><<<grid, kThreads, 0, st>>>(
             k, v, 1, n, n, true, nullptr, np, ks, vs, kc, vc, nullptr, nullptr, nullptr, nullptr);

@@ -68,7 +68,7 @@ struct Recip {
     float s, r;
     __device__ __forceinline__ explicit Recip(float s_) {
         s = s_;
-        r = __fdiv_rn(1.0f, s_);
+        r = __frcp_rn(s_);                     // correctly rounded reciprocal
     }
 };
 
@@ -91,39 +91,61 @@ __device__ __forceinline__ void div2(float& a, float& b, const Recip& d) {
     f2_unpack(q1, a, b);
 }
 
+// One correctly rounded quotient x / d.s (same method as div2), x >= 0.
+__device__ __forceinline__ float div1(float x, const Recip& d) {
+    const float q0 = __fmul_rn(x, d.r);
+    const float rem = __fmaf_rn(-q0, d.s, x);
+    return __fmaf_rn(rem, d.r, q0);
+}
+
 // y with the sign bit of x (a non-zero quotient already has it; fixes -0).
 __device__ __forceinline__ float sign_of(float y, float x) {
     return __uint_as_float(__float_as_uint(y) | (__float_as_uint(x) & 0x80000000u));
 }
 
-// Eight E2M1 codes (element j in bits 4j..4j+3) of quotients y[8]: the
-// hardware conversion (round to nearest even, saturating to 6) agrees with
-// the nearest-value rule except at an exact midpoint, where the rule takes the
-// smaller magnitude. Midpoints (0.25 .. 5) carry at most two mantissa bits, so
-// lanes whose quotients all have non-zero low mantissa bits skip the exact
-// recount.
-__device__ __forceinline__ uint32_t e2m1x8(const float y[8]) {
+// Eight E2M1 codes (element j in bits 4j..4j+3) of quotients y[8], by the
+// hardware conversion: round to nearest even, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float y[8]) {
     uint32_t w = 0;
-    bool maybe_tie = false;
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
         uint16_t b;
         asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
             : "=h"(b) : "f"(y[j + 1]), "f"(y[j]));
         w |= (uint32_t)(b & 0xFF) << (4 * j);
-        maybe_tie |= (__float_as_uint(y[j]) & 0x1FFFFFu) == 0u;
-        maybe_tie |= (__float_as_uint(y[j + 1]) & 0x1FFFFFu) == 0u;
     }
-    if (maybe_tie) {
-        w = 0;
+    return w;
+}
+
+// The pages' rule (first index of the minimum distance) differs from round to
+// nearest even only at exact midpoints, and only where round-to-even goes up:
+// 0.75, 1.75 and 3.5 (0.25, 1.25, 2.5 and 5 already round down to an even
+// code). Each such element steps down by one (its code is 2, 4 or 6, so the
+// nibble never borrows). The sign bit is (y < 0): an exact -0.0 encodes as +0.
+__device__ __forceinline__ uint32_t e2m1x8_fix(uint32_t w, const float y[8]) {
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const float a = fabsf(y[j]);
-            const uint32_t m = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) + (a > 2.5f) +
-                               (a > 3.5f) + (a > 5.0f);
-            w |= (m | (y[j] < 0.0f ? 8u : 0u)) << (4 * j);
-        }
+    for (int j = 0; j < 8; j++) {
+        const uint32_t u = __float_as_uint(y[j]);
+        const uint32_t a = u & 0x7FFFFFFFu;
+        if ((a == 0x3F400000u) | (a == 0x3FE00000u) | (a == 0x40600000u)) w -= 1u << (4 * j);
+        if (u == 0x80000000u) w -= 8u << (4 * j);
     }
+    return w;
+}
+
+// Exact E2M1 codes of y[8] (pages' rule).
+__device__ __forceinline__ uint32_t e2m1x8(const float y[8]) { return e2m1x8_fix(e2m1x8_rne(y), y); }
+
+// Same result for quotients whose exact midpoints are rare (a division by an
+// arbitrary scale): midpoints carry at most two mantissa bits, so the exact fix
+// runs only when some lane of the warp holds a quotient with zero low mantissa
+// bits. All 32 lanes must call it together.
+__device__ __forceinline__ uint32_t e2m1x8_screened(const float y[8]) {
+    uint32_t w = e2m1x8_rne(y);
+    bool cand = false;
+#pragma unroll
+    for (int j = 0; j < 8; j++) cand |= (__float_as_uint(y[j]) & 0x1FFFFFu) == 0u;
+    if (__any_sync(0xffffffffu, cand)) w = e2m1x8_fix(w, y);
     return w;
 }
 
@@ -143,18 +165,8 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
 }
 
-// E4M3 code of one fp32 already clamped to +-448.
+// E4M3 code of one fp32 (saturating at +-448).
 __device__ __forceinline__ uint32_t e4m3_code(float y) { return e4m3x2(y, 0.0f) & 0xFF; }
-
-// E2M1 code of y: the nearest grid magnitude, an exact midpoint going to the
-// smaller magnitude (first index of the minimum distance), sign bit = (y < 0).
-// Magnitudes above 6 give code 7 (the clamp to +-6 of the fake-quant).
-__device__ __forceinline__ uint32_t e2m1_code(float y) {
-    float a = fabsf(y);
-    uint32_t m = (a > 0.25f) + (a > 0.75f) + (a > 1.25f) + (a > 1.75f) +
-                 (a > 2.5f) + (a > 3.5f) + (a > 5.0f);
-    return m | (y < 0.0f ? 8u : 0u);
-}
 
 // Value of a 4-bit E2M1 code (sign bit 3) as fp32; code 8 gives -0.0.
 __device__ __forceinline__ float e2m1_value(uint32_t c) {
