@@ -17,13 +17,11 @@
 //              (M=128, N=256, K=32) per K block into one of two TMEM
 //              accumulators (2 x 256 columns), committed to the stage's
 //              "empty" barrier and the accumulator's "full" barrier.
-//  warps 2-17  promotion + epilogue: each thread owns one output row and 64
+//  warps 2-9   promotion + epilogue: each thread owns one output row and 128
 //              columns; per K block it loads its partial sums from TMEM
 //              (tcgen05.ld), multiplies by sA*sB and adds into fp32 registers,
 //              then frees the accumulator; at the end of the tile it rounds
-//              to bf16 and stores. Sixteen warps (four per TMEM lane quarter)
-//              keep enough TMEM loads in flight to promote a K block in less
-//              time than its MMAs take.
+//              to bf16 and stores.
 // The MMA of K block kb+1 runs while block kb is being promoted.
 //
 // When M spans an even number of 128-row tiles, CTAs run in clusters of two
@@ -46,8 +44,9 @@ constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
 constexpr int A_BYTES = BM * BK;                  // 16 KB
 constexpr int B_BYTES = BN * BK;                  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 16;
+constexpr int EPI_WARPS = 8;
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per promotion thread
+constexpr int SD = 2;                            // K blocks of scales kept in flight
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
@@ -172,24 +171,24 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             float acc[EPI_COLS];
 #pragma unroll
             for (int i = 0; i < EPI_COLS; i++) acc[i] = 0.0f;
-            // Scales of the next two K blocks stay in flight as raw loads (an L2
+            // Scales of the next SD K blocks stay in flight as raw loads (an L2
             // round trip is longer than one block's MMAs); each is multiplied out
             // only when its block is promoted, so no load is waited on early.
-            float ra[2], rb[2];
+            float ra[SD], rb[SD];
 #pragma unroll
-            for (int u = 0; u < 2; u++) {
+            for (int u = 0; u < SD; u++) {
                 ra[u] = u < nkb ? __ldg(sa_row + u) : 0.0f;
                 rb[u] = u < nkb ? __ldg(sb_row + u) : 0.0f;
             }
-            for (int kb0 = 0; kb0 < nkb && ok; kb0 += 2) {
+            for (int kb0 = 0; kb0 < nkb && ok; kb0 += SD) {
 #pragma unroll
-                for (int u = 0; u < 2; u++) {
+                for (int u = 0; u < SD; u++) {
                     const int kb = kb0 + u;
                     if (kb >= nkb || !ok) break;
                     const float scale = ra[u] * rb[u];
-                    if (kb + 2 < nkb) {
-                        ra[u] = __ldg(sa_row + kb + 2);
-                        rb[u] = __ldg(sb_row + kb + 2);
+                    if (kb + SD < nkb) {
+                        ra[u] = __ldg(sa_row + kb + SD);
+                        rb[u] = __ldg(sb_row + kb + SD);
                     }
                     const int b = ac & 1;
                     if (!mbar_wait(tfull(b), (ac >> 1) & 1, &g_fp8_err)) { ok = false; break; }

@@ -5,29 +5,38 @@
 // is the weight bytes read from HBM, so the kernel streams the packed
 // weights exactly once and does the rest on chip.
 //
-// Design (one GB300, sm_103a):
+// Two kernels share the arithmetic below:
+//  * up to 16 tokens (decode): w4a16_rd_kernel, register-direct. A CTA owns 32
+//    weight columns; its 8 warps split K by 128-deep scale groups. Each lane
+//    loads the packed weights with one coalesced 16-byte load per k-octet row
+//    (4 consecutive columns), two groups ahead of the math, straight into
+//    registers: no shared-memory staging, so many small CTAs share each SM,
+//    their loads overlap, and the next launch's CTAs start as soon as any
+//    of these finish. The warps' partial sums meet in shared memory and are
+//    added in a fixed order.
+//  * 17 to 64 tokens: w4a16_kernel, persistent CTAs (at most one per SM) walking
+//    tiles of NT weight columns x the whole K range, fed by a producer thread
+//    that stages 256-deep K slices through an mbarrier ring with 2-D tensor TMA
+//    (weights as 32-column x 32-row boxes with the 128-byte swizzle,
+//    activations as one 256 x MT box, scales as one NT x 2 box). Two MMA
+//    warps share each 16-column slice, one per 128-deep scale group of every
+//    stage. Grouped launches (a decoder step's linears) stream all problems'
+//    tiles through one pipeline.
+// Common to both:
 //  * swap A and B: the MMA computes Y^T = W^T A^T, so 16 weight columns fill
-//    the MMA's 16-row side and up to 8 tokens its 8-wide side; M <= 64 tokens
-//    take MT/8 MMAs per weight fragment (mma.m16n8k16, bf16 in, fp32 out).
-//  * persistent CTAs (at most one per SM) walk a list of tiles of NT weight
-//    columns x the whole K range; NT is chosen so that a single problem has
-//    about one tile per SM (no split-K across CTAs, no scratch memory), and
-//    grouped launches (a decoder step's linears) stream all problems' tiles
-//    through one warm pipeline. Two MMA warps share each 16-column slice,
-//    one per 128-deep scale group of every stage, and add their sums in
-//    shared memory at the end of the tile.
-//  * a producer thread stages 256-deep K slices through an mbarrier ring with
-//    2-D tensor TMA: the packed weights as 32-column x 32-row boxes (4 KB,
-//    128-byte swizzle), the activations as one 256 x MT box (rows beyond M
-//    and K beyond the end read as zero) and the scales as one NT x 2 box --
-//    a handful of large copies per stage, so the copy engine keeps HBM busy.
+//    the MMA's 16-row side and up to 8 tokens its 8-wide side (mma.m16n8k16,
+//    bf16 in, fp32 out; MT/8 MMAs per weight fragment).
 //  * the INT4 codes are exact integers in bf16, so each 128-deep group is
 //    multiplied exactly and the fp32 group sum is scaled by its bf16 scale
 //    (folding the scale into bf16 weights would round).
+//  * in the register-direct kernel the unpack stops at the biased code v = q + 136
+//    (exact in bf16) and the MMA sums a*v; a second MMA of the activations
+//    against a fragment of ones gives sum(a) over the same k, and the group
+//    sum is sum(a*v) - 136*sum(a). That drops one bf16x2 FMA per code pair.
 //  * k inside a 32-deep chunk is permuted consistently for both operands:
-//    thread (g, t) takes the whole packed word of k-octet t, so one 32-bit
-//    shared load feeds two MMA k-steps, and the matching activations are 8
-//    consecutive bf16 (one 16-byte load).
+//    thread (g, t) takes the whole packed word of k-octet t, so one word feeds
+//    two MMA k-steps, and the matching activations are 8 consecutive bf16
+//    (one 16-byte load).
 #include "qz_tc.cuh"
 
 #include <cuda_bf16.h>
@@ -40,11 +49,9 @@ namespace {
 __device__ unsigned int g_w4a16_err;
 
 constexpr int KT = 256;                 // K per pipeline stage (two scale groups)
-constexpr int NTMAX = 128;              // widest tile (16 MMA warps)
 
-// Widest tile for an MT-token kernel: more tokens need more accumulator
-// registers, so fewer (wider-register) MMA warps.
-__host__ __device__ constexpr int ntmax_for(int mt) { return mt <= 16 ? 128 : 64; }
+// Widest tile of the TMA-staged kernel (17 to 64 tokens): 64 columns, 8 MMA warps.
+__host__ __device__ constexpr int ntmax_for(int) { return 64; }
 constexpr int PER_LAUNCH = 56;          // problems per launch (kernel parameter space: 32 KB)
 constexpr int WBOX = 4096;              // one 32-column x 32-row weight box
 
@@ -108,6 +115,183 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t w4) {
 __device__ __forceinline__ uint32_t wbox_word(const uint8_t* box, int r, int c) {
     return *reinterpret_cast<const uint32_t*>(box + r * 128 + ((((c >> 2) ^ (r & 7)) << 4) | ((c & 3) << 2)));
 }
+
+// ------------------------------------------------ register-direct kernel
+
+constexpr int RD_COLS = 32;             // weight columns per CTA
+constexpr int RD_WARPS = 8;             // warps per CTA, taking 128-deep groups round-robin
+constexpr int RD_MAX_PROBLEMS = 256;    // problems per launch (kernel parameter space: 32 KB)
+
+struct RdProb {
+    const uint16_t* A;                  // bf16 [M, K]
+    const uint4* W;                     // qweight [K/8, N] int32, as 16-byte quads of columns
+    const uint16_t* S;                  // bf16 [K/128, N]
+    uint16_t* Y;                        // bf16 [M, N]
+    int M, N, K;
+    int cta_begin;                      // first CTA of this problem
+};
+
+struct RdParams {
+    RdProb p[RD_MAX_PROBLEMS];
+    int count;
+};
+
+// Biased unpack: bf16x2 (q_even + 136, q_odd + 136) of byte B of w (w4 = w >> 4).
+template <int B>
+__device__ __forceinline__ uint32_t nib_pair_biased(uint32_t w, uint32_t w4) {
+    const uint32_t r = __byte_perm(w, w4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43084308u));
+    return v;
+}
+
+// Weights of one 128-deep group for one lane: k-octet rows 4c + t (c = 0..3),
+// columns 4g .. 4g+3 of the CTA's 32, and the group's 4 scales of those columns.
+struct RdGroup {
+    uint4 w[4];
+    uint2 s;
+};
+
+__device__ __forceinline__ void rd_load(RdGroup& G, const RdProb& pr, int n0, int grp, int g, int t) {
+    const int nq = pr.N >> 2;                                     // 16-byte quads per row
+    const uint4* base = pr.W + (size_t)(grp * 16 + t) * nq + ((n0 >> 2) + g);
+#pragma unroll
+    for (int c = 0; c < 4; c++) {                                  // streamed once: no L1 allocation
+        const uint4* q = base + (size_t)(4 * c) * nq;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(G.w[c].x), "=r"(G.w[c].y), "=r"(G.w[c].z), "=r"(G.w[c].w) : "l"(q));
+    }
+    G.s = __ldg(reinterpret_cast<const uint2*>(pr.S + (size_t)grp * pr.N + n0 + 4 * g));
+}
+
+template <int MT>
+__global__ void __launch_bounds__(RD_WARPS * 32, MT <= 8 ? 3 : 2)
+w4a16_rd_kernel(const __grid_constant__ RdParams P) {
+    constexpr int MB = MT / 8;
+    __shared__ float red[RD_WARPS][MT][RD_COLS + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    int lo = 0, hi = P.count - 1;                                  // last problem with cta_begin <= blockIdx.x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.p[mid].cta_begin <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const RdProb& pr = P.p[lo];
+    const int n0 = ((int)blockIdx.x - pr.cta_begin) * RD_COLS;
+    const int ngroups = pr.K >> 7;
+    // Programmatic dependent launch: the next kernel may start as SMs free up;
+    // this one loads its first weights before waiting for the previous kernel
+    // (whose output may be this kernel's activations).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // Ask L2 for the CTA's whole weight and scale range at once (one 128-byte
+    // line per k-octet row, one 64-byte segment per scale row): HBM then streams
+    // at full rate while the register loads below find their lines in flight
+    // or already in L2.
+    {
+        const int nq = pr.N >> 2;
+        const int rows = pr.K >> 3;
+        for (int r = threadIdx.x; r < rows; r += RD_WARPS * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(pr.W + (size_t)r * nq + (n0 >> 2)));
+        for (int r = threadIdx.x; r < ngroups; r += RD_WARPS * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(pr.S + (size_t)r * pr.N + n0));
+    }
+
+    float acc[2][MB][4];
+#pragma unroll
+    for (int sl = 0; sl < 2; sl++)
+#pragma unroll
+        for (int mb = 0; mb < MB; mb++) acc[sl][mb][0] = acc[sl][mb][1] = acc[sl][mb][2] = acc[sl][mb][3] = 0.0f;
+
+    RdGroup cur, nxt;
+    int grp = warp;
+    if (grp < ngroups) rd_load(cur, pr, n0, grp, g, t);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint16_t* arow[MB];
+    bool live[MB];
+#pragma unroll
+    for (int mb = 0; mb < MB; mb++) {
+        live[mb] = mb * 8 + g < pr.M;
+        arow[mb] = pr.A + (size_t)(live[mb] ? mb * 8 + g : 0) * pr.K + 8 * t;
+    }
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+    for (; grp < ngroups; grp += RD_WARPS) {
+        if (grp + RD_WARPS < ngroups) rd_load(nxt, pr, n0, grp + RD_WARPS, g, t);   // next group in flight
+        float ag[2][MB][4], sg[MB][4];
+#pragma unroll
+        for (int mb = 0; mb < MB; mb++) {
+            sg[mb][0] = sg[mb][1] = sg[mb][2] = sg[mb][3] = 0.0f;
+#pragma unroll
+            for (int sl = 0; sl < 2; sl++) ag[sl][mb][0] = ag[sl][mb][1] = ag[sl][mb][2] = ag[sl][mb][3] = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; c++) {                             // 32-deep chunks of the group
+            uint4 bv[MB];
+#pragma unroll
+            for (int mb = 0; mb < MB; mb++) {                      // 8 activations of token mb*8+g
+                bv[mb] = live[mb] ? __ldg(reinterpret_cast<const uint4*>(arow[mb] + grp * 128 + 32 * c))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            }
+            const uint32_t wq[4] = {cur.w[c].x, cur.w[c].y, cur.w[c].z, cur.w[c].w};
+#pragma unroll
+            for (int sl = 0; sl < 2; sl++) {                       // MMA rows g, g+8 = columns 4g+2sl, 4g+2sl+1
+                const uint32_t w0 = wq[2 * sl], w1 = wq[2 * sl + 1];
+                const uint32_t x0 = w0 >> 4, x1 = w1 >> 4;
+                const uint32_t f0[4] = {nib_pair_biased<0>(w0, x0), nib_pair_biased<0>(w1, x1),
+                                        nib_pair_biased<1>(w0, x0), nib_pair_biased<1>(w1, x1)};
+                const uint32_t f1[4] = {nib_pair_biased<2>(w0, x0), nib_pair_biased<2>(w1, x1),
+                                        nib_pair_biased<3>(w0, x0), nib_pair_biased<3>(w1, x1)};
+#pragma unroll
+                for (int mb = 0; mb < MB; mb++) {
+                    mma_bf16(ag[sl][mb], f0, bv[mb].x, bv[mb].y);
+                    mma_bf16(ag[sl][mb], f1, bv[mb].z, bv[mb].w);
+                }
+            }
+#pragma unroll
+            for (int mb = 0; mb < MB; mb++) {                      // sum(a) of tokens 2t, 2t+1
+                mma_bf16(sg[mb], ones, bv[mb].x, bv[mb].y);
+                mma_bf16(sg[mb], ones, bv[mb].z, bv[mb].w);
+            }
+        }
+        const float sc[4] = {bf16_bits_to_f32(cur.s.x & 0xFFFFu), bf16_bits_to_f32(cur.s.x >> 16),
+                             bf16_bits_to_f32(cur.s.y & 0xFFFFu), bf16_bits_to_f32(cur.s.y >> 16)};
+#pragma unroll
+        for (int sl = 0; sl < 2; sl++)
+#pragma unroll
+            for (int mb = 0; mb < MB; mb++) {                      // remove the bias, scale, accumulate
+                acc[sl][mb][0] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[mb][0], ag[sl][mb][0]), acc[sl][mb][0]);
+                acc[sl][mb][1] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[mb][1], ag[sl][mb][1]), acc[sl][mb][1]);
+                acc[sl][mb][2] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][0], ag[sl][mb][2]), acc[sl][mb][2]);
+                acc[sl][mb][3] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][1], ag[sl][mb][3]), acc[sl][mb][3]);
+            }
+        cur = nxt;
+    }
+    // partial sums of this warp -> shared memory; fixed-order sum over warps
+#pragma unroll
+    for (int sl = 0; sl < 2; sl++)
+#pragma unroll
+        for (int mb = 0; mb < MB; mb++) {
+            const int m = mb * 8 + 2 * t, col = 4 * g + 2 * sl;
+            red[warp][m][col] = acc[sl][mb][0];
+            red[warp][m + 1][col] = acc[sl][mb][1];
+            red[warp][m][col + 1] = acc[sl][mb][2];
+            red[warp][m + 1][col + 1] = acc[sl][mb][3];
+        }
+    __syncthreads();
+    const int mrows = min(pr.M, MT);
+    for (int i = threadIdx.x; i < mrows * (RD_COLS / 2); i += RD_WARPS * 32) {
+        const int m = i / (RD_COLS / 2), col = 2 * (i % (RD_COLS / 2));
+        float y0 = red[0][m][col], y1 = red[0][m][col + 1];
+#pragma unroll
+        for (int w = 1; w < RD_WARPS; w++) {
+            y0 += red[w][m][col];
+            y1 += red[w][m][col + 1];
+        }
+        const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
+        *reinterpret_cast<__nv_bfloat162*>(pr.Y + (size_t)m * pr.N + n0 + col) = o;
+    }
+}
+
+// ------------------------------------------------ TMA-staged kernel
 
 template <int MT>
 __global__ void __launch_bounds__((2 * ntmax_for(MT) / 16 + 1) * 32, 1)
@@ -315,6 +499,38 @@ w4a16_kernel(const __grid_constant__ Params P, int nt, int ns) {
 
 int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
+// Register-direct launch for up to 16 tokens: one CTA per 32 columns of every
+// problem, programmatic dependent launch.
+template <int MT>
+qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+    RdParams P;                                   // the kernel parameter block (copied at launch)
+    int total = 0;
+    P.count = count;
+    for (int i = 0; i < count; i++) {
+        const qz_w4a16_problem& q = problems[i];
+        RdProb& p = P.p[i];
+        p.A = q.A;
+        p.W = reinterpret_cast<const uint4*>(q.qweight);
+        p.S = q.scale_bf16;
+        p.Y = q.Y;
+        p.M = q.M; p.N = q.N; p.K = q.K;
+        p.cta_begin = total;
+        total += q.N / RD_COLS;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(total);
+    cfg.blockDim = dim3(RD_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT>, P) != cudaSuccess) return QZ_ERR_CUDA;
+    return launch_status();
+}
+
 template <int MT>
 qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
     // One persistent CTA per SM (or per tile, if fewer), ring as deep as fits.
@@ -366,12 +582,7 @@ qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int 
         total += (q.N + nt - 1) / nt;
     }
     P.total_tiles = total;
-    switch (mt) {
-    case 8: return launch_mt<8>(P, nt, st);
-    case 16: return launch_mt<16>(P, nt, st);
-    case 32: return launch_mt<32>(P, nt, st);
-    default: return launch_mt<64>(P, nt, st);
-    }
+    return mt == 32 ? launch_mt<32>(P, nt, st) : launch_mt<64>(P, nt, st);
 }
 
 } // namespace
@@ -393,6 +604,14 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     // one tile per SM (capped at the widest tile for M); grouped problems use
     // the widest tile.
     const int mt = choose_mt(mmax);
+    if (mt <= 16) {
+        for (int i = 0; i < count; i += RD_MAX_PROBLEMS) {
+            const int c = std::min(RD_MAX_PROBLEMS, count - i);
+            const qz_status s = mt == 8 ? launch_rd<8>(problems + i, c, st) : launch_rd<16>(problems + i, c, st);
+            if (s != QZ_OK) return s;
+        }
+        return QZ_OK;
+    }
     int nt = ntmax_for(mt);
     if (count == 1) {
         const int N = problems[0].N;

@@ -106,10 +106,11 @@ __device__ __forceinline__ int64_t chunk_offset(int64_t i, bool contig, int64_t 
     return r * ldx + (i - r * cpr) * E;
 }
 
-// Loads per thread kept in flight by the streaming kernels (amax pass, and the
-// warp-uniform encoders: chunks of 8 elements per lane per iteration).
+// Chunks of 8 elements per lane per iteration: U for the amax pass (loads kept
+// in flight), UQ for the warp-uniform encoders (one: those run as many small
+// CTAs instead, which measured faster than deeper unrolling).
 constexpr int U = 4;
-constexpr int UQ = 4;
+constexpr int UQ = 1;
 
 // ------------------------------------------------------ per-tensor amax
 
@@ -578,10 +579,14 @@ void launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStrea
     cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-int stream_grid(int64_t threads_needed) {
+// Grid of a grid-stride kernel: one thread per unit of work, capped at
+// per_sm CTAs per SM (the warp-uniform encoders run best with many small CTAs
+// in flight; the two-pass per-tensor encoder with one wave).
+int stream_grid(int64_t threads_needed, int per_sm = 4) {
     const int64_t ctas = (threads_needed + kThreads - 1) / kThreads;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * 4));   // one wave of resident CTAs
+    return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm));
 }
+constexpr int kEncoderCtasPerSm = 16;
 
 bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
     const size_t es = t == QZ_F32 ? 4 : 2;
@@ -634,7 +639,7 @@ static qz_status fp8_launch_t(const T* x, int64_t rows, int64_t cols, int64_t ld
         break;
     }
     case QZ_FP8_GROUP_1x128:
-        fp8_group_kernel<T><<<stream_grid(rows * cols / 8), kThreads, 0, st>>>(
+        fp8_group_kernel<T><<<stream_grid(rows * cols / 8, kEncoderCtasPerSm), kThreads, 0, st>>>(
             x, rows, cols, ldx, contig, codes, scales, deq);
         break;
     case QZ_FP8_BLOCK_128x128: {
@@ -659,7 +664,7 @@ qz_status quantize_fp8_launch(const void* x, qz_dtype xt, int64_t rows, int64_t 
 qz_status quantize_mxfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
                                 uint8_t* codes, uint8_t* e8m0, float* deq, cudaStream_t st) {
     const bool contig = (ldx == cols);
-    const int grid = stream_grid(rows * cols / 8);
+    const int grid = stream_grid(rows * cols / 8, kEncoderCtasPerSm);
     if (xt == QZ_F32)
         mxfp4_kernel<float><<<grid, kThreads, 0, st>>>((const float*)x, rows, cols, ldx, contig, codes, e8m0, deq);
     else
@@ -673,7 +678,7 @@ qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_
     const bool contig = (ldx == cols);
     float* partial = amax_in ? nullptr : (float*)ws;
     const int np = amax_grid();
-    const int grid = stream_grid(rows * cols / 8);
+    const int grid = stream_grid(rows * cols / 8, kEncoderCtasPerSm);
     const float* cpart = partial;
     if (xt == QZ_F32) {
         if (partial) launch_tensor_amax<float, true>(x, x, 1, rows, cols, ldx, contig, partial, st);

@@ -133,3 +133,20 @@ def test_w4a16_grouped_qwen_shapes(qz):
     qz.qz_gemm_w4a16_grouped(probs)
     for (name, ii, jj, y_ref, bound), (_, _, _, Y) in zip(refs, probs):
         check(host(Y)[ii, jj], y_ref, bound, f"grouped {name}")
+
+
+@pytest.mark.parametrize("tokens", [3, 16])
+def test_w4a16_grouped_decode_tokens(qz, tokens):
+    """Grouped launch at decode batch sizes (the register-direct kernel): one
+    Qwen3-0.6B layer's seven linears with mixed K and N, every output checked."""
+    probs, refs = [], []
+    for layer, name, A, w in syn.qwen3_decode_linears(layers=1, tokens=tokens, seed=1):
+        qw, sc, _ = oracle.quant_int4_g128(w, want_deq=False)
+        K, N = w.shape
+        Y = torch.empty((tokens, N), dtype=torch.bfloat16, device="cuda")
+        probs.append((dev_bf16(A), torch.from_numpy(qw).cuda(),
+                      torch.from_numpy(sc.view(np.int16)).cuda().view(torch.bfloat16), Y))
+        refs.append((name,) + oracle.gemm_w4a16(A, qw, sc))
+    qz.qz_gemm_w4a16_grouped(probs)
+    for (name, y_ref, bound), (_, _, _, Y) in zip(refs, probs):
+        check(host(Y), y_ref, bound, f"grouped {name} tokens={tokens}")
