@@ -24,12 +24,6 @@
 //              to bf16 and stores.
 // The MMA of K block kb+1 runs while block kb is being promoted.
 //
-// When M spans an even number of 128-row tiles, CTAs run in clusters of two
-// that compute vertically adjacent tiles with the same B tile: each CTA loads
-// its own A box and half of the B box, multicasting that half into both CTAs'
-// shared memory (TMA .multicast::cluster), so a CTA pulls 32 KB instead of
-// 48 KB from L2 per K block. Both CTAs' MMAs release a stage (multicast commit)
-// before either refills it.
 #include "qz_tc.cuh"
 
 #include <algorithm>
@@ -52,7 +46,6 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 
-template <int CL>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const float* __restrict__ sA, const float* __restrict__ sB, uint16_t* __restrict__ Y,
@@ -68,20 +61,13 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     auto tempty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Cluster tiles: CL vertically adjacent 128 x 256 tiles sharing one B tile,
-    // M-fastest; CTA `rank` of a cluster computes rows m0 = (group*CL + rank)*128.
-    const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
-    const int cid = CL > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
-    const int ncl = CL > 1 ? (int)cluster_count_x() : (int)gridDim.x;
-    const int mgroups = M / (BM * CL), tiles = mgroups * (N / BN), nkb = K / BK;
-    auto tile_m0 = [&](int ct) { return ((ct % mgroups) * CL + (int)rank) * BM; };
-    auto tile_n0 = [&](int ct) { return (ct / mgroups) * BN; };
-    constexpr uint16_t kPair = 0x3;
+    // Tiles M-fastest: the CTAs working at one time share few B tiles (L2 reuse).
+    const int mt = M / BM, tiles = mt * (N / BN), nkb = K / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), CL);             // released by every CTA's MMAs
+            mbar_init(empty(s), 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull(b), 1);
@@ -97,7 +83,6 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();                  // peers' barriers are initialised
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -106,21 +91,15 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int ct = cid; ct < tiles && ok; ct += ncl) {
-                const int m0 = tile_m0(ct), n0 = tile_n0(ct);
+            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(empty(s), ph ^ 1, &g_fp8_err)) { ok = false; break; }
                     mbar_arrive_expect_tx(full(s), STAGE_BYTES);
                     tma_load_2d(sbase + s * STAGE_BYTES, &tmA, kb * BK, m0, full(s));
-                    if (CL == 1) {
-                        tma_load_2d(sbase + s * STAGE_BYTES + A_BYTES, &tmB, kb * BK, n0, full(s));
-                    } else {                             // this CTA's half of B, into both CTAs
-                        const int half = BN / CL;
-                        tma_load_2d_mc(sbase + s * STAGE_BYTES + A_BYTES + rank * half * BK, &tmB, kb * BK,
-                                       n0 + (int)rank * half, full(s), kPair);
-                    }
+                    tma_load_2d(sbase + s * STAGE_BYTES + A_BYTES, &tmB, kb * BK, n0, full(s));
                 }
             }
             // Before the CTA may exit, every stage it filled has been released
@@ -134,7 +113,7 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (lane == 0) {
             uint32_t it = 0, ac = 0;
             bool ok = true;
-            for (int ct = cid; ct < tiles && ok; ct += ncl) {
+            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
                 for (int kb = 0; kb < nkb; kb++, it++, ac++) {
                     const int b = ac & 1;
                     if (!mbar_wait(tempty(b), ((ac >> 1) & 1) ^ 1, &g_fp8_err)) { ok = false; break; }
@@ -148,8 +127,7 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 #pragma unroll
                     for (int ks = 0; ks < BK / 32; ks++)                 // K = 32 bytes per MMA
                         mma_f8f6f4(d, ad + (uint64_t)(ks * 2), bd + (uint64_t)(ks * 2), IDESC, ks > 0);
-                    if (CL == 1) tc_commit(empty(s));
-                    else tc_commit_mc(empty(s), kPair);
+                    tc_commit(empty(s));
                     tc_commit(tfull(b));
                 }
             }
@@ -164,8 +142,8 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const int r = q * 32 + lane;              // row within the tile
         uint32_t ac = 0;
         bool ok = true;
-        for (int ct = cid; ct < tiles && ok; ct += ncl) {
-            const int m0 = tile_m0(ct), n0 = tile_n0(ct);
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
             const float* sa_row = sA + (size_t)(m0 + r) * nkb;
             const float* sb_row = sB + (size_t)((n0 + h * EPI_COLS) / 128) * nkb;
             float acc[EPI_COLS];
@@ -226,51 +204,10 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();                  // no peer still writes or arrives here
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
-}
-
-template <int CL>
-qz_status launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const float* sA, const float* sB, uint16_t* Y,
-                    int M, int N, int K, cudaStream_t st) {
-    static int attr_set[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(fp8_block_gemm_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return QZ_ERR_CUDA;
-        attr_set[dev] = 1;
-    }
-    const int ctiles = (M / (BM * CL)) * (N / BN);
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = num_sms() / CL;
-    if (CL > 1) {
-        cfg.gridDim = dim3(CL * clusters);
-        int maxc = 0;
-        if (cudaOccupancyMaxActiveClusters(&maxc, fp8_block_gemm_kernel<CL>, &cfg) == cudaSuccess && maxc > 0)
-            clusters = std::min(clusters, maxc);
-        cudaGetLastError();
-    }
-    clusters = std::max(1, std::min(clusters, ctiles));
-    cfg.gridDim = dim3(CL * clusters);
-    if (cudaLaunchKernelEx(&cfg, fp8_block_gemm_kernel<CL>, ta, tb, sA, sB, Y, M, N, K) != cudaSuccess)
-        return QZ_ERR_CUDA;
-    return launch_status();
 }
 
 } // namespace
@@ -286,11 +223,22 @@ qz_status fp8_block_error_read_and_clear() {
 
 qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
                                 uint16_t* Y, int M, int N, int K, void*, size_t, cudaStream_t st) {
-    const int CL = (M / BM) % 2 == 0 ? 2 : 1;   // pairs of vertically adjacent tiles share B
     CUtensorMap ta, tb;
     if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM)) return QZ_ERR_CUDA;
-    if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN / CL)) return QZ_ERR_CUDA;
-    return CL == 2 ? launch_cl<2>(ta, tb, sA, sB, Y, M, N, K, st) : launch_cl<1>(ta, tb, sA, sB, Y, M, N, K, st);
+    if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN)) return QZ_ERR_CUDA;
+    static int attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(fp8_block_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return QZ_ERR_CUDA;
+        attr_set[dev] = 1;
+    }
+    const int tiles = (M / BM) * (N / BN);
+    fp8_block_gemm_kernel<<<std::min(tiles, num_sms()), THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, M, N, K);
+    return launch_status();
 }
 
 } // namespace qz

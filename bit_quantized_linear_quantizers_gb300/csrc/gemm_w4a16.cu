@@ -6,15 +6,15 @@
 // weights exactly once and does the rest on chip.
 //
 // Two kernels share the arithmetic below:
-//  * up to 16 tokens (decode): w4a16_rd_kernel, register-direct. A CTA owns 32
+//  * up to 8 tokens (decode): w4a16_rd_kernel, register-direct. A CTA owns 32
 //    weight columns; its 8 warps split K by 128-deep scale groups. Each lane
 //    loads the packed weights with one coalesced 16-byte load per k-octet row
-//    (4 consecutive columns), two groups ahead of the math, straight into
-//    registers: no shared-memory staging, so many small CTAs share each SM,
-//    their loads overlap, and the next launch's CTAs start as soon as any
-//    of these finish. The warps' partial sums meet in shared memory and are
+//    (4 consecutive columns) straight into registers, after an L2 prefetch
+//    of the CTA's whole weight range has been issued: no shared-memory
+//    staging, so several small CTAs share each SM, their loads overlap, and
+//    the next launch's CTAs start as soon as any of these finish. The warps' partial sums meet in shared memory and are
 //    added in a fixed order.
-//  * 17 to 64 tokens: w4a16_kernel, persistent CTAs (at most one per SM) walking
+//  * 9 to 64 tokens: w4a16_kernel, persistent CTAs (at most one per SM) walking
 //    tiles of NT weight columns x the whole K range, fed by a producer thread
 //    that stages 256-deep K slices through an mbarrier ring with 2-D tensor TMA
 //    (weights as 32-column x 32-row boxes with the 128-byte swizzle,
@@ -50,8 +50,9 @@ __device__ unsigned int g_w4a16_err;
 
 constexpr int KT = 256;                 // K per pipeline stage (two scale groups)
 
-// Widest tile of the TMA-staged kernel (17 to 64 tokens): 64 columns, 8 MMA warps.
-__host__ __device__ constexpr int ntmax_for(int) { return 64; }
+// Widest tile of the TMA-staged kernel (9 to 64 tokens): more tokens need more
+// accumulator registers, so fewer (wider-register) MMA warps.
+__host__ __device__ constexpr int ntmax_for(int mt) { return mt <= 16 ? 128 : 64; }
 constexpr int PER_LAUNCH = 56;          // problems per launch (kernel parameter space: 32 KB)
 constexpr int WBOX = 4096;              // one 32-column x 32-row weight box
 
@@ -202,7 +203,7 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
 #pragma unroll
         for (int mb = 0; mb < MB; mb++) acc[sl][mb][0] = acc[sl][mb][1] = acc[sl][mb][2] = acc[sl][mb][3] = 0.0f;
 
-    RdGroup cur, nxt;
+    RdGroup cur;
     int grp = warp;
     if (grp < ngroups) rd_load(cur, pr, n0, grp, g, t);
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -215,7 +216,6 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
     }
     const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
     for (; grp < ngroups; grp += RD_WARPS) {
-        if (grp + RD_WARPS < ngroups) rd_load(nxt, pr, n0, grp + RD_WARPS, g, t);   // next group in flight
         float ag[2][MB][4], sg[MB][4];
 #pragma unroll
         for (int mb = 0; mb < MB; mb++) {
@@ -263,7 +263,8 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
                 acc[sl][mb][2] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][0], ag[sl][mb][2]), acc[sl][mb][2]);
                 acc[sl][mb][3] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][1], ag[sl][mb][3]), acc[sl][mb][3]);
             }
-        cur = nxt;
+        // the next group's loads (already requested from L2 by the prefetch above)
+        if (grp + RD_WARPS < ngroups) rd_load(cur, pr, n0, grp + RD_WARPS, g, t);
     }
     // partial sums of this warp -> shared memory; fixed-order sum over warps
 #pragma unroll
@@ -499,7 +500,7 @@ w4a16_kernel(const __grid_constant__ Params P, int nt, int ns) {
 
 int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
-// Register-direct launch for up to 16 tokens: one CTA per 32 columns of every
+// Register-direct launch for up to 8 tokens: one CTA per 32 columns of every
 // problem, programmatic dependent launch.
 template <int MT>
 qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
@@ -582,7 +583,7 @@ qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int 
         total += (q.N + nt - 1) / nt;
     }
     P.total_tiles = total;
-    return mt == 32 ? launch_mt<32>(P, nt, st) : launch_mt<64>(P, nt, st);
+    return mt == 16 ? launch_mt<16>(P, nt, st) : mt == 32 ? launch_mt<32>(P, nt, st) : launch_mt<64>(P, nt, st);
 }
 
 } // namespace
@@ -604,10 +605,9 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     // one tile per SM (capped at the widest tile for M); grouped problems use
     // the widest tile.
     const int mt = choose_mt(mmax);
-    if (mt <= 16) {
+    if (mt == 8) {                                // up to 8 tokens: register-direct kernel
         for (int i = 0; i < count; i += RD_MAX_PROBLEMS) {
-            const int c = std::min(RD_MAX_PROBLEMS, count - i);
-            const qz_status s = mt == 8 ? launch_rd<8>(problems + i, c, st) : launch_rd<16>(problems + i, c, st);
+            const qz_status s = launch_rd<8>(problems + i, std::min(RD_MAX_PROBLEMS, count - i), st);
             if (s != QZ_OK) return s;
         }
         return QZ_OK;

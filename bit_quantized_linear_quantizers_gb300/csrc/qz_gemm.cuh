@@ -73,22 +73,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     return false;
 }
 
-// The same bounded wait with cluster-scope acquire, for barriers that CTAs of
-// the cluster arrive on remotely.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
-                 "selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned int* err) {
-    for (uint32_t i = 0; i < kWaitLimit; i++)
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-    atomicExch(err, (unsigned int)QZ_ERR_TIMEOUT);
-    return false;
-}
-
 // 1-D bulk copy global -> shared through the TMA unit, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
