@@ -489,23 +489,47 @@ def kv_rows(qz, syn, stream, pk, timer, ws, bf, q):
 
 def qwen3_step(qz, syn, stream, dev, pk, timer, ws):
     """Config 5: one decode step of a random-init Qwen3-0.6B-shaped decoder at 64
-    tokens, all 196 linears in W4A16 as one grouped launch, plus the FP8 KV write."""
+    tokens, all 196 linears (a) in W4A16 as one grouped launch and (b) in NVFP4 as
+    grouped launches over prepared weight scales, the activations NVFP4-quantized per
+    linear (timed apart: a real decoder fuses that into the op producing them)."""
     import numpy as np
     import torch
-    probs = []
-    wbytes = 0
+    probs, nv_probs, nv_acts = [], [], []
+    wbytes = nvbytes = 0
     for layer, name, A, w in syn.qwen3_decode_linears(layers=28, tokens=64, seed=0):
         K, N = w.shape
         with torch.cuda.stream(stream):
-            qw, sc, _ = qz.qz_quantize_int4_g128(torch.from_numpy(w).to(dev), stream=stream)
+            w_d = torch.from_numpy(w).to(dev)
+            qw, sc, _ = qz.qz_quantize_int4_g128(w_d, stream=stream)
+            bt = w_d.t().contiguous().to(torch.bfloat16)                  # weights as B^T [N, K]
+            cb, sb, gb, _ = qz.qz_quantize_nvfp4(bt, ws=ws, stream=stream)
+            sbp = qz.qz_prepare_fp4_scales(sb, K, nv=True, stream=stream)
         a_d = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).to(dev)
         Y = torch.empty((64, N), dtype=torch.bfloat16, device=dev)
         probs.append((a_d, qw, sc, Y))
         wbytes += K * N // 2 + (K // 128) * N * 2 + 64 * K * 2 + 64 * N * 2
-    stream.synchronize()
+        with torch.cuda.stream(stream):
+            ca, sa, ga, _ = qz.qz_quantize_nvfp4(a_d, ws=ws, stream=stream)
+        Yn = torch.empty((64, N), dtype=torch.bfloat16, device=dev)
+        nv_probs.append((ca, sa, ga, cb, sbp, gb, Yn))
+        nv_acts.append((a_d, ca, sa, ga))
+        nvbytes += N * K // 2 + N * K // 16 + 64 * K // 2 + 64 * K // 16 + 64 * N * 2 + 8
+        stream.synchronize()
+        del w_d, bt, sb
     us = timer(lambda i: qz.qz_gemm_w4a16_grouped(probs, stream=stream), 20)
     out = {"w4a16_grouped_196_linears_us": round(us, 2), "w4a16_gbps": round(wbytes / us / 1e3, 1),
            "w4a16_frac_of_hbm": round(wbytes / us / 1e3 / pk["hbm_gbs"], 3)}
+    nws = qz.Workspace(dev)
+    us = timer(lambda i: qz.qz_gemm_nvfp4_grouped(nv_probs, ws=nws, stream=stream), 20)
+    out.update({"nvfp4_grouped_196_linears_us": round(us, 2), "nvfp4_gbps": round(nvbytes / us / 1e3, 1),
+                "nvfp4_frac_of_hbm": round(nvbytes / us / 1e3 / pk["hbm_gbs"], 3),
+                "nvfp4_bytes": nvbytes})
+
+    def quant_all(i):
+        for a_d, ca, sa, ga in nv_acts:
+            qz.qz_quantize_nvfp4(a_d, codes=ca, scale_e4m3=sa, global_scale=ga, ws=ws, stream=stream)
+    us = timer(quant_all, 3)
+    out["nvfp4_activation_quant_196_us"] = round(us, 2)
     return out
 
 

@@ -20,7 +20,8 @@ __all__ = [
     "FP8_GROUP_1x128", "SCALE_COMPUTE", "SCALE_GIVEN", "qz_workspace_size", "qz_status_string",
     "qz_device_error", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
     "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
-    "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_mxfp4", "Workspace",
+    "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
+    "qz_gemm_nvfp4_grouped", "Workspace",
 ]
 
 F32, BF16 = 0, 1
@@ -28,6 +29,7 @@ FP8_PER_TENSOR, FP8_PER_ROW, FP8_BLOCK_128x128, FP8_GROUP_1x128 = 0, 1, 2, 3
 SCALE_COMPUTE, SCALE_GIVEN = 0, 1
 OP_QUANTIZE_FP8, OP_QUANTIZE_NVFP4, OP_KV_WRITE_FP8 = 0, 1, 2
 OP_GEMM_W4A16, OP_GEMM_FP8_BLOCK, OP_GEMM_NVFP4, OP_GEMM_MXFP4 = 3, 4, 5, 6
+OP_GEMM_NVFP4_GROUPED, OP_PREPARE_FP4_SCALES = 7, 8
 
 if not os.path.exists(LIB):
     raise ImportError(f"libqz.so is not built ({LIB}); run bit_quantized_linear_quantizers_gb300.build() "
@@ -41,6 +43,11 @@ _P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size
 class _W4A16Problem(ctypes.Structure):
     _fields_ = [("A", _P), ("qweight", _P), ("scale_bf16", _P), ("Y", _P),
                 ("M", _I), ("N", _I), ("K", _I)]
+
+
+class _Nvfp4Problem(ctypes.Structure):
+    _fields_ = [("qA", _P), ("sA", _P), ("gA", _P), ("qB", _P), ("sB_prepared", _P), ("gB", _P),
+                ("Y", _P), ("M", _I), ("N", _I), ("K", _I)]
 
 
 _SIGS = {
@@ -58,6 +65,8 @@ _SIGS = {
     "qz_gemm_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "qz_gemm_mxfp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "qz_gemm_nvfp4_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_prepare_fp4_scales": (_I, [_P, _I, _I, _I, _P, _P]),
+    "qz_gemm_nvfp4_grouped": (_I, [ctypes.POINTER(_Nvfp4Problem), _I, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -309,3 +318,32 @@ def qz_gemm_mxfp4(qA, eA, qB, eB, Y=None, ws=None, stream=None):
     _check(lib.qz_gemm_mxfp4(_ptr(qA), _ptr(eA), _ptr(qB), _ptr(eB), _ptr(Y), M, N, K, _ptr(buf), nb,
                              _stream(stream)), "qz_gemm_mxfp4")
     return Y
+
+
+def qz_prepare_fp4_scales(scales, K: int, nv: bool = True, out=None, stream=None):
+    """Block scales [rows, K/16] (NVFP4) or [rows, K/32] (MXFP4), row-major uint8, re-laid
+    into the tensor cores' scale-factor order (rows padded to a multiple of 128)."""
+    rows = scales.shape[0]
+    if out is None:
+        out = torch.empty(qz_workspace_size(OP_PREPARE_FP4_SCALES, rows, K, int(nv)), dtype=torch.uint8,
+                          device=scales.device)
+    _check(lib.qz_prepare_fp4_scales(_ptr(scales), rows, K, int(nv), _ptr(out), _stream(stream)),
+           "qz_prepare_fp4_scales")
+    return out
+
+
+def qz_gemm_nvfp4_grouped(problems, ws=None, stream=None):
+    """Run independent NVFP4 problems [(qA, sA, gA, qB, sB_prepared, gB, Y), ...] (decode
+    shapes, M <= 128) with one scale re-layout launch and one GEMM launch per 80 problems."""
+    arr = (_Nvfp4Problem * len(problems))()
+    kmax = 0
+    dev = None
+    for i, (qA, sA, gA, qB, sBp, gB, Y) in enumerate(problems):
+        M, K = qA.shape[0], qA.shape[1] * 2
+        N = qB.shape[0]
+        arr[i] = _Nvfp4Problem(qA.data_ptr(), sA.data_ptr(), gA.data_ptr(), qB.data_ptr(), sBp.data_ptr(),
+                               gB.data_ptr(), Y.data_ptr(), M, N, K)
+        kmax, dev = max(kmax, K), qA.device
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4_GROUPED, len(problems), kmax), dev)
+    _check(lib.qz_gemm_nvfp4_grouped(arr, len(problems), _ptr(buf), nb, _stream(stream)),
+           "qz_gemm_nvfp4_grouped")

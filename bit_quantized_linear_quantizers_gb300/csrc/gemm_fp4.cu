@@ -26,6 +26,12 @@
 //              per stage into one 256-column fp32 accumulator.
 //  warps 2-9   epilogue: drain the accumulator into registers (then release it
 //              so the next tile's MMAs start), apply gA*gB, round to bf16, store.
+//
+// The CTAs walk a table of problems (one entry for qz_gemm_nvfp4/mxfp4, a
+// decoder step's linears for the grouped call): tile t belongs to the last
+// problem whose first tile is <= t. Rows of A beyond M (a decode batch is one
+// partial 128-row tile) are read as zeros by TMA, their scales re-laid as
+// zeros, and never stored.
 #include "qz_tc.cuh"
 
 #include <algorithm>
@@ -52,26 +58,78 @@ constexpr uint32_t SF_COL = 256;                  // scale-factor ring after the
 constexpr uint32_t SF_COLS_PER_STAGE = 48;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 
-// Row-major scales sf[R][KS] -> atoms[R/128][KS/4][512]: byte (m%32)*16 +
-// (m/32)*4 + k of atom (rb, kg) holds sf[rb*128 + m][kg*4 + k].
-__global__ void sf_relayout_kernel(const uint8_t* __restrict__ sf, int R, int KS, uint8_t* __restrict__ out) {
-    const int64_t words = (int64_t)(R / 128) * (KS / 4) * 128;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t a = i >> 7;
-        const int p = (int)(i & 127);
-        const int64_t rb = a / (KS / 4), kg = a % (KS / 4);
-        const int64_t m = rb * 128 + (p >> 2) + 32 * (p & 3);
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(sf + m * KS + kg * 4));
-        reinterpret_cast<uint32_t*>(out)[i] = w;
+// Row-major scales sf[R][KS] -> atoms[ceil(R/128)][KS/4][512]: byte
+// (m%32)*16 + (m/32)*4 + k of atom (rb, kg) holds sf[rb*128 + m][kg*4 + k]
+// (0 for rows >= R). One launch re-lays every job of the table.
+constexpr int RELAY_MAX = 256;
+
+struct RelayJob {
+    const uint8_t* src;
+    uint8_t* dst;
+    long long word_begin;             // first 32-bit word of this job in the launch
+    int R, KS;
+};
+
+struct RelayParams {
+    RelayJob j[RELAY_MAX];
+    int count;
+    long long total_words;
+};
+
+__global__ void sf_relayout_kernel(const __grid_constant__ RelayParams P) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < P.total_words;
+         i += (long long)gridDim.x * blockDim.x) {
+        int lo = 0, hi = P.count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.j[mid].word_begin <= i) lo = mid; else hi = mid - 1;
+        }
+        const RelayJob& jb = P.j[lo];
+        const long long w = i - jb.word_begin;
+        const long long a = w >> 7;
+        const int p = (int)(w & 127);
+        const long long rb = a / (jb.KS / 4), kg = a % (jb.KS / 4);
+        const long long m = rb * 128 + (p >> 2) + 32 * (p & 3);
+        const uint32_t v = m < jb.R ? __ldg(reinterpret_cast<const uint32_t*>(jb.src + m * jb.KS + kg * 4)) : 0u;
+        reinterpret_cast<uint32_t*>(jb.dst)[w] = v;
     }
 }
 
+long long relay_words(int R, int KS) { return (long long)((R + 127) / 128) * (KS / 4) * 128; }
+
+qz_status relayout(const RelayParams& P, cudaStream_t st) {
+    if (P.total_words == 0) return QZ_OK;
+    const long long blocks = (P.total_words + 255) / 256;
+    const int grid = (int)std::min<long long>(blocks, (long long)num_sms() * 8);
+    sf_relayout_kernel<<<grid, 256, 0, st>>>(P);
+    return launch_status();
+}
+
+// One GEMM problem of a launch (kernel parameter space: 80 of them fit).
+struct Fp4Prob {
+    CUtensorMap tmA;                  // A codes [M, K/2] u8, box 128 B x 128 rows
+    CUtensorMap tmB;                  // B^T codes [N, K/2] u8, box 128 B x 256 rows
+    const uint8_t* sfA;               // A scales, tensor-core atoms, rows padded to 128
+    const uint8_t* sfB;               // B scales, tensor-core atoms
+    const float* gA;                  // NVFP4 tensor scales (unused for MXFP4)
+    const float* gB;
+    uint16_t* Y;
+    int M, N, K;
+    int mt;                           // 128-row tiles of M
+    int tile_begin;                   // first tile of this problem in the launch
+};
+
+constexpr int FP4_PER_LAUNCH = 80;
+
+struct Fp4Params {
+    Fp4Prob p[FP4_PER_LAUNCH];
+    int count;
+    int total_tiles;
+};
+
 template <bool NV>
 __global__ void __launch_bounds__(THREADS, 1)
-fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const uint8_t* __restrict__ sfA, const uint8_t* __restrict__ sfB,
-                const float* __restrict__ gA, const float* __restrict__ gB, uint16_t* __restrict__ Y,
-                int M, int N, int K) {
+fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
     constexpr int G = NV ? 4 : 2;                 // scale atoms per row block per stage
     constexpr uint32_t SFA_COLS = 4 * G;          // TMEM columns of A's scales per stage
     extern __shared__ uint8_t smem_raw[];
@@ -84,9 +142,15 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t tfull = smem_u32(bars + 2 * STAGES), tempty = smem_u32(bars + 2 * STAGES + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = M / BM, tiles = mt * (N / BN), nks = K / (2 * BKB);
-    const int ksa = K / (NV ? 16 : 32);           // scales per row
-    const int atoms_per_rb = ksa / 4;
+    const int tiles = P.total_tiles;
+    auto find = [&](int tile) {                   // last problem with tile_begin <= tile
+        int lo = 0, hi = P.count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.p[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
@@ -96,8 +160,6 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         mbar_init(tfull, 1);
         mbar_init(tempty, EPI_WARPS);
         fence_barrier_init();
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -115,17 +177,23 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
-                const uint8_t* sa = sfA + ((size_t)(m0 / 128) * atoms_per_rb) * ATOM;
-                const uint8_t* sb0 = sfB + ((size_t)(n0 / 128) * atoms_per_rb) * ATOM;
+                const Fp4Prob& pr = P.p[find(tile)];
+                const int local = tile - pr.tile_begin;
+                const int m0 = (local % pr.mt) * BM, n0 = (local / pr.mt) * BN;
+                const int nks = pr.K / (2 * BKB);
+                const int atoms_per_rb = pr.K / (NV ? 16 : 32) / 4;
+                const uint8_t* sa = pr.sfA + ((size_t)(m0 / 128) * atoms_per_rb) * ATOM;
+                const uint8_t* sb0 = pr.sfB + ((size_t)(n0 / 128) * atoms_per_rb) * ATOM;
                 const uint8_t* sb1 = sb0 + (size_t)atoms_per_rb * ATOM;
+                prefetch_tmap(&pr.tmA);
+                prefetch_tmap(&pr.tmB);
                 for (int c = 0; c < nks; c++, it++) {
                     const int s = it % STAGES;
                     if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, &g_fp4_err)) { ok = false; break; }
                     const uint32_t st = sbase + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(full(s), A_BYTES + B_BYTES + sf_bytes);
-                    tma_load_2d(st, &tmA, c * BKB, m0, full(s));
-                    tma_load_2d(st + A_BYTES, &tmB, c * BKB, n0, full(s));
+                    tma_load_2d(st, &pr.tmA, c * BKB, m0, full(s));     // rows >= M read as zeros
+                    tma_load_2d(st + A_BYTES, &pr.tmB, c * BKB, n0, full(s));
                     const size_t off = (size_t)c * G * ATOM;
                     bulk_g2s(st + A_BYTES + B_BYTES, sa + off, G * ATOM, full(s));
                     bulk_g2s(st + A_BYTES + B_BYTES + G * ATOM, sb0 + off, G * ATOM, full(s));
@@ -141,6 +209,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, tcount++) {
+                const int nks = P.p[find(tile)].K / (2 * BKB);
                 if (!mbar_wait(tempty, (tcount & 1) ^ 1, &g_fp4_err)) { ok = false; break; }
                 tc_fence_after();
                 for (int c = 0; c < nks; c++, it++) {
@@ -182,10 +251,12 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3, h = (warp - 2) >> 2, r = q * 32 + lane;
-        const float gscale = NV ? __ldg(gA) * __ldg(gB) : 1.0f;
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, tcount++) {
-            const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
+            const Fp4Prob& pr = P.p[find(tile)];
+            const int local = tile - pr.tile_begin;
+            const int m0 = (local % pr.mt) * BM, n0 = (local / pr.mt) * BN;
+            const float gscale = NV ? __ldg(pr.gA) * __ldg(pr.gB) : 1.0f;
             if (!mbar_wait(tfull, tcount & 1, &g_fp4_err)) break;
             tc_fence_after();
             float acc[128];
@@ -201,7 +272,8 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
-            uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * 128);
+            if (m0 + r >= pr.M) continue;                       // padding rows of a partial tile
+            uint4* yrow = reinterpret_cast<uint4*>(pr.Y + (size_t)(m0 + r) * pr.N + n0 + h * 128);
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 uint4 o;
@@ -224,13 +296,55 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 }
 
 size_t sf_bytes(bool nv, int R, int K) { return (size_t)R * (K / (nv ? 16 : 32)); }
+size_t round1k(size_t b) { return (b + 1023) & ~size_t(1023); }
+
+// Fills problem slot `p` (tensor maps and tile bookkeeping); false if a
+// tensor map cannot be encoded.
+bool fill_problem(Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA, const float* gA, const uint8_t* qB,
+                  const uint8_t* sfB, const float* gB, uint16_t* Y, int M, int N, int K, int& tiles) {
+    if (!encode_tmap_2d_u8(&p.tmA, qA, (uint64_t)K / 2, (uint64_t)M, (uint64_t)K / 2, BKB, BM) ||
+        !encode_tmap_2d_u8(&p.tmB, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN))
+        return false;
+    p.sfA = sfA; p.sfB = sfB; p.gA = gA; p.gB = gB; p.Y = Y;
+    p.M = M; p.N = N; p.K = K;
+    p.mt = (M + BM - 1) / BM;
+    p.tile_begin = tiles;
+    tiles += p.mt * (N / BN);
+    return true;
+}
+
+qz_status launch_table(bool nv, const Fp4Params& P, cudaStream_t st) {
+    static int attr_set[64][2];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    const void* fn = nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
+    if (!attr_set[dev][nv]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+            return QZ_ERR_CUDA;
+        attr_set[dev][nv] = 1;
+    }
+    const int grid = std::min(P.total_tiles, num_sms());
+    if (nv)
+        fp4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
+    else
+        fp4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(P);
+    return launch_status();
+}
 
 } // namespace
 
 size_t ws_gemm_fp4(int M, int N, int K) {
     // re-laid scales of A and B (NVFP4 size; MXFP4 uses half)
-    return ((sf_bytes(true, M, K) + 1023) & ~size_t(1023)) + ((sf_bytes(true, N, K) + 1023) & ~size_t(1023));
+    return round1k(sf_bytes(true, M, K)) + round1k(sf_bytes(true, N, K));
 }
+
+size_t ws_gemm_nvfp4_grouped(int count, int kmax) {
+    // re-laid scales of each problem's A (at most 128 rows)
+    return (size_t)count * round1k(sf_bytes(true, 128, kmax));
+}
+
+size_t prepared_fp4_scale_bytes(int rows, int K, bool nv) { return sf_bytes(nv, (rows + 127) / 128 * 128, K); }
 
 qz_status fp4_error_read_and_clear() {
     unsigned int v = 0, z = 0;
@@ -243,35 +357,61 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
                           const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
                           int M, int N, int K, void* ws, size_t, cudaStream_t st) {
     uint8_t* wsA = static_cast<uint8_t*>(ws);
-    uint8_t* wsB = wsA + ((sf_bytes(true, M, K) + 1023) & ~size_t(1023));
+    uint8_t* wsB = wsA + round1k(sf_bytes(true, M, K));
     const int ks = K / (nv ? 16 : 32);
-    {
-        const int64_t wa = (int64_t)M * ks / 4, wb = (int64_t)N * ks / 4;
-        const int ga = (int)std::min<int64_t>((wa + 255) / 256, (int64_t)num_sms() * 8);
-        const int gb = (int)std::min<int64_t>((wb + 255) / 256, (int64_t)num_sms() * 8);
-        sf_relayout_kernel<<<ga, 256, 0, st>>>(sA, M, ks, wsA);
-        sf_relayout_kernel<<<gb, 256, 0, st>>>(sB, N, ks, wsB);
+    RelayParams R;
+    R.count = 2;
+    R.j[0] = RelayJob{sA, wsA, 0, M, ks};
+    R.j[1] = RelayJob{sB, wsB, relay_words(M, ks), N, ks};
+    R.total_words = relay_words(M, ks) + relay_words(N, ks);
+    QZ_TRY(relayout(R, st));
+    Fp4Params P;
+    int tiles = 0;
+    if (!fill_problem(P.p[0], qA, wsA, gA, qB, wsB, gB, Y, M, N, K, tiles)) return QZ_ERR_CUDA;
+    P.count = 1;
+    P.total_tiles = tiles;
+    return launch_table(nv, P, st);
+}
+
+qz_status gemm_nvfp4_grouped_launch(const qz_nvfp4_problem* problems, int count, void* ws, size_t,
+                                    cudaStream_t st) {
+    // every problem's A scales re-laid in one launch (B's come prepared)
+    int kmax = 0;
+    for (int i = 0; i < count; i++) kmax = std::max(kmax, problems[i].K);
+    const size_t slot = round1k(sf_bytes(true, 128, kmax));
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    RelayParams R;
+    R.count = count;
+    R.total_words = 0;
+    for (int i = 0; i < count; i++) {
+        const qz_nvfp4_problem& q = problems[i];
+        R.j[i] = RelayJob{q.sA, wsb + (size_t)i * slot, R.total_words, q.M, q.K / 16};
+        R.total_words += relay_words(q.M, q.K / 16);
     }
-    CUtensorMap ta, tb;
-    if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K / 2, (uint64_t)M, (uint64_t)K / 2, BKB, BM)) return QZ_ERR_CUDA;
-    if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN)) return QZ_ERR_CUDA;
-    static int attr_set[64][2];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    const void* fn = nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
-    if (!attr_set[dev][nv]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-            return QZ_ERR_CUDA;
-        attr_set[dev][nv] = 1;
+    QZ_TRY(relayout(R, st));
+    for (int i0 = 0; i0 < count; i0 += FP4_PER_LAUNCH) {
+        Fp4Params P;
+        int tiles = 0;
+        P.count = std::min(FP4_PER_LAUNCH, count - i0);
+        for (int i = 0; i < P.count; i++) {
+            const qz_nvfp4_problem& q = problems[i0 + i];
+            if (!fill_problem(P.p[i], q.qA, wsb + (size_t)(i0 + i) * slot, q.gA, q.qB, q.sB_prepared, q.gB, q.Y,
+                              q.M, q.N, q.K, tiles))
+                return QZ_ERR_CUDA;
+        }
+        P.total_tiles = tiles;
+        QZ_TRY(launch_table(true, P, st));
     }
-    const int tiles = (M / BM) * (N / BN);
-    const int grid = std::min(tiles, num_sms());
-    if (nv)
-        fp4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, wsA, wsB, gA, gB, Y, M, N, K);
-    else
-        fp4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, wsA, wsB, gA, gB, Y, M, N, K);
-    return launch_status();
+    return QZ_OK;
+}
+
+qz_status prepare_fp4_scales_launch(const uint8_t* scales, int rows, int K, bool nv, uint8_t* out,
+                                    cudaStream_t st) {
+    RelayParams R;
+    R.count = 1;
+    R.j[0] = RelayJob{scales, out, 0, rows, K / (nv ? 16 : 32)};
+    R.total_words = relay_words(rows, K / (nv ? 16 : 32));
+    return relayout(R, st);
 }
 
 } // namespace qz

@@ -67,12 +67,6 @@ bool is_aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 using namespace qz;
 
-#define QZ_TRY(expr)                                   \
-    do {                                               \
-        const qz_status _s = (expr);                   \
-        if (_s != QZ_OK) return _s;                    \
-    } while (0)
-
 static size_t elem_size(qz_dtype t) { return t == QZ_F32 ? 4 : 2; }
 static bool dtype_ok(qz_dtype t) { return t == QZ_F32 || t == QZ_BF16; }
 
@@ -101,6 +95,12 @@ size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2) {
     case QZ_OP_GEMM_FP8_BLOCK: return ws_gemm_fp8_block((int)d0, (int)d1, (int)d2);
     case QZ_OP_GEMM_NVFP4: return ws_gemm_fp4((int)d0, (int)d1, (int)d2);
     case QZ_OP_GEMM_MXFP4: return ws_gemm_fp4((int)d0, (int)d1, (int)d2);
+    case QZ_OP_GEMM_NVFP4_GROUPED:
+        return d0 >= 1 && d0 <= kNvfp4MaxProblems && d1 >= 1 && d1 <= (1 << 24) ? ws_gemm_nvfp4_grouped((int)d0, (int)d1)
+                                                                                 : 0;
+    case QZ_OP_PREPARE_FP4_SCALES:
+        return d0 >= 1 && d0 <= (1 << 24) && d1 >= 1 && d1 <= (1 << 24) ? prepared_fp4_scale_bytes((int)d0, (int)d1, d2 != 0)
+                                                                         : 0;
     }
     return 0;
 }
@@ -271,6 +271,35 @@ qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB,
     QZ_TRY(device_check());
     return gemm_fp4_launch(false, qA, eA, nullptr, qB, eB, nullptr, Y, M, N, K, ws, ws_bytes,
                            (cudaStream_t)stream);
+}
+
+qz_status qz_prepare_fp4_scales(const uint8_t* scales, int rows, int K, int nv, uint8_t* out, void* stream) {
+    if (!scales || !out || (nv != 0 && nv != 1)) return QZ_ERR_INVALID_ARG;
+    if (rows < 1 || K < 1) return QZ_ERR_INVALID_ARG;
+    if (K % kFp4BlockK) return QZ_ERR_SHAPE;
+    if (!is_aligned(scales, 4) || !is_aligned(out, 16)) return QZ_ERR_ALIGNMENT;
+    QZ_TRY(device_check());
+    return prepare_fp4_scales_launch(scales, rows, K, nv == 1, out, (cudaStream_t)stream);
+}
+
+qz_status qz_gemm_nvfp4_grouped(const qz_nvfp4_problem* problems, int count, void* ws, size_t ws_bytes,
+                                void* stream) {
+    if (!problems || count < 1 || count > kNvfp4MaxProblems) return QZ_ERR_INVALID_ARG;
+    int kmax = 0;
+    for (int i = 0; i < count; i++) {
+        const qz_nvfp4_problem& p = problems[i];
+        if (!p.qA || !p.sA || !p.gA || !p.qB || !p.sB_prepared || !p.gB || !p.Y) return QZ_ERR_INVALID_ARG;
+        if (p.M < 1 || p.N < 1 || p.K < 1) return QZ_ERR_INVALID_ARG;
+        if (p.M > kFp4BlockM || p.N % kFp4BlockN || p.K % kFp4BlockK) return QZ_ERR_SHAPE;
+        if (!is_aligned(p.qA, 16) || !is_aligned(p.qB, 16) || !is_aligned(p.sB_prepared, 16) ||
+            !is_aligned(p.Y, 16) || !is_aligned(p.sA, 4))
+            return QZ_ERR_ALIGNMENT;
+        kmax = std::max(kmax, p.K);
+    }
+    const size_t need = ws_gemm_nvfp4_grouped(count, kmax);
+    if (!ws || ws_bytes < need || !is_aligned(ws, 16)) return QZ_ERR_WORKSPACE;
+    QZ_TRY(device_check());
+    return gemm_nvfp4_grouped_launch(problems, count, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 // Same computation as qz_gemm_nvfp4; the scratch is the library's fixed array

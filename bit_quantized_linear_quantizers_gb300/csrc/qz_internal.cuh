@@ -17,6 +17,13 @@
 namespace qz {
 
 // The clamp floor of the fake-quant functions: the fp32 value nearest 1e-12.
+// Return the status of `expr` from the calling function unless it is QZ_OK.
+#define QZ_TRY(expr)                                   \
+    do {                                               \
+        const qz_status _s = (expr);                   \
+        if (_s != QZ_OK) return _s;                    \
+    } while (0)
+
 constexpr float kAmaxMin = 1e-12f;
 constexpr float kFp8Max = 448.0f;
 constexpr float kFp4Max = 6.0f;
@@ -72,26 +79,7 @@ struct Recip {
     }
 };
 
-__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
-    unsigned long long d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
-    return d;
-}
-__device__ __forceinline__ void f2_unpack(unsigned long long d, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
-}
-
-// Two quotients at once with packed fp32x2 arithmetic.
-__device__ __forceinline__ void div2(float& a, float& b, const Recip& d) {
-    const unsigned long long x = f2_pack(a, b), r = f2_pack(d.r, d.r), ns = f2_pack(-d.s, -d.s);
-    unsigned long long q0, rem, q1;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(r));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rem) : "l"(q0), "l"(ns), "l"(x));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(rem), "l"(r), "l"(q0));
-    f2_unpack(q1, a, b);
-}
-
-// One correctly rounded quotient x / d.s (same method as div2), x >= 0.
+// One correctly rounded quotient x / d.s (Markstein's correction step), x >= 0.
 __device__ __forceinline__ float div1(float x, const Recip& d) {
     const float q0 = __fmul_rn(x, d.r);
     const float rem = __fmaf_rn(-q0, d.s, x);
@@ -133,8 +121,6 @@ __device__ __forceinline__ uint32_t e2m1x8_fix(uint32_t w, const float y[8]) {
     return w;
 }
 
-// Exact E2M1 codes of y[8] (pages' rule).
-__device__ __forceinline__ uint32_t e2m1x8(const float y[8]) { return e2m1x8_fix(e2m1x8_rne(y), y); }
 
 // Same result for quotients whose exact midpoints are rare (a division by an
 // arbitrary scale): midpoints carry at most two mantissa bits, so the exact fix

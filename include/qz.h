@@ -68,7 +68,10 @@ typedef enum qz_op {
     QZ_OP_GEMM_W4A16 = 3,     /* d0 = M, d1 = N, d2 = K                    */
     QZ_OP_GEMM_FP8_BLOCK = 4, /* d0 = M, d1 = N, d2 = K                    */
     QZ_OP_GEMM_NVFP4 = 5,     /* d0 = M, d1 = N, d2 = K                    */
-    QZ_OP_GEMM_MXFP4 = 6      /* d0 = M, d1 = N, d2 = K                    */
+    QZ_OP_GEMM_MXFP4 = 6,     /* d0 = M, d1 = N, d2 = K                    */
+    QZ_OP_GEMM_NVFP4_GROUPED = 7, /* d0 = problem count, d1 = largest K    */
+    QZ_OP_PREPARE_FP4_SCALES = 8  /* d0 = rows, d1 = K, d2 = 1 NVFP4 / 0 MXFP4:
+                                     bytes of the prepared output (not scratch) */
 } qz_op;
 
 /* Bytes of workspace the call `op` needs for the given sizes (0 if none).
@@ -225,6 +228,45 @@ qz_status qz_gemm_nvfp4(const uint8_t* qA, const uint8_t* sA, const float* gA,
  * qz_quantize_mxfp4 on A [M, K] and B^T [N, K]. Shapes and alignment as NVFP4. */
 qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
                         uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+/* Re-lays a row-major block-scale matrix, as the FP4 quantizers write it
+ * (NVFP4: E4M3 [rows, K/16], nv = 1; MXFP4: E8M0 [rows, K/32], nv = 0), into the
+ * order the FP4 tensor cores read scale factors in: per 128 rows and 4
+ * consecutive scales, a 512-byte block where byte (m%32)*16 + (m/32)*4 + k holds
+ * the scale k of row m (rows beyond `rows` up to a multiple of 128 are 0).
+ * Weights are static, so their scales are re-laid once and handed to
+ * qz_gemm_nvfp4_grouped; the single-problem GEMMs do this per call in their
+ * workspace. This is a layout step of this library; the pages define no
+ * layout for the scales beyond the row-major block order.
+ * out: qz_workspace_size(QZ_OP_PREPARE_FP4_SCALES, rows, K, nv) bytes, 16 B
+ * aligned, caller-owned. Shapes: rows >= 1, K % 256 == 0. */
+qz_status qz_prepare_fp4_scales(const uint8_t* scales, int rows, int K, int nv, uint8_t* out, void* stream);
+
+/* One problem of qz_gemm_nvfp4_grouped: Y = A B with A NVFP4 codes [M, K/2],
+ * row-major E4M3 scales [M, K/16] and tensor scale gA (as qz_quantize_nvfp4
+ * writes them), B^T NVFP4 codes [N, K/2] with its scales already re-laid by
+ * qz_prepare_fp4_scales(nv = 1) and tensor scale gB, Y bf16 [M, N]. */
+typedef struct qz_nvfp4_problem {
+    const uint8_t* qA;
+    const uint8_t* sA;
+    const float* gA;
+    const uint8_t* qB;
+    const uint8_t* sB_prepared;
+    const float* gB;
+    uint16_t* Y;
+    int M, N, K;
+} qz_nvfp4_problem;
+
+/* Runs `count` independent NVFP4 GEMMs of decode shape (the linears of a
+ * decoder step, "量化部署实战", 精度比较: every linear of the block quantized)
+ * with one scale re-layout launch for all A operands and one GEMM launch per
+ * 80 problems, the problems' 128 x 256 output tiles shared out over the SMs.
+ * Same arithmetic as qz_gemm_nvfp4. Shapes per problem: 1 <= M <= 128,
+ * N % 256 == 0, K % 256 == 0. count <= 256. Alignment: codes, prepared scales
+ * and Y 16 B, sA 4 B. ws: qz_workspace_size(QZ_OP_GEMM_NVFP4_GROUPED, count,
+ * largest K, 0) bytes. */
+qz_status qz_gemm_nvfp4_grouped(const qz_nvfp4_problem* problems, int count, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /* NVFP4 GEMM that allocates nothing and takes no workspace. (The surveyed
  * pages have no counterpart: this is an interface convenience of this library.)

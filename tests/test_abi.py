@@ -120,3 +120,38 @@ def test_gemm_validation(qz):
     assert L.qz_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 200, 256, NULL, 0, NULL) == 2
     assert L.qz_gemm_mxfp4(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 100, NULL, 0, NULL) == 2
     assert L.qz_gemm_mxfp4(ODD, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 3
+
+
+def test_grouped_nvfp4_and_prepare_validation(qz):
+    L = qz.lib
+    P = qz._Nvfp4Problem
+
+    def one(**kw):
+        f = dict(qA=0x10000, sA=0x10000, gA=0x10000, qB=0x10000, sB_prepared=0x10000, gB=0x10000,
+                 Y=0x10000, M=64, N=1024, K=1024)
+        f.update(kw)
+        arr = (P * 1)()
+        arr[0] = P(**f)
+        return arr
+
+    ws_need = qz.qz_workspace_size(qz.OP_GEMM_NVFP4_GROUPED, 1, 1024)
+    assert ws_need == 128 * 1024 // 16
+    assert L.qz_gemm_nvfp4_grouped(None, 1, FAKE, ws_need, NULL) == 1
+    assert L.qz_gemm_nvfp4_grouped(one(), 0, FAKE, ws_need, NULL) == 1                  # count < 1
+    assert L.qz_gemm_nvfp4_grouped(one(), 257, FAKE, ws_need, NULL) == 1                # count > 256
+    assert L.qz_gemm_nvfp4_grouped(one(M=129), 1, FAKE, ws_need, NULL) == 2             # decode: M <= 128
+    assert L.qz_gemm_nvfp4_grouped(one(N=1000), 1, FAKE, ws_need, NULL) == 2            # N % 256
+    assert L.qz_gemm_nvfp4_grouped(one(K=1000), 1, FAKE, ws_need, NULL) == 2            # K % 256
+    assert L.qz_gemm_nvfp4_grouped(one(gB=0), 1, FAKE, ws_need, NULL) == 1
+    assert L.qz_gemm_nvfp4_grouped(one(qB=0x10008), 1, FAKE, ws_need, NULL) == 3        # 16-byte alignment
+    assert L.qz_gemm_nvfp4_grouped(one(sA=0x10002), 1, FAKE, ws_need, NULL) == 3        # 4-byte alignment
+    assert L.qz_gemm_nvfp4_grouped(one(), 1, FAKE, ws_need - 1, NULL) == 7              # workspace too small
+    assert L.qz_gemm_nvfp4_grouped(one(), 1, NULL, ws_need, NULL) == 7
+    # scales, rows, K, nv, out, stream
+    assert qz.qz_workspace_size(qz.OP_PREPARE_FP4_SCALES, 200, 1024, 1) == 256 * 64
+    assert qz.qz_workspace_size(qz.OP_PREPARE_FP4_SCALES, 200, 1024, 0) == 256 * 32
+    assert L.qz_prepare_fp4_scales(NULL, 128, 256, 1, FAKE, NULL) == 1
+    assert L.qz_prepare_fp4_scales(FAKE, 128, 256, 2, FAKE, NULL) == 1                 # nv must be 0 or 1
+    assert L.qz_prepare_fp4_scales(FAKE, 0, 256, 1, FAKE, NULL) == 1
+    assert L.qz_prepare_fp4_scales(FAKE, 128, 100, 1, FAKE, NULL) == 2                 # K % 256
+    assert L.qz_prepare_fp4_scales(FAKE, 128, 256, 1, ODD, NULL) == 3

@@ -128,3 +128,97 @@ def test_fp4_gemm_full_size_sampled(qz, fmt):
     ref = oracle.gemm_nvfp4 if fmt == "nv" else oracle.gemm_mxfp4
     y_ref, bound = ref(*ops, ii, jj)
     check(y[ii, jj], y_ref, bound, f"{fmt} full size")
+
+
+# ------------------------------------------------- prepared scales, grouped decode
+
+def relayout_reference(sf, K, nv):
+    """The tensor cores' scale-factor order written out with numpy: per 128 rows and 4
+    scales, byte (m%32)*16 + (m/32)*4 + k holds sf[m][4*kg + k]; padding rows are 0."""
+    R, KS = sf.shape
+    assert KS == K // (16 if nv else 32)
+    rp = -(-R // 128) * 128
+    pad = np.zeros((rp, KS), np.uint8)
+    pad[:R] = sf
+    out = np.zeros((rp // 128, KS // 4, 512), np.uint8)
+    m = np.arange(128)
+    for rb in range(rp // 128):
+        for kg in range(KS // 4):
+            for k in range(4):
+                out[rb, kg, (m % 32) * 16 + (m // 32) * 4 + k] = pad[rb * 128 + m, 4 * kg + k]
+    return out.ravel()
+
+
+@pytest.mark.parametrize("nv", [True, False])
+@pytest.mark.parametrize("rows", [1, 200, 256])
+def test_prepare_fp4_scales_layout(qz, nv, rows):
+    K = 512
+    rng = np.random.default_rng(rows + nv)
+    sf = rng.integers(0, 256, (rows, K // (16 if nv else 32)), dtype=np.uint8)
+    got = host(qz.qz_prepare_fp4_scales(dev(sf), K, nv=nv))
+    assert np.array_equal(got, relayout_reference(sf, K, nv))
+
+
+def grouped_case(qz, shapes, seed):
+    """Quantize each (M, N, K) with the oracle, re-lay B's scales on the GPU, run one
+    grouped call; returns the problems (with sentinel-filled Y) and the oracle operands."""
+    probs, ops = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        a, bt = inputs(M, N, K, seed + i)
+        ca, sa, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+        cb, sb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+        Y = torch.full((M + 1, N), -7.0, dtype=torch.bfloat16, device="cuda")   # row M: sentinel
+        probs.append((dev(ca), dev(sa), dev(np.float32([ga])), dev(cb),
+                      qz.qz_prepare_fp4_scales(dev(sb), K, nv=True), dev(np.float32([gb])), Y[:M]))
+        ops.append((ca, sa, ga, cb, sb, gb, Y))
+    qz.qz_gemm_nvfp4_grouped(probs)
+    torch.cuda.synchronize()
+    return ops
+
+
+def test_nvfp4_grouped_mixed_decode_shapes(qz):
+    """Partial 128-row tiles (M = 1, 37, 128) and different N and K in one launch; every
+    output checked, and the row after each Y untouched."""
+    shapes = [(1, 256, 256), (37, 512, 1024), (128, 256, 512), (64, 768, 256)]
+    for (M, N, K), (ca, sa, ga, cb, sb, gb, Y) in zip(shapes, grouped_case(qz, shapes, 11)):
+        y_ref, bound = oracle.gemm_nvfp4(ca, sa, ga, cb, sb, gb)
+        yh = host(Y)
+        check(yh[:M], y_ref, bound, f"grouped M={M} N={N} K={K}")
+        assert np.all(bf16_bits_to_f64(yh[M]) == -7.0), "a padding row was stored"
+
+
+def test_nvfp4_grouped_matches_single_call(qz):
+    """At M = 128 the grouped call and qz_gemm_nvfp4 run the same tiles: equal outputs."""
+    shapes = [(128, 512, 512)]
+    (ca, sa, ga, cb, sb, gb, Y), = grouped_case(qz, shapes, 21)
+    y_single = host(qz.qz_gemm_nvfp4(dev(ca), dev(sa), dev(np.float32([ga])), dev(cb), dev(sb),
+                                     dev(np.float32([gb]))))
+    assert np.array_equal(host(Y)[:128], y_single)
+
+
+def test_nvfp4_grouped_more_than_one_launch(qz):
+    """85 problems: two GEMM launches (80 problems fit one launch's parameters)."""
+    shapes = [(8 + (i % 3), 256, 256) for i in range(85)]
+    ops = grouped_case(qz, shapes, 31)
+    for i in (0, 41, 79, 80, 84):
+        (ca, sa, ga, cb, sb, gb, Y), (M, N, K) = ops[i], shapes[i]
+        y_ref, bound = oracle.gemm_nvfp4(ca, sa, ga, cb, sb, gb)
+        check(host(Y)[:M], y_ref, bound, f"problem {i}")
+
+
+def test_nvfp4_grouped_qwen_layer(qz):
+    """One Qwen3-0.6B layer's seven linears at 64 tokens (the decode-step configuration),
+    weights as B^T, all outputs checked."""
+    probs, refs = [], []
+    for layer, name, A, w in syn.qwen3_decode_linears(layers=1, tokens=64, seed=2):
+        K, N = w.shape
+        bt = syn.to_bf16_bits(np.ascontiguousarray(w.T))
+        ca, sa, ga, _ = oracle.quant_nvfp4(A, want_deq=False)
+        cb, sb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+        Y = torch.empty((64, N), dtype=torch.bfloat16, device="cuda")
+        probs.append((dev(ca), dev(sa), dev(np.float32([ga])), dev(cb),
+                      qz.qz_prepare_fp4_scales(dev(sb), K, nv=True), dev(np.float32([gb])), Y))
+        refs.append((name,) + oracle.gemm_nvfp4(ca, sa, ga, cb, sb, gb))
+    qz.qz_gemm_nvfp4_grouped(probs)
+    for (name, y_ref, bound), p in zip(refs, probs):
+        check(host(p[6]), y_ref, bound, f"qwen {name}")
