@@ -14,7 +14,7 @@
 //    staging, so several small CTAs share each SM, their loads overlap, and
 //    the next launch's CTAs start as soon as any of these finish. The warps' partial sums meet in shared memory and are
 //    added in a fixed order.
-//  * 9 to 64 tokens: w4a16_kernel, persistent CTAs (at most one per SM) walking
+//  * 9 to 16 tokens: w4a16_kernel, persistent CTAs (at most one per SM) walking
 //    tiles of NT weight columns x the whole K range, fed by a producer thread
 //    that stages 256-deep K slices through an mbarrier ring with 2-D tensor TMA
 //    (weights as 32-column x 32-row boxes with the 128-byte swizzle,
@@ -22,6 +22,7 @@
 //    warps share each 16-column slice, one per 128-deep scale group of every
 //    stage. Grouped launches (a decoder step's linears) stream all problems'
 //    tiles through one pipeline.
+//  * 17 to 64 tokens: the tcgen05 kernel of gemm_w4a16_tc.cu.
 // Common to both:
 //  * swap A and B: the MMA computes Y^T = W^T A^T, so 16 weight columns fill
 //    the MMA's 16-row side and up to 8 tokens its 8-wide side (mma.m16n8k16,
@@ -50,9 +51,8 @@ __device__ unsigned int g_w4a16_err;
 
 constexpr int KT = 256;                 // K per pipeline stage (two scale groups)
 
-// Widest tile of the TMA-staged kernel (9 to 64 tokens): more tokens need more
-// accumulator registers, so fewer (wider-register) MMA warps.
-__host__ __device__ constexpr int ntmax_for(int mt) { return mt <= 16 ? 128 : 64; }
+// Widest tile of the TMA-staged kernel (9 to 16 tokens): 128 columns, 16 MMA warps.
+__host__ __device__ constexpr int ntmax_for(int) { return 128; }
 constexpr int PER_LAUNCH = 56;          // problems per launch (kernel parameter space: 32 KB)
 constexpr int WBOX = 4096;              // one 32-column x 32-row weight box
 
@@ -583,7 +583,7 @@ qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int 
         total += (q.N + nt - 1) / nt;
     }
     P.total_tiles = total;
-    return mt == 16 ? launch_mt<16>(P, nt, st) : mt == 32 ? launch_mt<32>(P, nt, st) : launch_mt<64>(P, nt, st);
+    return launch_mt<16>(P, nt, st);             // 9..16 tokens (the only width this kernel serves)
 }
 
 } // namespace
@@ -612,6 +612,7 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
         }
         return QZ_OK;
     }
+    if (mt >= 32) return w4a16_tc_launch(problems, count, mt, st);   // 17..64 tokens: tcgen05
     int nt = ntmax_for(mt);
     if (count == 1) {
         const int N = problems[0].N;

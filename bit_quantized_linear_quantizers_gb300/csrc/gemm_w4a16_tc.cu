@@ -1,0 +1,361 @@
+// gemm_w4a16_tc.cu -- W4A16 GEMM for 17 to 64 tokens on the tcgen05 tensor
+// cores: Y[M, N] = A[M, K] (bf16) times an INT4 weight with one bf16 scale per
+// 128 rows of K, fp32 accumulation, bf16 output ("量化：让每一步搬更少的字节",
+// 路线一: one kernel that unpacks, dequantizes and multiplies, so the packed
+// weights cross HBM once).
+//
+// The MMA computes Y^T = W^T A^T: the 128 weight columns of a tile are the
+// MMA's M side, the tokens its N side (N = MT = 32 or 64), so one staged
+// activation slice serves 128 weight columns. Per CTA (one per SM, persistent
+// over tiles of 128 weight columns x all of K, several problems per launch):
+//  warp 0       TMA producer: per 128-deep K group, the packed weights (16
+//               k-octet rows x 128 columns of int32, 8 KB) and the activations
+//               (two 64-element x MT boxes, 128-byte swizzle) into a ring.
+//  warps 2-9    unpack: each packed word (8 consecutive k of one column)
+//               becomes 8 exact bf16 integers q in [-8, 7], written as one
+//               16-byte chunk of a 128-byte-swizzled K-major bf16 tile (the
+//               UMMA layout), double-buffered; then fence.proxy.async so the
+//               tensor core sees the stores.
+//  warp 1       MMA issuer (one thread): per group 8 x tcgen05.mma kind::f16
+//               (M = 128, N = MT, K = 16) into one of four TMEM accumulators.
+//  warps 10-13  promotion + epilogue: thread = one weight column (its TMEM
+//               lane); per group it loads the MT partial sums, multiplies them
+//               by the group's bf16 scale and adds them into fp32 registers
+//               (the scale is not folded into bf16 weights, which would round);
+//               at the end of the tile it rounds to bf16 and stores column n of
+//               every token row.
+// Every wait is bounded; on expiry the kernel records QZ_ERR_TIMEOUT and winds
+// down.
+#include "qz_tc.cuh"
+
+#include <cuda_bf16.h>
+#include <algorithm>
+
+namespace qz {
+
+namespace {
+
+__device__ unsigned int g_w4tc_err;
+
+constexpr int TN = 128;                           // weight columns per tile (MMA M)
+constexpr int GK = 128;                           // K per group = per pipeline stage
+constexpr int W_BYTES = (GK / 8) * TN * 4;        // packed weights of one group: 8 KB
+constexpr int WT_BYTES = TN * GK * 2;             // unpacked bf16 tile: 32 KB
+constexpr int NWT = 2;                            // unpacked tiles in flight
+constexpr int NACC = 4;                           // TMEM accumulators in flight
+constexpr int UNPACK_WARPS = 8, PROMO_WARPS = 4;
+constexpr int THREADS = (2 + UNPACK_WARPS + PROMO_WARPS) * 32;
+constexpr int TC_PER_LAUNCH = 80;                 // problems per launch (kernel parameter space)
+
+struct TcProb {
+    CUtensorMap tmW;                              // qweight [K/8][N] int32, box 128 x 16, no swizzle
+    CUtensorMap tmA;                              // A [M][K] bf16, box 64 x MT, 128-byte swizzle
+    const uint16_t* S;                            // scale bf16 [K/128][N]
+    uint16_t* Y;                                  // bf16 [M][N]
+    int M, N, K;
+    int tile_begin;
+};
+
+struct TcParams {
+    TcProb p[TC_PER_LAUNCH];
+    int count;
+    int total_tiles;
+};
+
+template <int MT>
+struct TcLayout {
+    static constexpr int A_BYTES = MT * GK * 2;                       // two 64 x MT boxes
+    static constexpr int STAGE = (W_BYTES + A_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGES = (MT == 64 ? 5 : 8);
+    static constexpr int SMEM = STAGES * STAGE + NWT * WT_BYTES + 512 + 1024;
+    static constexpr uint32_t TMEM_COLS = NACC * MT < 32 ? 32 : NACC * MT;
+    static constexpr uint32_t IDESC = idesc_dense(1u, 1u, TN, MT);   // bf16 x bf16 -> fp32
+};
+
+__device__ __forceinline__ void mma_bf16_tc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Packed word -> 8 exact bf16 integers (element 2B in the low nibble of byte B,
+// two's complement). One byte-permute brings the even code of byte B (from w)
+// and the odd one (from w >> 4) into the low nibbles of the two halves; one
+// lop3 keeps the nibbles, flips their sign bit (u = q + 8) and sets the
+// exponent of 128, so each half holds 128 + u exactly; one bf16x2 fma
+// (x * 1 - 136) leaves q.
+template <int B>
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, uint32_t w4) {
+    const uint32_t r = __byte_perm(w, w4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
+    uint32_t v, out;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43084308u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out) : "r"(v), "r"(0x3F803F80u), "r"(0xC308C308u));
+    return out;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(THREADS, 1)
+w4a16_tc_kernel(const __grid_constant__ TcParams P) {
+    using L = TcLayout<MT>;
+    constexpr int S = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t wtbase = sbase + S * L::STAGE;
+    uint8_t* wt_gen = smem + S * L::STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * L::STAGE + NWT * WT_BYTES);
+    auto full = [&](int s) { return smem_u32(bars + s); };
+    auto empty = [&](int s) { return smem_u32(bars + S + s); };
+    auto wfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
+    auto wempty = [&](int b) { return smem_u32(bars + 2 * S + NWT + b); };
+    auto afull = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + b); };
+    auto aempty = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + NACC + b); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NWT + 2 * NACC);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto find = [&](int tile) {                   // last problem with tile_begin <= tile
+        int lo = 0, hi = P.count - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.p[mid].tile_begin <= tile) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < NWT; b++) {
+            mbar_init(wfull(b), UNPACK_WARPS);
+            mbar_init(wempty(b), 1);
+        }
+        for (int b = 0; b < NACC; b++) {
+            mbar_init(afull(b), 1);
+            mbar_init(aempty(b), PROMO_WARPS);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // Programmatic dependent launch: the next kernel may start launching now;
+    // this one waits for the previous kernel only before loading activations.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true, waited = false;
+            for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+                const TcProb& pr = P.p[find(tile)];
+                const int n0 = (tile - pr.tile_begin) * TN;
+                const int ng = pr.K / GK;
+                prefetch_tmap(&pr.tmW);
+                prefetch_tmap(&pr.tmA);
+                for (int g = 0; g < ng; g++, it++) {
+                    const int s = it % S;
+                    if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
+                    const uint32_t st = sbase + s * L::STAGE;
+                    mbar_arrive_expect_tx(full(s), W_BYTES + L::A_BYTES);
+                    tma_load_2d(st, &pr.tmW, n0, g * (GK / 8), full(s));              // columns past N: zeros
+                    if (!waited) {
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        waited = true;
+                    }
+                    tma_load_2d(st + W_BYTES, &pr.tmA, g * GK, 0, full(s));           // tokens past M: zeros
+                    tma_load_2d(st + W_BYTES + MT * 128, &pr.tmA, g * GK + 64, 0, full(s));
+                }
+            }
+            for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; j++)
+                mbar_wait(empty(j % S), (j / S) & 1, &g_w4tc_err);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+                const int ng = P.p[find(tile)].K / GK;
+                for (int g = 0; g < ng; g++, it++) {
+                    const int s = it % S, wb = it % NWT, ab = it % NACC;
+                    if (!mbar_wait(aempty(ab), ((it / NACC) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
+                    if (!mbar_wait(full(s), (it / S) & 1, &g_w4tc_err)) { ok = false; break; }
+                    if (!mbar_wait(wfull(wb), (it / NWT) & 1, &g_w4tc_err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + ab * MT;
+#pragma unroll
+                    for (int ks = 0; ks < GK / 16; ks++) {               // K = 16 per MMA
+                        const int slab = ks >> 2, kk = ks & 3;           // 64-element slab, 32-byte step
+                        const uint64_t ad = sdesc_k_sw128(wtbase + wb * WT_BYTES + slab * (TN * 128)) + kk * 2;
+                        const uint64_t bd = sdesc_k_sw128(sbase + s * L::STAGE + W_BYTES + slab * (MT * 128)) + kk * 2;
+                        mma_bf16_tc(d, ad, bd, L::IDESC, ks > 0);
+                    }
+                    tc_commit(empty(s));
+                    tc_commit(wempty(wb));
+                    tc_commit(afull(ab));
+                }
+            }
+            if (it > 0) mbar_wait(afull((it - 1) % NACC), ((it - 1) / NACC) & 1, &g_w4tc_err);
+        }
+        __syncwarp();
+    } else if (warp < 2 + UNPACK_WARPS) {
+        // ------------------------------------------------------------ unpack
+        const int t = threadIdx.x - 64;                  // 0 .. 255
+        const int n = t & (TN - 1), j0 = t >> 7;         // column; first k-octet row (0 or 1)
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+            const int ng = P.p[find(tile)].K / GK;
+            for (int g = 0; g < ng; g++, it++) {
+                const int s = it % S, wb = it % NWT;
+                if (!mbar_wait(full(s), (it / S) & 1, &g_w4tc_err)) { ok = false; break; }
+                if (!mbar_wait(wempty(wb), ((it / NWT) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
+                const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(smem + s * L::STAGE);
+                uint8_t* dst = wt_gen + wb * WT_BYTES + n * 128;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int j = j0 + 2 * i;                    // k-octet row of the group
+                    const uint32_t w = wsrc[j * TN + n], w4 = w >> 4;
+                    uint4 o;
+                    o.x = unpack_pair<0>(w, w4);
+                    o.y = unpack_pair<1>(w, w4);
+                    o.z = unpack_pair<2>(w, w4);
+                    o.w = unpack_pair<3>(w, w4);
+                    // row n of slab j/8; 16-byte chunk j%8 at position (j%8) ^ (n%8)
+                    *reinterpret_cast<uint4*>(dst + (j >> 3) * (TN * 128) + ((((j & 7) ^ (n & 7))) << 4)) = o;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wfull(wb));
+            }
+        }
+    } else {
+        // ------------------------------------------------ promotion + epilogue
+        const int q = warp & 3;                          // TMEM lane quarter
+        const int n = q * 32 + lane;                     // weight column within the tile
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
+            const TcProb& pr = P.p[find(tile)];
+            const int n0 = (tile - pr.tile_begin) * TN;
+            const int ng = pr.K / GK;
+            const bool col_ok = n0 + n < pr.N;
+            const uint16_t* srow = pr.S + n0 + (col_ok ? n : 0);
+            float acc[MT];
+#pragma unroll
+            for (int i = 0; i < MT; i++) acc[i] = 0.0f;
+            uint32_t sraw = __ldg(srow);                  // scale of group 0, then one group ahead
+            for (int g = 0; g < ng; g++, it++) {
+                const float sc = bf16_bits_to_f32(sraw);
+                if (g + 1 < ng) sraw = __ldg(srow + (size_t)(g + 1) * pr.N);
+                const int ab = it % NACC;
+                if (!mbar_wait(afull(ab), (it / NACC) & 1, &g_w4tc_err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * MT;
+#pragma unroll
+                for (int c = 0; c < MT / 16; c++) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c * 16, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c * 16 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aempty(ab));
+            }
+            if (!ok) break;
+            if (col_ok) {
+                const int mrows = min(pr.M, MT);
+                uint16_t* ycol = pr.Y + n0 + n;
+#pragma unroll
+                for (int m = 0; m < MT; m++)
+                    if (m < mrows) ycol[(size_t)m * pr.N] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int MT>
+qz_status launch_tc(const TcParams& P, cudaStream_t st) {
+    using L = TcLayout<MT>;
+    static int attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(w4a16_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
+            cudaSuccess)
+            return QZ_ERR_CUDA;
+        attr_set[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(P.total_tiles, num_sms()));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)L::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<MT>, P) != cudaSuccess) return QZ_ERR_CUDA;
+    return launch_status();
+}
+
+} // namespace
+
+qz_status w4a16_tc_error_read_and_clear() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_w4tc_err, sizeof(v)) != cudaSuccess) return QZ_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_w4tc_err, &z, sizeof(z)) != cudaSuccess) return QZ_ERR_CUDA;
+    return v ? QZ_ERR_TIMEOUT : QZ_OK;
+}
+
+// Problems with 17..64 tokens (mt = 32 or 64 padded rows), up to 80 per launch.
+qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st) {
+    for (int i0 = 0; i0 < count; i0 += TC_PER_LAUNCH) {
+        TcParams P;
+        int tiles = 0;
+        P.count = std::min(TC_PER_LAUNCH, count - i0);
+        for (int i = 0; i < P.count; i++) {
+            const qz_w4a16_problem& q = problems[i0 + i];
+            TcProb& p = P.p[i];
+            if (!encode_tmap_2d(&p.tmW, q.qweight, 4, (uint64_t)q.N, (uint64_t)q.K / 8, (uint64_t)q.N * 4, TN,
+                                GK / 8, false) ||
+                !encode_tmap_2d(&p.tmA, q.A, 2, (uint64_t)q.K, (uint64_t)q.M, (uint64_t)q.K * 2, 64, (uint32_t)mt,
+                                true))
+                return QZ_ERR_CUDA;
+            p.S = q.scale_bf16;
+            p.Y = q.Y;
+            p.M = q.M; p.N = q.N; p.K = q.K;
+            p.tile_begin = tiles;
+            tiles += (q.N + TN - 1) / TN;
+        }
+        P.total_tiles = tiles;
+        const qz_status s = mt == 32 ? launch_tc<32>(P, st) : launch_tc<64>(P, st);
+        if (s != QZ_OK) return s;
+    }
+    return QZ_OK;
+}
+
+} // namespace qz

@@ -50,11 +50,12 @@ qz_status device_check() {
 }
 
 qz_status device_error_read_and_clear() {
-    qz_status s = w4a16_error_read_and_clear();
-    if (s != QZ_OK) return s;
-    s = fp8_block_error_read_and_clear();
-    if (s != QZ_OK) return s;
-    return fp4_error_read_and_clear();
+    // read and clear every word, report the first error found
+    const qz_status s[4] = {w4a16_error_read_and_clear(), w4a16_tc_error_read_and_clear(),
+                            fp8_block_error_read_and_clear(), fp4_error_read_and_clear()};
+    for (qz_status v : s)
+        if (v != QZ_OK) return v;
+    return QZ_OK;
 }
 
 qz_status launch_status() {

@@ -32,6 +32,9 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
 // Device error words of the GEMM translation units (read and cleared by
 // qz_device_error). Each returns QZ_OK, QZ_ERR_TIMEOUT or QZ_ERR_CUDA.
 qz_status w4a16_error_read_and_clear();
+qz_status w4a16_tc_error_read_and_clear();
+// tcgen05 W4A16 for 17..64 tokens (mt = 32 or 64: the token count padded)
+qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st);
 qz_status fp8_block_error_read_and_clear();
 qz_status fp4_error_read_and_clear();
 qz_status device_error_read_and_clear();

@@ -71,6 +71,16 @@ def test_w4a16_shapes(qz, K, N):
     check(run(qz, A, qw, sc), y_ref, bound, f"K={K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(24, 256, 192), (64, 640, 320), (12, 128, 64)])
+def test_w4a16_partial_column_tiles(qz, M, K, N):
+    """N not a multiple of the 128-column tiles of the tensor-core kernel (9-64 tokens):
+    the columns past N are read as zeros and never stored."""
+    qw, sc = quantized_weight(K, N, seed=N)
+    A = activations(M, K, seed=M)
+    y_ref, bound = oracle.gemm_w4a16(A, qw, sc)
+    check(run(qz, A, qw, sc), y_ref, bound, f"M={M} K={K} N={N}")
+
+
 def test_w4a16_integer_exact(qz):
     """Unit scales and small integer activations: the result is an exact integer
     (a plain integer matmul), so the GPU must match it exactly after bf16 rounding."""
