@@ -11,12 +11,14 @@
 //  warp 0       TMA producer: per 128-deep K group, the packed weights (16
 //               k-octet rows x 128 columns of int32, 8 KB) and the activations
 //               (two 64-element x MT boxes, 128-byte swizzle) into a ring.
-//  warps 2-9    unpack: each packed word (8 consecutive k of one column)
-//               becomes 8 exact bf16 integers q in [-8, 7], written as one
-//               16-byte chunk of a 128-byte-swizzled K-major bf16 tile (the
-//               UMMA layout), double-buffered; then fence.proxy.async so the
-//               tensor core sees the stores.
+//  warps 2-9    unpack: thread = one weight column (its TMEM lane); each of
+//               its packed words (8 consecutive k) becomes 8 exact bf16
+//               integers q in [-8, 7], and the 64 K of the thread's half of
+//               the group go straight from registers into tensor memory
+//               (tcgen05.st), which is where the MMA reads its A operand from
+//               (double-buffered, 64 TMEM columns per group).
 //  warp 1       MMA issuer (one thread): per group 8 x tcgen05.mma kind::f16
+//               with A in TMEM and the activations from shared memory
 //               (M = 128, N = MT, K = 16) into one of four TMEM accumulators.
 //  warps 10-13  promotion + epilogue: thread = one weight column (its TMEM
 //               lane); per group it loads the MT partial sums, multiplies them
@@ -40,8 +42,7 @@ __device__ unsigned int g_w4tc_err;
 constexpr int TN = 128;                           // weight columns per tile (MMA M)
 constexpr int GK = 128;                           // K per group = per pipeline stage
 constexpr int W_BYTES = (GK / 8) * TN * 4;        // packed weights of one group: 8 KB
-constexpr int WT_BYTES = TN * GK * 2;             // unpacked bf16 tile: 32 KB
-constexpr int NWT = 2;                            // unpacked tiles in flight
+constexpr int NWT = 2;                            // unpacked weight tiles (in TMEM) in flight
 constexpr int NACC = 4;                           // TMEM accumulators in flight
 constexpr int UNPACK_WARPS = 8, PROMO_WARPS = 4;
 constexpr int THREADS = (2 + UNPACK_WARPS + PROMO_WARPS) * 32;
@@ -66,22 +67,32 @@ template <int MT>
 struct TcLayout {
     static constexpr int A_BYTES = MT * GK * 2;                       // two 64 x MT boxes
     static constexpr int STAGE = (W_BYTES + A_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = (MT == 64 ? 5 : 8);
-    static constexpr int SMEM = STAGES * STAGE + NWT * WT_BYTES + 512 + 1024;
-    static constexpr uint32_t TMEM_COLS = NACC * MT < 32 ? 32 : NACC * MT;
+    static constexpr int STAGES = MT == 64 ? 8 : 12;      // 196 KB of ring
+    static constexpr int SMEM = STAGES * STAGE + 512 + 1024;
+    static constexpr uint32_t ACC_COLS = NACC * MT;                     // accumulators first
+    static constexpr uint32_t TMEM_COLS = ACC_COLS + NWT * 64 <= 128 ? 128 : ACC_COLS + NWT * 64 <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC = idesc_dense(1u, 1u, TN, MT);   // bf16 x bf16 -> fp32
 };
 
-__device__ __forceinline__ void mma_bf16_tc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+// D (TMEM) (+)= A (TMEM, 128 lanes x K/2 columns of bf16 pairs) x B (smem desc)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// 32 consecutive 32-bit columns of this thread's TMEM lane from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                   "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+                   "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+                   "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+                   "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Packed word -> 8 exact bf16 integers (element 2B in the low nibble of byte B,
 // two's complement). One byte-permute brings the even code of byte B (from w)
@@ -106,9 +117,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t wtbase = sbase + S * L::STAGE;
-    uint8_t* wt_gen = smem + S * L::STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * L::STAGE + NWT * WT_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * L::STAGE);
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + S + s); };
     auto wfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
@@ -197,11 +206,11 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
                     tc_fence_after();
                     const uint32_t d = tmem_base + ab * MT;
 #pragma unroll
-                    for (int ks = 0; ks < GK / 16; ks++) {               // K = 16 per MMA
+                    for (int ks = 0; ks < GK / 16; ks++) {               // K = 16 per MMA = 8 TMEM columns
                         const int slab = ks >> 2, kk = ks & 3;           // 64-element slab, 32-byte step
-                        const uint64_t ad = sdesc_k_sw128(wtbase + wb * WT_BYTES + slab * (TN * 128)) + kk * 2;
+                        const uint32_t at = tmem_base + L::ACC_COLS + wb * 64 + ks * 8;
                         const uint64_t bd = sdesc_k_sw128(sbase + s * L::STAGE + W_BYTES + slab * (MT * 128)) + kk * 2;
-                        mma_bf16_tc(d, ad, bd, L::IDESC, ks > 0);
+                        mma_bf16_ts(d, at, bd, L::IDESC, ks > 0);
                     }
                     tc_commit(empty(s));
                     tc_commit(wempty(wb));
@@ -213,8 +222,8 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
         __syncwarp();
     } else if (warp < 2 + UNPACK_WARPS) {
         // ------------------------------------------------------------ unpack
-        const int t = threadIdx.x - 64;                  // 0 .. 255
-        const int n = t & (TN - 1), j0 = t >> 7;         // column; first k-octet row (0 or 1)
+        const int q = warp & 3, h = (warp - 2) >> 2;     // TMEM lane quarter; half of the group's K
+        const int n = q * 32 + lane;                     // weight column = TMEM lane
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
@@ -223,21 +232,20 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
                 const int s = it % S, wb = it % NWT;
                 if (!mbar_wait(full(s), (it / S) & 1, &g_w4tc_err)) { ok = false; break; }
                 if (!mbar_wait(wempty(wb), ((it / NWT) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
+                tc_fence_after();
                 const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(smem + s * L::STAGE);
-                uint8_t* dst = wt_gen + wb * WT_BYTES + n * 128;
+                uint32_t o[32];
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const int j = j0 + 2 * i;                    // k-octet row of the group
-                    const uint32_t w = wsrc[j * TN + n], w4 = w >> 4;
-                    uint4 o;
-                    o.x = unpack_pair<0>(w, w4);
-                    o.y = unpack_pair<1>(w, w4);
-                    o.z = unpack_pair<2>(w, w4);
-                    o.w = unpack_pair<3>(w, w4);
-                    // row n of slab j/8; 16-byte chunk j%8 at position (j%8) ^ (n%8)
-                    *reinterpret_cast<uint4*>(dst + (j >> 3) * (TN * 128) + ((((j & 7) ^ (n & 7))) << 4)) = o;
+                for (int i = 0; i < 8; i++) {                    // k-octet rows 8h .. 8h+7
+                    const uint32_t w = wsrc[(8 * h + i) * TN + n], w4 = w >> 4;
+                    o[4 * i + 0] = unpack_pair<0>(w, w4);
+                    o[4 * i + 1] = unpack_pair<1>(w, w4);
+                    o[4 * i + 2] = unpack_pair<2>(w, w4);
+                    o[4 * i + 3] = unpack_pair<3>(w, w4);
                 }
-                fence_proxy_async_smem();
+                tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + L::ACC_COLS + wb * 64 + h * 32, o);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(wfull(wb));
             }
