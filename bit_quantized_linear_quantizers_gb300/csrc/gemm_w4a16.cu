@@ -111,12 +111,6 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t w4) {
     return out;
 }
 
-// Word at (row r, column c) of a 32 x 32-word box written by TMA with the
-// 128-byte swizzle (16-byte chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t wbox_word(const uint8_t* box, int r, int c) {
-    return *reinterpret_cast<const uint32_t*>(box + r * 128 + ((((c >> 2) ^ (r & 7)) << 4) | ((c & 3) << 2)));
-}
-
 // ------------------------------------------------ register-direct kernel
 
 constexpr int RD_COLS = 32;             // weight columns per CTA

@@ -431,8 +431,25 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
             if (i < total) {
                 float y[8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) y[j] = __fadd_rn(__fmul_rn(v[u][j], inv), 0.0f);
-                const uint32_t packed = e2m1x8_fix(e2m1x8_rne(y), y);
+                for (int j = 0; j < 8; j++) y[j] = __fadd_rn(__fmul_rn(v[u][j], inv), 0.0f);   // -0 -> +0
+                uint32_t packed;
+                if constexpr (sizeof(T) == 2) {
+                    // bf16 inputs: y = x * 2^(2-E) keeps x's 8 significant bits, so no
+                    // y lies strictly between a midpoint and the fp32 value one ulp
+                    // above it. Stepping every non-zero y one fp32 ulp toward zero
+                    // therefore moves exact midpoints just below themselves (ties go
+                    // down, the pages' rule) and changes no other code; the hardware's
+                    // round-to-nearest-even then gives the exact codes.
+                    float yd[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const uint32_t b = __float_as_uint(y[j]);
+                        yd[j] = __uint_as_float(b - min(b & 0x7FFFFFFFu, 1u));
+                    }
+                    packed = e2m1x8_rne(yd);
+                } else {
+                    packed = e2m1x8_fix(e2m1x8_rne(y), y);
+                }
                 reinterpret_cast<uint32_t*>(codes)[i] = packed;
                 if (deq) {
                     float o[8];
