@@ -21,7 +21,7 @@ __all__ = [
     "qz_device_error", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
     "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
     "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
-    "qz_gemm_nvfp4_grouped", "Workspace",
+    "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
 ]
 
 F32, BF16 = 0, 1
@@ -29,7 +29,7 @@ FP8_PER_TENSOR, FP8_PER_ROW, FP8_BLOCK_128x128, FP8_GROUP_1x128 = 0, 1, 2, 3
 SCALE_COMPUTE, SCALE_GIVEN = 0, 1
 OP_QUANTIZE_FP8, OP_QUANTIZE_NVFP4, OP_KV_WRITE_FP8 = 0, 1, 2
 OP_GEMM_W4A16, OP_GEMM_FP8_BLOCK, OP_GEMM_NVFP4, OP_GEMM_MXFP4 = 3, 4, 5, 6
-OP_GEMM_NVFP4_GROUPED, OP_PREPARE_FP4_SCALES = 7, 8
+OP_GEMM_NVFP4_GROUPED, OP_PREPARE_FP4_SCALES, OP_QUANTIZE_NVFP4_GROUPED = 7, 8, 9
 
 if not os.path.exists(LIB):
     raise ImportError(f"libqz.so is not built ({LIB}); run bit_quantized_linear_quantizers_gb300.build() "
@@ -50,6 +50,11 @@ class _Nvfp4Problem(ctypes.Structure):
                 ("Y", _P), ("M", _I), ("N", _I), ("K", _I)]
 
 
+class _Nvfp4Tensor(ctypes.Structure):
+    _fields_ = [("x", _P), ("rows", _I64), ("cols", _I64), ("codes", _P), ("scale_e4m3", _P),
+                ("global_scale", _P)]
+
+
 _SIGS = {
     "qz_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
     "qz_status_string": (ctypes.c_char_p, [_I]),
@@ -67,6 +72,7 @@ _SIGS = {
     "qz_gemm_nvfp4_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "qz_prepare_fp4_scales": (_I, [_P, _I, _I, _I, _P, _P]),
     "qz_gemm_nvfp4_grouped": (_I, [ctypes.POINTER(_Nvfp4Problem), _I, _P, _SZ, _P]),
+    "qz_quantize_nvfp4_grouped": (_I, [ctypes.POINTER(_Nvfp4Tensor), _I, _I, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -208,6 +214,35 @@ def qz_quantize_nvfp4(x: torch.Tensor, codes=None, scale_e4m3=None, global_scale
                                  _ptr(global_scale), _ptr(global_amax_in), _ptr(deq), _ptr(buf), nb,
                                  _stream(stream)), "qz_quantize_nvfp4")
     return codes, scale_e4m3, global_scale, deq
+
+
+def qz_quantize_nvfp4_grouped(xs, outs=None, ws=None, stream=None):
+    """NVFP4 quantization of several contiguous 2-D tensors of one dtype in two launches.
+    Returns [(codes, scale_e4m3, global_scale), ...] as qz_quantize_nvfp4 would per tensor;
+    `outs` may give those buffers."""
+    n = len(xs)
+    arr = (_Nvfp4Tensor * n)()
+    res = []
+    xt = _dtype_code(xs[0]) if n else F32
+    for i, x in enumerate(xs):
+        if x.dim() != 2 or not x.is_contiguous():
+            raise ValueError("qz_quantize_nvfp4_grouped takes contiguous 2-D tensors")
+        if _dtype_code(x) != xt:
+            raise TypeError("qz_quantize_nvfp4_grouped takes tensors of one dtype")
+        rows, cols = x.shape
+        if outs is not None:
+            codes, sc, g = outs[i]
+        else:
+            codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+            sc = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+            g = torch.empty((1,), dtype=torch.float32, device=x.device)
+        arr[i] = _Nvfp4Tensor(x.data_ptr(), rows, cols, codes.data_ptr(), sc.data_ptr(), g.data_ptr())
+        res.append((codes, sc, g))
+    dev = xs[0].device if n else torch.device("cuda")
+    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4_GROUPED, n) if n else 0, dev)
+    _check(lib.qz_quantize_nvfp4_grouped(arr, n, xt, _ptr(buf), nb, _stream(stream)),
+           "qz_quantize_nvfp4_grouped")
+    return res
 
 
 def qz_quantize_int4_g128(w: torch.Tensor, qweight=None, scale_bf16=None, dequant=False, stream=None):

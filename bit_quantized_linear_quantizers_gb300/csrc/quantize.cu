@@ -515,6 +515,101 @@ nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
     }
 }
 
+// ------------------------------------------------- NVFP4, many tensors
+
+// A decode step's activations (one small tensor per linear) quantized in two
+// launches instead of two per tensor: kernel 1 reduces each tensor's amax in
+// NV_SLICES partial maxima (one CTA per slice), kernel 2 walks the
+// concatenation of all tensors' 8-element chunks; each chunk looks up its
+// tensor, reduces that tensor's partials to g and encodes as nvfp4_kernel does.
+constexpr int NV_GROUP_MAX = 256;
+constexpr int NV_SLICES = 4;
+
+struct NvTensor {
+    const void* x;                      // contiguous [rows, cols]
+    uint8_t* codes;                     // [rows, cols/2]
+    uint8_t* sb;                        // [rows, cols/16]
+    float* g;                           // 1 fp32
+    long long chunk_begin;              // first 8-element chunk of this tensor in the launch
+    long long chunks;
+};
+
+struct NvGroup {
+    NvTensor t[NV_GROUP_MAX];
+    int count;
+    long long total_chunks;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+nvfp4_group_amax_kernel(const __grid_constant__ NvGroup P, float* __restrict__ partial) {
+    __shared__ float red[kWarps];
+    const int ti = blockIdx.x / NV_SLICES, sl = blockIdx.x % NV_SLICES;
+    const NvTensor& tn = P.t[ti];
+    const T* x = static_cast<const T*>(tn.x);
+    const long long cb = tn.chunks * sl / NV_SLICES, ce = tn.chunks * (sl + 1) / NV_SLICES;
+    float m = 0.0f;
+    for (long long i0 = cb + threadIdx.x; i0 < ce; i0 += (long long)U * kThreads) {
+        float v[U][8];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const long long i = i0 + (long long)u * kThreads;
+            if (i < ce) Load8<T>::run(x + i * 8, v[u]);
+            else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+    }
+    m = block_max(m, red);
+    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+    pdl_trigger();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+nvfp4_group_encode_kernel(const __grid_constant__ NvGroup P, const float* __restrict__ partial) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const Recip d6(kFp4Max);
+    const long long wbase = (((long long)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
+    const long long wstride = (long long)gridDim.x * kThreads;
+    for (long long base = wbase; base < P.total_chunks; base += wstride) {   // warp-uniform
+        const long long i = base + lane;
+        const bool live = i < P.total_chunks;
+        int lo = 0, hi = P.count - 1;                    // tensor of chunk i (tensors hold even chunk counts)
+        const long long ic = live ? i : P.total_chunks - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.t[mid].chunk_begin <= ic) lo = mid; else hi = mid - 1;
+        }
+        const NvTensor& tn = P.t[lo];
+        const long long li = ic - tn.chunk_begin;
+        float amax_t = 0.0f;
+#pragma unroll
+        for (int k = 0; k < NV_SLICES; k++) amax_t = fmaxf(amax_t, __ldg(partial + lo * NV_SLICES + k));
+        const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
+        if (live && li == 0) *tn.g = g;
+        const Recip dg(g);
+        float v[8];
+        if (live) Load8<T>::run(static_cast<const T*>(tn.x) + li * 8, v);
+        else for (int j = 0; j < 8; j++) v[j] = 0.0f;
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
+        m = warp_max(m, 2);                               // the other half of the 16-element block
+        const float t = div1(div1(m, d6), dg);
+        const uint32_t bcode = e4m3_code(t);
+        const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
+        const uint32_t packed = fp4_encode8(v, Recip(s), nullptr);   // all 32 lanes (warp vote)
+        if (live) {
+            reinterpret_cast<uint32_t*>(tn.codes)[li] = packed;
+            if ((li & 1) == 0) tn.sb[li >> 1] = (uint8_t)bcode;
+        }
+    }
+}
+
 // --------------------------------------------------------------- INT4 g128
 
 // One CTA per (group of 128 rows) x (64 columns) tile of w[K, N]: the tile is
@@ -705,6 +800,38 @@ qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_
         if (partial) launch_tensor_amax<uint16_t, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
         launch_dependent(nvfp4_kernel<uint16_t>, dim3(grid), dim3(kThreads), st, (const uint16_t*)x, rows, cols,
                          ldx, contig, cpart, np, amax_in, codes, sb, g, deq);
+    }
+    return launch_status();
+}
+
+size_t ws_quantize_nvfp4_grouped(int count) { return (size_t)count * NV_SLICES * sizeof(float); }
+
+qz_status quantize_nvfp4_grouped_launch(const qz_nvfp4_tensor* tensors, int count, qz_dtype xt, void* ws,
+                                        cudaStream_t st) {
+    NvGroup P;
+    P.count = count;
+    long long total = 0;
+    for (int i = 0; i < count; i++) {
+        const qz_nvfp4_tensor& q = tensors[i];
+        NvTensor& t = P.t[i];
+        t.x = q.x;
+        t.codes = q.codes;
+        t.sb = q.scale_e4m3;
+        t.g = q.global_scale;
+        t.chunk_begin = total;
+        t.chunks = q.rows * q.cols / 8;
+        total += t.chunks;
+    }
+    P.total_chunks = total;
+    float* partial = static_cast<float*>(ws);
+    const int grid = stream_grid(total, kEncoderCtasPerSm);
+    if (xt == QZ_F32) {
+        nvfp4_group_amax_kernel<float><<<count * NV_SLICES, kThreads, 0, st>>>(P, partial);
+        launch_dependent(nvfp4_group_encode_kernel<float>, dim3(grid), dim3(kThreads), st, P, (const float*)partial);
+    } else {
+        nvfp4_group_amax_kernel<uint16_t><<<count * NV_SLICES, kThreads, 0, st>>>(P, partial);
+        launch_dependent(nvfp4_group_encode_kernel<uint16_t>, dim3(grid), dim3(kThreads), st, P,
+                         (const float*)partial);
     }
     return launch_status();
 }

@@ -99,6 +99,8 @@ size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2) {
     case QZ_OP_GEMM_NVFP4_GROUPED:
         return d0 >= 1 && d0 <= kNvfp4MaxProblems && d1 >= 1 && d1 <= (1 << 24) ? ws_gemm_nvfp4_grouped((int)d0, (int)d1)
                                                                                  : 0;
+    case QZ_OP_QUANTIZE_NVFP4_GROUPED:
+        return d0 >= 1 && d0 <= kNvfp4GroupMax ? ws_quantize_nvfp4_grouped((int)d0) : 0;
     case QZ_OP_PREPARE_FP4_SCALES:
         return d0 >= 1 && d0 <= (1 << 24) && d1 >= 1 && d1 <= (1 << 24) ? prepared_fp4_scale_bytes((int)d0, (int)d1, d2 != 0)
                                                                          : 0;
@@ -272,6 +274,21 @@ qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB,
     QZ_TRY(device_check());
     return gemm_fp4_launch(false, qA, eA, nullptr, qB, eB, nullptr, Y, M, N, K, ws, ws_bytes,
                            (cudaStream_t)stream);
+}
+
+qz_status qz_quantize_nvfp4_grouped(const qz_nvfp4_tensor* tensors, int count, qz_dtype xt, void* ws,
+                                    size_t ws_bytes, void* stream) {
+    if (!tensors || count < 1 || count > kNvfp4GroupMax || !dtype_ok(xt)) return QZ_ERR_INVALID_ARG;
+    for (int i = 0; i < count; i++) {
+        const qz_nvfp4_tensor& t = tensors[i];
+        if (!t.x || !t.codes || !t.scale_e4m3 || !t.global_scale) return QZ_ERR_INVALID_ARG;
+        if (t.rows < 1 || t.cols < 1) return QZ_ERR_INVALID_ARG;
+        if (t.cols % 16) return QZ_ERR_SHAPE;
+        if (!is_aligned(t.x, 16) || !is_aligned(t.codes, 4)) return QZ_ERR_ALIGNMENT;
+    }
+    if (!ws || ws_bytes < ws_quantize_nvfp4_grouped(count) || !is_aligned(ws, 4)) return QZ_ERR_WORKSPACE;
+    QZ_TRY(device_check());
+    return quantize_nvfp4_grouped_launch(tensors, count, xt, ws, (cudaStream_t)stream);
 }
 
 qz_status qz_prepare_fp4_scales(const uint8_t* scales, int rows, int K, int nv, uint8_t* out, void* stream) {

@@ -178,6 +178,10 @@ bool is_aligned(const void* p, size_t a);
 namespace qz {
 size_t ws_quantize_fp8_tensor(int64_t rows, int64_t cols);
 size_t ws_quantize_nvfp4(int64_t rows, int64_t cols);
+size_t ws_quantize_nvfp4_grouped(int count);
+constexpr int kNvfp4GroupMax = 256;
+qz_status quantize_nvfp4_grouped_launch(const qz_nvfp4_tensor* tensors, int count, qz_dtype xt, void* ws,
+                                        cudaStream_t st);
 size_t ws_kv_write(int64_t n);
 
 qz_status quantize_fp8_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,

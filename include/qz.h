@@ -70,8 +70,9 @@ typedef enum qz_op {
     QZ_OP_GEMM_NVFP4 = 5,     /* d0 = M, d1 = N, d2 = K                    */
     QZ_OP_GEMM_MXFP4 = 6,     /* d0 = M, d1 = N, d2 = K                    */
     QZ_OP_GEMM_NVFP4_GROUPED = 7, /* d0 = problem count, d1 = largest K    */
-    QZ_OP_PREPARE_FP4_SCALES = 8  /* d0 = rows, d1 = K, d2 = 1 NVFP4 / 0 MXFP4:
+    QZ_OP_PREPARE_FP4_SCALES = 8, /* d0 = rows, d1 = K, d2 = 1 NVFP4 / 0 MXFP4:
                                      bytes of the prepared output (not scratch) */
+    QZ_OP_QUANTIZE_NVFP4_GROUPED = 9 /* d0 = tensor count                    */
 } qz_op;
 
 /* Bytes of workspace the call `op` needs for the given sizes (0 if none).
@@ -143,6 +144,25 @@ qz_status qz_quantize_nvfp4(const void* x, qz_dtype xt, int64_t rows, int64_t co
                             uint8_t* codes, uint8_t* scale_e4m3, float* global_scale,
                             const float* global_amax_in, float* dequant,
                             void* ws, size_t ws_bytes, void* stream);
+
+/* One tensor of qz_quantize_nvfp4_grouped: contiguous x [rows, cols] (cols %
+ * 16 == 0) and its outputs, laid out as qz_quantize_nvfp4 writes them. */
+typedef struct qz_nvfp4_tensor {
+    const void* x;
+    int64_t rows, cols;
+    uint8_t* codes;
+    uint8_t* scale_e4m3;
+    float* global_scale;
+} qz_nvfp4_tensor;
+
+/* NVFP4 quantization of `count` independent tensors (the activations of a
+ * decoder step's linears, "量化部署实战", 精度比较: each linear quantizes its
+ * input) in two launches: the same computation as one qz_quantize_nvfp4 call
+ * with a computed tensor amax per tensor, bit for bit. All tensors share the
+ * dtype xt. count <= 256. Alignment: x 16 B, codes 4 B. ws:
+ * qz_workspace_size(QZ_OP_QUANTIZE_NVFP4_GROUPED, count, 0, 0) bytes. */
+qz_status qz_quantize_nvfp4_grouped(const qz_nvfp4_tensor* tensors, int count, qz_dtype xt,
+                                    void* ws, size_t ws_bytes, void* stream);
 
 /* Symmetric INT4 weight quantization with one bf16 scale per group of 128
  * along K, for a row-major weight w[K, N] (leading dim ldw >= N)

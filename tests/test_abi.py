@@ -155,3 +155,31 @@ def test_grouped_nvfp4_and_prepare_validation(qz):
     assert L.qz_prepare_fp4_scales(FAKE, 0, 256, 1, FAKE, NULL) == 1
     assert L.qz_prepare_fp4_scales(FAKE, 128, 100, 1, FAKE, NULL) == 2                 # K % 256
     assert L.qz_prepare_fp4_scales(FAKE, 128, 256, 1, ODD, NULL) == 3
+
+
+def test_grouped_nvfp4_quantize_validation(qz):
+    L = qz.lib
+    T = qz._Nvfp4Tensor
+
+    def one(n=1, **kw):
+        f = dict(x=0x10000, rows=4, cols=1024, codes=0x10000, scale_e4m3=0x10000, global_scale=0x10000)
+        f.update(kw)
+        arr = (T * n)()
+        for i in range(n):
+            arr[i] = T(**f)
+        return arr
+
+    ws_need = qz.qz_workspace_size(qz.OP_QUANTIZE_NVFP4_GROUPED, 3)
+    assert ws_need == 3 * 4 * 4
+    assert qz.qz_workspace_size(qz.OP_QUANTIZE_NVFP4_GROUPED, 257) == 0
+    assert L.qz_quantize_nvfp4_grouped(None, 1, 0, FAKE, ws_need, NULL) == 1
+    assert L.qz_quantize_nvfp4_grouped(one(), 0, 0, FAKE, ws_need, NULL) == 1             # count < 1
+    assert L.qz_quantize_nvfp4_grouped(one(257), 257, 1, FAKE, 1 << 20, NULL) == 1        # count > 256
+    assert L.qz_quantize_nvfp4_grouped(one(), 1, 5, FAKE, ws_need, NULL) == 1             # dtype
+    assert L.qz_quantize_nvfp4_grouped(one(rows=0), 1, 0, FAKE, ws_need, NULL) == 1
+    assert L.qz_quantize_nvfp4_grouped(one(global_scale=0), 1, 0, FAKE, ws_need, NULL) == 1
+    assert L.qz_quantize_nvfp4_grouped(one(cols=40), 1, 0, FAKE, ws_need, NULL) == 2      # cols % 16
+    assert L.qz_quantize_nvfp4_grouped(one(x=0x10008), 1, 0, FAKE, ws_need, NULL) == 3    # x 16-byte
+    assert L.qz_quantize_nvfp4_grouped(one(codes=0x10002), 1, 0, FAKE, ws_need, NULL) == 3
+    assert L.qz_quantize_nvfp4_grouped(one(3), 3, 0, FAKE, ws_need - 1, NULL) == 7         # workspace
+    assert L.qz_quantize_nvfp4_grouped(one(3), 3, 0, NULL, ws_need, NULL) == 7

@@ -197,6 +197,56 @@ def test_fp4_config4_full_size_sampled(qz):
             assert_same_bytes(me[r:r + 1], re_, f"{name} mx scales row {r}")
 
 
+def check_nv_grouped(qz, xs, what):
+    outs = qz.qz_quantize_nvfp4_grouped([to_dev(x) for x in xs])
+    torch.cuda.synchronize()
+    for i, (x, (c, s, g)) in enumerate(zip(xs, outs)):
+        rc, rs, rg, _ = oracle.quant_nvfp4(x, want_deq=False)
+        assert_same_bytes(host(g), np.float32([rg]), f"{what} tensor {i} global scale")
+        assert_same_bytes(host(s), rs, f"{what} tensor {i} block scales")
+        assert_same_bytes(host(c), rc, f"{what} tensor {i} codes")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_nvfp4_grouped_mixed_tensors(qz, dtype):
+    """Tensors of unrelated sizes in one call (some a single 16-element block, so one warp
+    spans several tensors); each must equal its own single-tensor quantization."""
+    shapes = [(1, 16), (1, 1024), (3, 4096), (2, 48), (17, 3072), (1, 32), (5, 64), (128, 96), (1, 16)]
+    xs = [edge_tensor(r, c, seed=11 * i + r) for i, (r, c) in enumerate(shapes)]
+    xs[3] *= np.float32(1e-30)                               # tiny amax: the 1e-12 floors decide
+    if dtype == "bf16":
+        xs = [syn.to_bf16_bits(x) for x in xs]
+    check_nv_grouped(qz, xs, f"grouped {dtype}")
+
+
+def test_nvfp4_grouped_maximum_count(qz):
+    """256 tensors (the most one call takes), all-zero ones among them."""
+    rng = np.random.default_rng(5)
+    xs = []
+    for i in range(256):
+        x = (rng.standard_normal((1 + i % 3, 16 * (1 + i % 7))) * (1 + i)).astype(np.float32)
+        if i % 50 == 0:
+            x[:] = 0.0
+        xs.append(syn.to_bf16_bits(x))
+    check_nv_grouped(qz, xs, "grouped 256")
+
+
+def test_nvfp4_grouped_decode_activations(qz):
+    """The activations of one Qwen3-0.6B decode layer at 16 tokens (q/k/v/o, gate/up, down
+    inputs), matching per-tensor qz_quantize_nvfp4 calls in the same launch configuration."""
+    rng = np.random.default_rng(9)
+    shapes = [(16, 1024)] * 3 + [(16, 2048)] + [(16, 1024)] * 2 + [(16, 3072)]
+    xs = [syn.to_bf16_bits(rng.standard_normal(s).astype(np.float32) * 3) for s in shapes]
+    outs = qz.qz_quantize_nvfp4_grouped([dev_bf16(x) for x in xs])
+    for x, (c, s, g) in zip(xs, outs):
+        c1, s1, g1, _ = qz.qz_quantize_nvfp4(dev_bf16(x))
+        torch.cuda.synchronize()
+        assert_same_bytes(host(c), host(c1), "codes vs single call")
+        assert_same_bytes(host(s), host(s1), "scales vs single call")
+        assert_same_bytes(host(g), host(g1), "global scale vs single call")
+    check_nv_grouped(qz, xs[:2], "decode layer sample")
+
+
 # -------------------------------------------------------------- INT4 g128
 
 @pytest.mark.parametrize("shape", [(128, 64), (384, 192), (1024, 1024)])
