@@ -279,7 +279,7 @@ def gpu_arm(args, rank, world, local_rank):
     h2d = COPIES * sum(M * K_DIM * 2 for M in MS)
     d2h = COPIES * sum(M * N_DIM * 2 for M in MS)
 
-    # ---- roofline of the dominant kernel: w4a16_rd_kernel (M <= 8 tokens, two thirds of
+    # ---- roofline of the dominant kernel: w4a16_bulk_kernel (M <= 8 tokens, two thirds of
     # the step's launches). Each M is timed on its own as a CUDA graph of 200 launches
     # over the rotating weight copies, CUDA events on the launching stream; the roofline
     # object is the M = 1 decode case, per_M lists every M (M = 16 runs w4a16_kernel).
@@ -290,14 +290,14 @@ def gpu_arm(args, rank, world, local_rank):
             q, s = weights[i % COPIES]
             qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
         us = timer(one, reps=200, warm=10)
-        per_m[M] = {"kernel": "w4a16_rd_kernel" if M <= 8 else "w4a16_kernel", "us": round(us, 3),
+        per_m[M] = {"kernel": "w4a16_bulk_kernel" if M <= 8 else "w4a16_kernel", "us": round(us, 3),
                     "algorithmic_bytes": step_bytes(M), "gbps": round(step_bytes(M) / us / 1e3, 1),
                     "frac_of_hbm": round(step_bytes(M) / us / 1e3 / pk["hbm_gbs"], 4)}
     achieved = per_m[1]["gbps"]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": kernel_traffic("w4a16_rd_kernel", "llama_mlp_M1"),
-                "kernel": "w4a16_rd_kernel", "workload": "M=1, K=4096, N=14336",
+                "traffic": kernel_traffic("w4a16_bulk_kernel", "llama_mlp_M1"),
+                "kernel": "w4a16_bulk_kernel", "workload": "M=1, K=4096, N=14336",
                 "peak_source": pk["source"], "algorithmic_bytes_per_launch": step_bytes(1),
                 "avg_launch_us": per_m[1]["us"],
                 "step_avg_launch_us": round(t_ms * 1e3 / (args.steps * launches_per_step), 3), "per_M": per_m}

@@ -5,8 +5,11 @@
 // is the weight bytes read from HBM, so the kernel streams the packed
 // weights exactly once and does the rest on chip.
 //
-// Two kernels share the arithmetic below:
-//  * up to 8 tokens (decode): w4a16_rd_kernel, register-direct. A CTA owns 32
+// Kernels by token count:
+//  * up to 8 tokens with K <= 8192: w4a16_bulk_kernel, the register-direct
+//    kernel's arithmetic with the CTA's whole weight range staged in shared
+//    memory by TMA boxes requested at once (see its section below).
+//  * up to 8 tokens, deeper K: w4a16_rd_kernel, register-direct. A CTA owns 32
 //    weight columns; its 8 warps split K by 128-deep scale groups. Each lane
 //    loads the packed weights with one coalesced 16-byte load per k-octet row
 //    (4 consecutive columns) straight into registers, after an L2 prefetch
@@ -23,7 +26,7 @@
 //    stage. Grouped launches (a decoder step's linears) stream all problems'
 //    tiles through one pipeline.
 //  * 17 to 64 tokens: the tcgen05 kernel of gemm_w4a16_tc.cu.
-// Common to both:
+// Common to the mma.sync kernels:
 //  * swap A and B: the MMA computes Y^T = W^T A^T, so 16 weight columns fill
 //    the MMA's 16-row side and up to 8 tokens its 8-wide side (mma.m16n8k16,
 //    bf16 in, fp32 out; MT/8 MMAs per weight fragment).
@@ -286,6 +289,200 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
     }
 }
 
+// ------------------------------------------------ bulk-staged kernel
+
+// Up to 8 tokens with K <= SA_KMAX: the arithmetic of the register-direct
+// kernel, but the CTA's whole weight and scale range is requested at once by
+// the TMA unit (one 2-D box of 16*SA_GPB k-octet rows x 32 columns plus the
+// matching 64-byte scale rows per mbarrier) into shared memory. The memory
+// system then holds the whole launch in flight from its first microsecond and
+// each warp only waits for the box of the group it is about to use; no
+// registers are spent on loads in flight. With a single token, sum(a) of a
+// group comes from one MMA whose 8 columns are 16-deep slices of the token's
+// activations (the ones fragment sums each column), instead of eight.
+constexpr int SA_GPB = 2;               // 128-deep scale groups per box and mbarrier
+constexpr int SA_MAX_PROBLEMS = 120;    // problems per launch (kernel parameter space: 32 KB)
+constexpr int SA_KMAX = 8192;           // deepest K staged whole (132 KB of weights per CTA)
+constexpr uint32_t SA_RED_BYTES = RD_WARPS * 8 * (RD_COLS + 1) * 4;
+
+struct SaProb {
+    CUtensorMap tmW;                    // qweight [K/8][N] int32, box 32 x 16*SA_GPB, no swizzle
+    const uint16_t* A;                  // bf16 [M, K]
+    const uint16_t* S;                  // bf16 [K/128, N]
+    uint16_t* Y;                        // bf16 [M, N]
+    int M, N, K;
+    int cta_begin;                      // first CTA of this problem
+};
+
+struct SaParams {
+    SaProb p[SA_MAX_PROBLEMS];
+    int count;
+};
+
+// Shared memory: whole boxes of weights (a partial last box is zero-filled
+// past K; the region later holds the cross-warp sums), the scale rows, the
+// mbarriers; 1 KB of slack to align the base.
+__host__ __device__ inline uint32_t sa_wregion(int K) {
+    const uint32_t nb = (uint32_t)((K / 128 + SA_GPB - 1) / SA_GPB);
+    const uint32_t w = nb * SA_GPB * 2048u;
+    return w > SA_RED_BYTES ? w : ((SA_RED_BYTES + 127u) & ~127u);
+}
+__host__ __device__ inline uint32_t sa_smem_bytes(int K) {
+    const int ng = K / 128, nb = (ng + SA_GPB - 1) / SA_GPB;
+    return 1024u + sa_wregion(K) + (uint32_t)ng * 64u + (uint32_t)nb * 8u;
+}
+
+// mma.m16n8k16 with a zero accumulator in.
+__device__ __forceinline__ void mma_bf16_z(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+                 : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// ONE: every problem of the launch has a single token.
+template <bool ONE>
+__global__ void __launch_bounds__(RD_WARPS * 32, 3)
+w4a16_bulk_kernel(const __grid_constant__ SaParams P) {
+    extern __shared__ uint8_t sa_dyn[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sa_dyn) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    int lo = 0, hi = P.count - 1;                                  // last problem with cta_begin <= blockIdx.x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.p[mid].cta_begin <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    const SaProb& pr = P.p[lo];
+    const int n0 = ((int)blockIdx.x - pr.cta_begin) * RD_COLS;
+    const int ngroups = pr.K >> 7;
+    const int nbars = (ngroups + SA_GPB - 1) / SA_GPB;
+    uint8_t* sW = sm;
+    uint8_t* sS = sm + sa_wregion(pr.K);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sS + ngroups * 64);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < nbars; b++) mbar_init(smem_u32(bars + b), 1);
+        fence_barrier_init();
+        prefetch_tmap(&pr.tmW);
+    }
+    __syncthreads();
+    // Programmatic dependent launch: the next kernel may start as SMs free up;
+    // the weight copies go out before waiting for the previous kernel (whose
+    // output may be this kernel's activations).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == 0) {
+        for (int b = lane; b < nbars; b += 32) {
+            const int gs = min(SA_GPB, ngroups - b * SA_GPB);
+            const uint32_t bar = smem_u32(bars + b);
+            mbar_arrive_expect_tx(bar, SA_GPB * 2048u + (uint32_t)gs * 64u);   // a box always lands whole
+            tma_load_2d(smem_u32(sW + (size_t)b * SA_GPB * 2048), &pr.tmW, n0, b * SA_GPB * 16, bar);
+            for (int j = 0; j < gs; j++) {
+                const int grp = b * SA_GPB + j;
+                bulk_g2s(smem_u32(sS + grp * 64), pr.S + (size_t)grp * pr.N + n0, 64u, bar);
+            }
+        }
+    }
+    float acc[2][4];
+#pragma unroll
+    for (int sl = 0; sl < 2; sl++) acc[sl][0] = acc[sl][1] = acc[sl][2] = acc[sl][3] = 0.0f;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const bool live = g < pr.M;                                    // token g of the lane's MMA column
+    const uint16_t* arow = pr.A + (size_t)(live ? g : 0) * pr.K + 8 * t;
+    const uint16_t* srow = pr.A + 16 * g + 4 * t;                   // ONE: slice g of the token's group
+    const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+    uint4 an[4];                                                   // the next group's activations
+    uint2 sn = make_uint2(0u, 0u);
+    if (warp < ngroups) {
+#pragma unroll
+        for (int c = 0; c < 4; c++)
+            an[c] = live ? __ldg(reinterpret_cast<const uint4*>(arow + warp * 128 + 32 * c)) : make_uint4(0u, 0u, 0u, 0u);
+        if (ONE) sn = __ldg(reinterpret_cast<const uint2*>(srow + warp * 128));
+    }
+    bool ok = true;
+    for (int grp = warp; grp < ngroups; grp += RD_WARPS) {
+        uint4 av[4];
+#pragma unroll
+        for (int c = 0; c < 4; c++) av[c] = an[c];
+        const uint2 sv = sn;
+        if (grp + RD_WARPS < ngroups) {
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                an[c] = live ? __ldg(reinterpret_cast<const uint4*>(arow + (grp + RD_WARPS) * 128 + 32 * c))
+                             : make_uint4(0u, 0u, 0u, 0u);
+            if (ONE) sn = __ldg(reinterpret_cast<const uint2*>(srow + (grp + RD_WARPS) * 128));
+        }
+        if (!mbar_wait(smem_u32(bars + grp / SA_GPB), 0, &g_w4a16_err)) { ok = false; break; }
+        float ag[2][4], sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint8_t* wg = sW + (size_t)grp * 2048 + t * 128 + g * 16;     // k-octet row 4c + t, columns 4g..4g+3
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(wg + c * 512);
+            const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int sl = 0; sl < 2; sl++) {                       // MMA rows g, g+8 = columns 4g+2sl, 4g+2sl+1
+                const uint32_t w0 = wq[2 * sl], w1 = wq[2 * sl + 1];
+                const uint32_t x0 = w0 >> 4, x1 = w1 >> 4;
+                const uint32_t f0[4] = {nib_pair_biased<0>(w0, x0), nib_pair_biased<0>(w1, x1),
+                                        nib_pair_biased<1>(w0, x0), nib_pair_biased<1>(w1, x1)};
+                const uint32_t f1[4] = {nib_pair_biased<2>(w0, x0), nib_pair_biased<2>(w1, x1),
+                                        nib_pair_biased<3>(w0, x0), nib_pair_biased<3>(w1, x1)};
+                if (c == 0) mma_bf16_z(ag[sl], f0, av[c].x, av[c].y);
+                else mma_bf16(ag[sl], f0, av[c].x, av[c].y);
+                mma_bf16(ag[sl], f1, av[c].z, av[c].w);
+            }
+            if (!ONE) {                                            // sum(a) of tokens 2t, 2t+1
+                mma_bf16(sg, ones, av[c].x, av[c].y);
+                mma_bf16(sg, ones, av[c].z, av[c].w);
+            }
+        }
+        if (ONE) {                                                 // columns hold 16-deep slices: add them all
+            float sd[4];
+            mma_bf16_z(sd, ones, sv.x, sv.y);
+            float v = sd[0] + sd[1];
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+            sg[0] = v;                                             // token 0 (lanes with t = 0 keep it)
+        }
+        const uint2 sc2 = *reinterpret_cast<const uint2*>(sS + grp * 64 + g * 8);
+        const float sc[4] = {bf16_bits_to_f32(sc2.x & 0xFFFFu), bf16_bits_to_f32(sc2.x >> 16),
+                             bf16_bits_to_f32(sc2.y & 0xFFFFu), bf16_bits_to_f32(sc2.y >> 16)};
+#pragma unroll
+        for (int sl = 0; sl < 2; sl++) {                           // remove the bias, scale, accumulate
+            acc[sl][0] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[0], ag[sl][0]), acc[sl][0]);
+            acc[sl][1] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[1], ag[sl][1]), acc[sl][1]);
+            acc[sl][2] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[0], ag[sl][2]), acc[sl][2]);
+            acc[sl][3] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[1], ag[sl][3]), acc[sl][3]);
+        }
+    }
+    // Every box must have landed before its region is reused for the sums; a
+    // warp that gave up on a wait checks the others with the same bound.
+    if (!ok)
+        for (int b = 0; b < nbars; b++) mbar_wait(smem_u32(bars + b), 0, &g_w4a16_err);
+    __syncthreads();
+    float (*red)[8][RD_COLS + 1] = reinterpret_cast<float (*)[8][RD_COLS + 1]>(sm);
+#pragma unroll
+    for (int sl = 0; sl < 2; sl++) {
+        const int m = 2 * t, col = 4 * g + 2 * sl;
+        red[warp][m][col] = acc[sl][0];
+        red[warp][m + 1][col] = acc[sl][1];
+        red[warp][m][col + 1] = acc[sl][2];
+        red[warp][m + 1][col + 1] = acc[sl][3];
+    }
+    __syncthreads();
+    const int mrows = min(pr.M, 8);
+    for (int i = threadIdx.x; i < mrows * (RD_COLS / 2); i += RD_WARPS * 32) {
+        const int m = i / (RD_COLS / 2), col = 2 * (i % (RD_COLS / 2));
+        float y0 = red[0][m][col], y1 = red[0][m][col + 1];
+#pragma unroll
+        for (int w = 1; w < RD_WARPS; w++) {
+            y0 += red[w][m][col];
+            y1 += red[w][m][col + 1];
+        }
+        const __nv_bfloat162 o = __floats2bfloat162_rn(y0, y1);
+        *reinterpret_cast<__nv_bfloat162*>(pr.Y + (size_t)m * pr.N + n0 + col) = o;
+    }
+}
+
 // ------------------------------------------------ TMA-staged kernel
 
 template <int MT>
@@ -526,6 +723,56 @@ qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st
     return launch_status();
 }
 
+// Bulk-staged launch for up to 8 tokens and K <= SA_KMAX: one CTA per 32
+// columns of every problem, programmatic dependent launch.
+qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+    SaParams P;                                   // the kernel parameter block (copied at launch)
+    int total = 0, kmax = 0, mmax = 0;
+    P.count = count;
+    for (int i = 0; i < count; i++) {
+        const qz_w4a16_problem& q = problems[i];
+        SaProb& p = P.p[i];
+        if (!encode_tmap_2d(&p.tmW, q.qweight, 4, (uint64_t)q.N, (uint64_t)q.K / 8, (uint64_t)q.N * 4, 32,
+                            16 * SA_GPB, false))
+            return QZ_ERR_CUDA;
+        p.A = q.A;
+        p.S = q.scale_bf16;
+        p.Y = q.Y;
+        p.M = q.M; p.N = q.N; p.K = q.K;
+        p.cta_begin = total;
+        total += q.N / RD_COLS;
+        kmax = std::max(kmax, q.K);
+        mmax = std::max(mmax, q.M);
+    }
+    const int smem = (int)sa_smem_bytes(kmax);
+    static int smem_set[64];                       // per device: largest size opted in so far
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
+    if (smem > smem_set[dev]) {
+        if (cudaFuncSetAttribute(w4a16_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(w4a16_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+            return QZ_ERR_CUDA;
+        smem_set[dev] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(total);
+    cfg.blockDim = dim3(RD_WARPS * 32);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = mmax == 1 ? cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<true>, P)
+                                    : cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<false>, P);
+    if (e != cudaSuccess) return QZ_ERR_CUDA;
+    return launch_status();
+}
+
 template <int MT>
 qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
     // One persistent CTA per SM (or per tile, if fewer), ring as deep as fits.
@@ -599,7 +846,16 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     // one tile per SM (capped at the widest tile for M); grouped problems use
     // the widest tile.
     const int mt = choose_mt(mmax);
-    if (mt == 8) {                                // up to 8 tokens: register-direct kernel
+    int kmax = 0;
+    for (int i = 0; i < count; i++) kmax = std::max(kmax, problems[i].K);
+    if (mt == 8 && kmax <= SA_KMAX) {             // up to 8 tokens: bulk-staged kernel
+        for (int i = 0; i < count; i += SA_MAX_PROBLEMS) {
+            const qz_status s = launch_bulk(problems + i, std::min(SA_MAX_PROBLEMS, count - i), st);
+            if (s != QZ_OK) return s;
+        }
+        return QZ_OK;
+    }
+    if (mt == 8) {                                // deeper K: register-direct kernel
         for (int i = 0; i < count; i += RD_MAX_PROBLEMS) {
             const qz_status s = launch_rd<8>(problems + i, std::min(RD_MAX_PROBLEMS, count - i), st);
             if (s != QZ_OK) return s;

@@ -160,3 +160,43 @@ def test_w4a16_grouped_decode_tokens(qz, tokens):
     qz.qz_gemm_w4a16_grouped(probs)
     for (name, y_ref, bound), (_, _, _, Y) in zip(refs, probs):
         check(host(Y), y_ref, bound, f"grouped {name} tokens={tokens}")
+
+
+@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("K,N", [(128, 64), (1152, 192), (2944, 64), (8192, 128), (8320, 64)])
+def test_w4a16_staging_depths(qz, M, K, N):
+    """Up to 8 tokens, K from one 128-deep group to the deepest K staged whole in shared
+    memory (8192), odd group counts (a half-filled last box), and one group deeper
+    (8320, the register-direct kernel)."""
+    qw, sc = quantized_weight(K, N, seed=K + M)
+    A = activations(M, K, seed=K + 7 * M)
+    y_ref, bound = oracle.gemm_w4a16(A, qw, sc)
+    check(run(qz, A, qw, sc), y_ref, bound, f"M={M} K={K} N={N}")
+
+
+def grouped_case(qz, shapes, seed):
+    rng = np.random.default_rng(seed)
+    probs, refs = [], []
+    for i, (M, K, N) in enumerate(shapes):
+        qw, sc = quantized_weight(K, N, seed=seed + i)
+        A = activations(M, K, seed=seed + 3 * i)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        probs.append((dev_bf16(A), torch.from_numpy(qw).cuda(),
+                      torch.from_numpy(sc.view(np.int16)).cuda().view(torch.bfloat16), Y))
+        refs.append(oracle.gemm_w4a16(A, qw, sc))
+    qz.qz_gemm_w4a16_grouped(probs)
+    for i, ((y_ref, bound), (_, _, _, Y)) in enumerate(zip(refs, probs)):
+        check(host(Y), y_ref, bound, f"problem {i} {shapes[i]}")
+
+
+def test_w4a16_grouped_single_token_many_problems(qz):
+    """130 single-token problems of mixed K and N: more than one launch's problem table."""
+    shapes = [(1, 128 * (1 + i % 5), 64 * (1 + i % 3)) for i in range(130)]
+    grouped_case(qz, shapes, seed=40)
+
+
+def test_w4a16_grouped_mixed_tokens_and_depths(qz):
+    """One token next to several in one launch, and a group that holds one K deeper than
+    8192 (the whole group then runs register-direct)."""
+    grouped_case(qz, [(1, 1024, 128), (2, 384, 64), (8, 2048, 192), (1, 128, 64)], seed=50)
+    grouped_case(qz, [(1, 1024, 128), (4, 8320, 64), (1, 256, 64)], seed=60)
