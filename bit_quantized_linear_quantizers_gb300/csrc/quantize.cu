@@ -79,20 +79,20 @@ __device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, ui
     }
 }
 
-// Encode 8 values to E2M1 with scale d.s (correctly rounded quotients);
-// returns 8 nibbles, element j at bits 4j..4j+3; writes dequant if asked.
-// Warp-collective (the tie screen votes): all 32 lanes call it together.
-__device__ __forceinline__ uint32_t fp4_encode8(const float v[8], const Recip& d, float* deq) {
-    float y[8];
+// Encode one 16-element block to E2M1 with scale d.s (correctly rounded
+// quotients, ties to the smaller magnitude); returns the 16 nibbles (element j
+// at bit 4j of word j / 8); writes the dequantized block if asked.
+__device__ __forceinline__ uint2 fp4_encode16(const float v[16], const Recip& d, float* deq) {
+    float y[16];
 #pragma unroll
-    for (int j = 0; j < 8; j++) y[j] = div1(v[j], d);
-    const uint32_t packed = e2m1x8_screened(y);     // quotients by an arbitrary scale: ties are rare
+    for (int j = 0; j < 16; j++) y[j] = div1(v[j], d);
+    const uint2 packed = make_uint2(e2m1x8_tiesdown(y), e2m1x8_tiesdown(y + 8));
     if (deq) {
-        float o[8];
+        float o[16];
 #pragma unroll
-        for (int j = 0; j < 8; j++) o[j] = __fmul_rn(e2m1_value(packed >> (4 * j)), d.s);
-        reinterpret_cast<float4*>(deq)[0] = make_float4(o[0], o[1], o[2], o[3]);
-        reinterpret_cast<float4*>(deq)[1] = make_float4(o[4], o[5], o[6], o[7]);
+        for (int j = 0; j < 16; j++) o[j] = __fmul_rn(e2m1_value((j < 8 ? packed.x : packed.y) >> (4 * (j & 7))), d.s);
+#pragma unroll
+        for (int q = 0; q < 4; q++) reinterpret_cast<float4*>(deq)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
     }
     return packed;
 }
@@ -448,7 +448,7 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
                     }
                     packed = e2m1x8_rne(yd);
                 } else {
-                    packed = e2m1x8_fix(e2m1x8_rne(y), y);
+                    packed = e2m1x8_tiesdown(y);
                 }
                 reinterpret_cast<uint32_t*>(codes)[i] = packed;
                 if (deq) {
@@ -466,52 +466,47 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
 
 // ------------------------------------------------------------------ NVFP4
 
-// 2 threads per 16-element block. g comes from the per-tensor partials (or
-// a given amax); the block scale is E4M3(amax16 / 6 / g).
-template <typename T>
+// One thread per 16-element block. g comes from the per-tensor partials (or
+// a given amax); the block scale is E4M3(amax16 / 6 / g). A tensor has at most
+// 128 block scales s = max(E4M3 value, 1e-12) * g, one per code: each CTA
+// tabulates s and RN(1/s) once, so a block pays one table read instead of a
+// correctly rounded reciprocal. I: the block index type (32 bits when the
+// tensor allows).
+template <typename T, typename I>
 __global__ void __launch_bounds__(kThreads)
 nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, bool contig,
              const float* __restrict__ partial, int nparts, const float* __restrict__ amax_in,
              uint8_t* __restrict__ codes, uint8_t* __restrict__ sb, float* __restrict__ g_out,
              float* __restrict__ deq) {
     __shared__ float red[kWarps];
+    __shared__ float tab_s[128], tab_r[128];
     const float amax_t = partial ? reduce_partials(partial, nparts, red) : __ldg(amax_in);
     const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    if (threadIdx.x < 128) {
+        const float sv = __fmul_rn(fmaxf(e4m3_value(threadIdx.x), kAmaxMin), g);
+        tab_s[threadIdx.x] = sv;
+        tab_r[threadIdx.x] = __frcp_rn(sv);
+    }
+    __syncthreads();
     const Recip dg(g), d6(kFp4Max);
-    const int lane = threadIdx.x & 31;
-    const int64_t cpr = cols / 8;
-    const int64_t total = rows * cpr;
-    const int64_t wbase = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * (32 * UQ);
-    const int64_t wstride = (int64_t)gridDim.x * kThreads * UQ;
-    for (int64_t base = wbase; base < total; base += wstride) {
-        float v[UQ][8];
+    const I bpr = (I)(cols / 16);
+    const I total = (I)rows * bpr;
+    const I stride = (I)gridDim.x * kThreads;
+    for (I i = (I)blockIdx.x * kThreads + threadIdx.x; i < total; i += stride) {
+        const T* p = x + (contig ? (int64_t)i * 16 : (int64_t)(i / bpr) * ldx + (int64_t)(i % bpr) * 16);
+        float v[16];
+        Load8<T>::run(p, v);
+        Load8<T>::run(p + 8, v + 8);
+        float m = 0.0f;
 #pragma unroll
-        for (int u = 0; u < UQ; u++) {
-            const int64_t i = base + u * 32 + lane;
-            if (i < total) Load8<T>::run(x + chunk_offset<true>(i, contig, cpr, ldx), v[u]);
-            else for (int j = 0; j < 8; j++) v[u][j] = 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < UQ; u++) {
-            const int64_t i = base + u * 32 + lane;
-            float m = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
-            m = warp_max(m, 2);
-            // t = (amax16 / 6) / g, both quotients correctly rounded
-            const float t = div1(div1(m, d6), dg);
-            const uint32_t bcode = e4m3_code(t);                 // saturating, as the clamp-free page
-            const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
-            // every lane encodes (the tie screen votes across the warp); lanes
-            // past the end hold zeros and store nothing
-            const bool live = i < total;
-            const uint32_t packed = fp4_encode8(v[u], Recip(s), (deq && live) ? deq + i * 8 : nullptr);
-            if (live) {
-                reinterpret_cast<uint32_t*>(codes)[i] = packed;
-                if ((lane & 1) == 0) sb[i >> 1] = (uint8_t)bcode;
-            }
-        }
+        for (int j = 0; j < 16; j++) m = fmaxf(m, fabsf(v[j]));
+        // t = (amax16 / 6) / g, both quotients correctly rounded
+        const float t = div1(div1(m, d6), dg);
+        const uint32_t bcode = e4m3_code(t);                     // saturating, as the clamp-free page
+        const uint2 packed = fp4_encode16(v, Recip(tab_s[bcode], tab_r[bcode]), deq ? deq + (int64_t)i * 16 : nullptr);
+        reinterpret_cast<uint2*>(codes)[i] = packed;
+        sb[i] = (uint8_t)bcode;
     }
 }
 
@@ -520,8 +515,9 @@ nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
 // A decode step's activations (one small tensor per linear) quantized in two
 // launches instead of two per tensor: kernel 1 reduces each tensor's amax in
 // NV_SLICES partial maxima (one CTA per slice), kernel 2 walks the
-// concatenation of all tensors' 8-element chunks; each chunk looks up its
-// tensor, reduces that tensor's partials to g and encodes as nvfp4_kernel does.
+// concatenation of all tensors' 16-element blocks, one per thread; each block
+// looks up its tensor, reduces that tensor's partials to g and encodes as
+// nvfp4_kernel does.
 constexpr int NV_GROUP_MAX = 256;
 constexpr int NV_SLICES = 4;
 
@@ -571,42 +567,35 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 nvfp4_group_encode_kernel(const __grid_constant__ NvGroup P, const float* __restrict__ partial) {
     pdl_wait();
-    const int lane = threadIdx.x & 31;
     const Recip d6(kFp4Max);
-    const long long wbase = (((long long)blockIdx.x * kThreads + threadIdx.x) >> 5) * 32;
-    const long long wstride = (long long)gridDim.x * kThreads;
-    for (long long base = wbase; base < P.total_chunks; base += wstride) {   // warp-uniform
-        const long long i = base + lane;
-        const bool live = i < P.total_chunks;
-        int lo = 0, hi = P.count - 1;                    // tensor of chunk i (tensors hold even chunk counts)
-        const long long ic = live ? i : P.total_chunks - 1;
+    const long long total = P.total_chunks / 2;              // 16-element blocks (every tensor holds whole ones)
+    for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < total; i += (long long)gridDim.x * kThreads) {
+        const long long c = 2 * i;                            // first chunk of block i
+        int lo = 0, hi = P.count - 1;                        // tensor of block i
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (P.t[mid].chunk_begin <= ic) lo = mid; else hi = mid - 1;
+            if (P.t[mid].chunk_begin <= c) lo = mid; else hi = mid - 1;
         }
         const NvTensor& tn = P.t[lo];
-        const long long li = ic - tn.chunk_begin;
+        const long long li = (c - tn.chunk_begin) >> 1;      // block within the tensor
         float amax_t = 0.0f;
 #pragma unroll
         for (int k = 0; k < NV_SLICES; k++) amax_t = fmaxf(amax_t, __ldg(partial + lo * NV_SLICES + k));
         const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
-        if (live && li == 0) *tn.g = g;
+        if (li == 0) *tn.g = g;
         const Recip dg(g);
-        float v[8];
-        if (live) Load8<T>::run(static_cast<const T*>(tn.x) + li * 8, v);
-        else for (int j = 0; j < 8; j++) v[j] = 0.0f;
+        float v[16];
+        const T* p = static_cast<const T*>(tn.x) + li * 16;
+        Load8<T>::run(p, v);
+        Load8<T>::run(p + 8, v + 8);
         float m = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
-        m = warp_max(m, 2);                               // the other half of the 16-element block
+        for (int j = 0; j < 16; j++) m = fmaxf(m, fabsf(v[j]));
         const float t = div1(div1(m, d6), dg);
         const uint32_t bcode = e4m3_code(t);
-        const float s = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
-        const uint32_t packed = fp4_encode8(v, Recip(s), nullptr);   // all 32 lanes (warp vote)
-        if (live) {
-            reinterpret_cast<uint32_t*>(tn.codes)[li] = packed;
-            if ((li & 1) == 0) tn.sb[li >> 1] = (uint8_t)bcode;
-        }
+        const float sv = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
+        reinterpret_cast<uint2*>(tn.codes)[li] = fp4_encode16(v, Recip(sv), nullptr);
+        tn.sb[li] = (uint8_t)bcode;
     }
 }
 
@@ -784,23 +773,37 @@ qz_status quantize_mxfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_
     return launch_status();
 }
 
+template <typename T, typename I>
+void launch_nvfp4_encode(const T* x, int64_t rows, int64_t cols, int64_t ldx, bool contig, const float* partial,
+                         int np, const float* amax_in, uint8_t* codes, uint8_t* sb, float* g, float* deq,
+                         cudaStream_t st) {
+    const int grid = stream_grid(rows * cols / 16, kEncoderCtasPerSm);
+    launch_dependent(nvfp4_kernel<T, I>, dim3(grid), dim3(kThreads), st, x, rows, cols, ldx, contig, partial, np,
+                     amax_in, codes, sb, g, deq);
+}
+
+template <typename T>
+void launch_nvfp4(const T* x, int64_t rows, int64_t cols, int64_t ldx, bool contig, float* partial,
+                  const float* amax_in, uint8_t* codes, uint8_t* sb, float* g, float* deq, cudaStream_t st) {
+    const int np = amax_grid();
+    if (partial) launch_tensor_amax<T, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
+    const int64_t blocks = rows * cols / 16;
+    // 32-bit block indices while the last grid-stride step cannot overflow them
+    if (blocks + (int64_t)stream_grid(blocks, kEncoderCtasPerSm) * kThreads < ((int64_t)1 << 31))
+        launch_nvfp4_encode<T, int>(x, rows, cols, ldx, contig, partial, np, amax_in, codes, sb, g, deq, st);
+    else
+        launch_nvfp4_encode<T, int64_t>(x, rows, cols, ldx, contig, partial, np, amax_in, codes, sb, g, deq, st);
+}
+
 qz_status quantize_nvfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
                                 uint8_t* codes, uint8_t* sb, float* g, const float* amax_in,
                                 float* deq, void* ws, size_t, cudaStream_t st) {
     const bool contig = (ldx == cols);
     float* partial = amax_in ? nullptr : (float*)ws;
-    const int np = amax_grid();
-    const int grid = stream_grid(rows * cols / 8, kEncoderCtasPerSm);
-    const float* cpart = partial;
-    if (xt == QZ_F32) {
-        if (partial) launch_tensor_amax<float, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-        launch_dependent(nvfp4_kernel<float>, dim3(grid), dim3(kThreads), st, (const float*)x, rows, cols, ldx,
-                         contig, cpart, np, amax_in, codes, sb, g, deq);
-    } else {
-        if (partial) launch_tensor_amax<uint16_t, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
-        launch_dependent(nvfp4_kernel<uint16_t>, dim3(grid), dim3(kThreads), st, (const uint16_t*)x, rows, cols,
-                         ldx, contig, cpart, np, amax_in, codes, sb, g, deq);
-    }
+    if (xt == QZ_F32)
+        launch_nvfp4<float>((const float*)x, rows, cols, ldx, contig, partial, amax_in, codes, sb, g, deq, st);
+    else
+        launch_nvfp4<uint16_t>((const uint16_t*)x, rows, cols, ldx, contig, partial, amax_in, codes, sb, g, deq, st);
     return launch_status();
 }
 
@@ -824,7 +827,7 @@ qz_status quantize_nvfp4_grouped_launch(const qz_nvfp4_tensor* tensors, int coun
     }
     P.total_chunks = total;
     float* partial = static_cast<float*>(ws);
-    const int grid = stream_grid(total, kEncoderCtasPerSm);
+    const int grid = stream_grid(total / 2, kEncoderCtasPerSm);
     if (xt == QZ_F32) {
         nvfp4_group_amax_kernel<float><<<count * NV_SLICES, kThreads, 0, st>>>(P, partial);
         launch_dependent(nvfp4_group_encode_kernel<float>, dim3(grid), dim3(kThreads), st, P, (const float*)partial);

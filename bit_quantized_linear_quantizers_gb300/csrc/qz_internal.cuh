@@ -77,6 +77,7 @@ struct Recip {
         s = s_;
         r = __frcp_rn(s_);                     // correctly rounded reciprocal
     }
+    __device__ __forceinline__ Recip(float s_, float r_) : s(s_), r(r_) {}   // r_ == RN(1 / s_)
 };
 
 // One correctly rounded quotient x / d.s (Markstein's correction step), x >= 0.
@@ -105,34 +106,38 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float y[8]) {
     return w;
 }
 
-// The pages' rule (first index of the minimum distance) differs from round to
-// nearest even only at exact midpoints, and only where round-to-even goes up:
-// 0.75, 1.75 and 3.5 (0.25, 1.25, 2.5 and 5 already round down to an even
-// code). Each such element steps down by one (its code is 2, 4 or 6, so the
-// nibble never borrows). The sign bit is (y < 0): an exact -0.0 encodes as +0.
-__device__ __forceinline__ uint32_t e2m1x8_fix(uint32_t w, const float y[8]) {
+// The pages' rule (first index of the minimum distance: ties go to the smaller
+// magnitude) differs from round to nearest even only at exact midpoints, and
+// only where round-to-even goes up: 0.75, 1.75 and 3.5 (0.25, 1.25, 2.5 and 5
+// already round down to an even code); its sign bit is (y < 0), so an exact
+// -0.0 encodes as +0. Both corrections come from a second round-to-nearest-even
+// conversion, of p = pred(y) = RN(y - y * 2^-24) (one fma: the exact difference
+// lies more than half an ulp below y and less than one, or exactly on pred(y)
+// for a power of two; pred(-0) is +0). The two codes differ only beside a
+// midpoint m: at y == m where round-to-even went up (the even code is wrong and
+// p rounds down), and at y == succ(m) where round-to-even of m goes down (p == m
+// rounds down wrongly and the odd code is right). Adjacent codes alternate in
+// parity, so the odd code of a differing pair is the right one, and elsewhere
+// the codes agree. Element j lands in bits 4j..4j+3.
+__device__ __forceinline__ uint32_t e2m1x8_tiesdown(const float y[8]) {
+    float p[8];
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const uint32_t u = __float_as_uint(y[j]);
-        const uint32_t a = u & 0x7FFFFFFFu;
-        if ((a == 0x3F400000u) | (a == 0x3FE00000u) | (a == 0x40600000u)) w -= 1u << (4 * j);
-        if (u == 0x80000000u) w -= 8u << (4 * j);
+    for (int j = 0; j < 8; j++) p[j] = __fmaf_rn(y[j], -0x1.0p-24f, y[j]);
+    uint32_t b1[4], b2[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        uint16_t r1, r2;
+        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
+            : "=h"(r1) : "f"(y[2 * j + 1]), "f"(y[2 * j]));
+        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
+            : "=h"(r2) : "f"(p[2 * j + 1]), "f"(p[2 * j]));
+        b1[j] = r1;
+        b2[j] = r2;
     }
-    return w;
-}
-
-
-// Same result for quotients whose exact midpoints are rare (a division by an
-// arbitrary scale): midpoints carry at most two mantissa bits, so the exact fix
-// runs only when some lane of the warp holds a quotient with zero low mantissa
-// bits. All 32 lanes must call it together.
-__device__ __forceinline__ uint32_t e2m1x8_screened(const float y[8]) {
-    uint32_t w = e2m1x8_rne(y);
-    bool cand = false;
-#pragma unroll
-    for (int j = 0; j < 8; j++) cand |= (__float_as_uint(y[j]) & 0x1FFFFFu) == 0u;
-    if (__any_sync(0xffffffffu, cand)) w = e2m1x8_fix(w, y);
-    return w;
+    const uint32_t w1 = __byte_perm(__byte_perm(b1[0], b1[1], 0x0040), __byte_perm(b1[2], b1[3], 0x0040), 0x5410);
+    const uint32_t w2 = __byte_perm(__byte_perm(b2[0], b2[1], 0x0040), __byte_perm(b2[2], b2[3], 0x0040), 0x5410);
+    const uint32_t odd = (w1 & 0x11111111u) * 15u;               // nibbles of w1 with an odd code, all ones
+    return w2 ^ ((w1 ^ w2) & odd);
 }
 
 // Two fp32 -> two E4M3 bytes, round to nearest even, saturating to +-448
