@@ -129,7 +129,22 @@ amax_partial_kernel(const T* __restrict__ x0, const T* __restrict__ x1, int64_t 
     float m = 0.0f;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; i0 < total; i0 += U * stride) {
-        if constexpr (VEC) {
+        if constexpr (VEC && sizeof(T) == 2) {               // bf16: raw words in flight, widened at use
+            uint4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t i = i0 + u * stride;
+                r[u] = i < total ? __ldg(reinterpret_cast<const uint4*>(x + chunk_offset<true>(i, contig, cpr, ldx)))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+            }
+        } else if constexpr (VEC) {
             float v[U][8];
 #pragma unroll
             for (int u = 0; u < U; u++) {
@@ -688,6 +703,7 @@ int stream_grid(int64_t threads_needed, int per_sm = 4) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm));
 }
 constexpr int kEncoderCtasPerSm = 16;
+constexpr int kNvfp4CtasPerSm = 8;       // the NVFP4 encoder's CTAs also build a scale table
 
 bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
     const size_t es = t == QZ_F32 ? 4 : 2;
@@ -777,7 +793,7 @@ template <typename T, typename I>
 void launch_nvfp4_encode(const T* x, int64_t rows, int64_t cols, int64_t ldx, bool contig, const float* partial,
                          int np, const float* amax_in, uint8_t* codes, uint8_t* sb, float* g, float* deq,
                          cudaStream_t st) {
-    const int grid = stream_grid(rows * cols / 16, kEncoderCtasPerSm);
+    const int grid = stream_grid(rows * cols / 16, kNvfp4CtasPerSm);
     launch_dependent(nvfp4_kernel<T, I>, dim3(grid), dim3(kThreads), st, x, rows, cols, ldx, contig, partial, np,
                      amax_in, codes, sb, g, deq);
 }
@@ -789,7 +805,7 @@ void launch_nvfp4(const T* x, int64_t rows, int64_t cols, int64_t ldx, bool cont
     if (partial) launch_tensor_amax<T, true>(x, x, 1, rows, cols, ldx, contig, partial, st);
     const int64_t blocks = rows * cols / 16;
     // 32-bit block indices while the last grid-stride step cannot overflow them
-    if (blocks + (int64_t)stream_grid(blocks, kEncoderCtasPerSm) * kThreads < ((int64_t)1 << 31))
+    if (blocks + (int64_t)stream_grid(blocks, kNvfp4CtasPerSm) * kThreads < ((int64_t)1 << 31))
         launch_nvfp4_encode<T, int>(x, rows, cols, ldx, contig, partial, np, amax_in, codes, sb, g, deq, st);
     else
         launch_nvfp4_encode<T, int64_t>(x, rows, cols, ldx, contig, partial, np, amax_in, codes, sb, g, deq, st);

@@ -93,16 +93,18 @@ __device__ __forceinline__ float sign_of(float y, float x) {
 }
 
 // Eight E2M1 codes (element j in bits 4j..4j+3) of quotients y[8], by the
-// hardware conversion: round to nearest even, saturating at 6.
+// hardware conversion: round to nearest even, saturating at 6. The four code
+// bytes are assembled inside one asm block (no widening or byte shuffles).
 __device__ __forceinline__ uint32_t e2m1x8_rne(const float y[8]) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-        uint16_t b;
-        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
-            : "=h"(b) : "f"(y[j + 1]), "f"(y[j]));
-        w |= (uint32_t)(b & 0xFF) << (4 * j);
-    }
+    uint32_t w;
+    asm("{ .reg .b8 a, b, c, d;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 a, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 d, %8, %7;\n\t"
+        "mov.b32 %0, {a, b, c, d}; }"
+        : "=r"(w)
+        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
     return w;
 }
 
@@ -123,19 +125,7 @@ __device__ __forceinline__ uint32_t e2m1x8_tiesdown(const float y[8]) {
     float p[8];
 #pragma unroll
     for (int j = 0; j < 8; j++) p[j] = __fmaf_rn(y[j], -0x1.0p-24f, y[j]);
-    uint32_t b1[4], b2[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        uint16_t r1, r2;
-        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
-            : "=h"(r1) : "f"(y[2 * j + 1]), "f"(y[2 * j]));
-        asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }"
-            : "=h"(r2) : "f"(p[2 * j + 1]), "f"(p[2 * j]));
-        b1[j] = r1;
-        b2[j] = r2;
-    }
-    const uint32_t w1 = __byte_perm(__byte_perm(b1[0], b1[1], 0x0040), __byte_perm(b1[2], b1[3], 0x0040), 0x5410);
-    const uint32_t w2 = __byte_perm(__byte_perm(b2[0], b2[1], 0x0040), __byte_perm(b2[2], b2[3], 0x0040), 0x5410);
+    const uint32_t w1 = e2m1x8_rne(y), w2 = e2m1x8_rne(p);
     const uint32_t odd = (w1 & 0x11111111u) * 15u;               // nibbles of w1 with an odd code, all ones
     return w2 ^ ((w1 ^ w2) & odd);
 }
