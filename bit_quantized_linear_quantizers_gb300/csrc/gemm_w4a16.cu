@@ -411,7 +411,7 @@ w4a16_bulk_kernel(const __grid_constant__ SaParams P) {
                              : make_uint4(0u, 0u, 0u, 0u);
             if (ONE) sn = __ldg(reinterpret_cast<const uint2*>(srow + (grp + RD_WARPS) * 128));
         }
-        if (!mbar_wait(smem_u32(bars + grp / SA_GPB), 0, &g_w4a16_err)) { ok = false; break; }
+        if (!mbar_wait<false>(smem_u32(bars + grp / SA_GPB), 0, &g_w4a16_err)) { ok = false; break; }
         float ag[2][4], sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         const uint8_t* wg = sW + (size_t)grp * 2048 + t * 128 + g * 16;     // k-octet row 4c + t, columns 4g..4g+3
 #pragma unroll
@@ -457,7 +457,7 @@ w4a16_bulk_kernel(const __grid_constant__ SaParams P) {
     // Every box must have landed before its region is reused for the sums; a
     // warp that gave up on a wait checks the others with the same bound.
     if (!ok)
-        for (int b = 0; b < nbars; b++) mbar_wait(smem_u32(bars + b), 0, &g_w4a16_err);
+        for (int b = 0; b < nbars; b++) mbar_wait<false>(smem_u32(bars + b), 0, &g_w4a16_err);
     __syncthreads();
     float (*red)[8][RD_COLS + 1] = reinterpret_cast<float (*)[8][RD_COLS + 1]>(sm);
 #pragma unroll
