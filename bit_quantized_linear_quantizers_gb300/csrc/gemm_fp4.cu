@@ -259,16 +259,16 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
             const float gscale = NV ? __ldg(pr.gA) * __ldg(pr.gB) : 1.0f;
             if (!mbar_wait(tfull, tcount & 1, &g_fp4_err)) break;
             tc_fence_after();
-            float acc[128];
+            uint32_t v[4][32];                           // all four loads in flight, one wait
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + h * 128;
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t v[32];
-                tmem_ld32(taddr + c * 32, v);
-                tmem_wait_ld();
+            for (int c = 0; c < 4; c++) tmem_ld32(taddr + c * 32, v[c]);
+            tmem_wait_ld();
+            float acc[128];
 #pragma unroll
-                for (int i = 0; i < 32; i++) acc[c * 32 + i] = __uint_as_float(v[i]);
-            }
+            for (int c = 0; c < 4; c++)
+#pragma unroll
+                for (int i = 0; i < 32; i++) acc[c * 32 + i] = __uint_as_float(v[c][i]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
