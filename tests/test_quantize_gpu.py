@@ -164,6 +164,27 @@ def test_fp4_midpoints_and_zero_signs(qz):
     check_nv(qz, x, "nv midpoints")
 
 
+def test_fp4_ulp_above_midpoints(qz):
+    """Quotients exactly on each E2M1 midpoint and one fp32 ulp above it, with unit scales
+    (NVFP4: given tensor amax 2688 -> g = 1, block amax 6 -> block scale 1; MXFP4: block amax
+    6 -> scale 2^0), so y = x: ties go down, one ulp above a midpoint goes up."""
+    mids = np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    above = np.nextafter(mids, np.float32(np.inf), dtype=np.float32)
+    below = np.nextafter(mids, np.float32(0), dtype=np.float32)
+    vals = np.concatenate([mids, above, below, -mids, -above])          # 35 values
+    x = np.zeros((3, 32), np.float32)
+    flat = np.concatenate([vals, np.float32([0.0, -0.0, 6.0, -6.0, 3.0, 1e-30, -1e-30])])
+    for r in range(3):
+        row = flat[r * 14:(r + 1) * 14] if r < 2 else flat[28:]
+        x[r, 0] = 6.0                                                   # each 16- and 32-block's max
+        x[r, 16] = 6.0
+        x[r, 1:1 + min(15, len(row))] = row[:15]
+        x[r, 17:17 + max(0, min(15, len(row) - 15))] = row[15:30]
+    check_nv(qz, x, "nv ulp above midpoints", amax_in=2688.0)
+    check_mx(qz, x, "mx ulp above midpoints")
+    check_nv(qz, syn.to_bf16_bits(x), "nv bf16 midpoints", amax_in=2688.0)
+
+
 def test_nvfp4_given_amax(qz):
     x = edge_tensor(64, 256, seed=8)
     check_nv(qz, x, "nv given amax", amax_in=float(np.abs(x).max()) * 2.0)
