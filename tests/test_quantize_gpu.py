@@ -312,6 +312,71 @@ def test_kv_write_config5_full(qz):
     assert_same_bytes(host(vc), rvc, "v codes")
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 1, 8), (1, 3, 100, 8), (2, 8, 1000, 64), (1, 8, 8192, 128)])
+def test_kv_write_shapes(qz, shape):
+    """Slices that leave some CTAs empty, a single 16-byte word, and a size past the
+    one-launch limit (the two-launch path)."""
+    B, H, T, D = shape
+    rng = np.random.default_rng(T + D)
+    k = syn.to_bf16_bits((rng.standard_normal(shape) * 3).astype(np.float32))
+    v = syn.to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    kc, vc, ks, vs = qz.qz_kv_write_fp8(dev_bf16(k), dev_bf16(v))
+    rkc, rvc, rks, rvs, _, _ = oracle.kv_write_fp8(k, v)
+    assert_same_bytes(host(ks), np.float32([rks]), "k scale")
+    assert_same_bytes(host(vs), np.float32([rvs]), "v scale")
+    assert_same_bytes(host(kc).ravel(), rkc.ravel(), "k codes")
+    assert_same_bytes(host(vc).ravel(), rvc.ravel(), "v codes")
+
+
+def test_kv_write_workspace_reuse_and_graph_replay(qz):
+    """One workspace across calls with different data, then a captured call replayed
+    on new data: each result must be that data's own (no stale meeting records)."""
+    shape = (1, 8, 512, 128)
+    ws = qz.Workspace()
+    kd = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    kc = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    vc = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    ks = torch.empty(1, dtype=torch.float32, device="cuda")
+    vs = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def data(seed):
+        rng = np.random.default_rng(seed)
+        scale = 1.0 + seed
+        return (syn.to_bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32)),
+                syn.to_bf16_bits((rng.standard_normal(shape) * 0.5 * scale).astype(np.float32)))
+
+    def check(k, v, what):
+        torch.cuda.synchronize()
+        rkc, rvc, rks, rvs, _, _ = oracle.kv_write_fp8(k, v)
+        assert_same_bytes(host(ks), np.float32([rks]), f"{what} k scale")
+        assert_same_bytes(host(vs), np.float32([rvs]), f"{what} v scale")
+        assert_same_bytes(host(kc).ravel(), rkc.ravel(), f"{what} k codes")
+        assert_same_bytes(host(vc).ravel(), rvc.ravel(), f"{what} v codes")
+
+    def load(k, v):
+        kd.copy_(dev_bf16(k))
+        vd.copy_(dev_bf16(v))
+
+    for seed in range(3):
+        k, v = data(seed)
+        load(k, v)
+        qz.qz_kv_write_fp8(kd, vd, k_codes=kc, v_codes=vc, k_scale=ks, v_scale=vs, ws=ws)
+        check(k, v, f"call {seed}")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        qz.qz_kv_write_fp8(kd, vd, k_codes=kc, v_codes=vc, k_scale=ks, v_scale=vs, ws=ws, stream=s)
+    for seed in range(3, 6):
+        k, v = data(seed)
+        load(k, v)
+        torch.cuda.synchronize()
+        g.replay()
+        check(k, v, f"replay {seed}")
+    assert qz.qz_device_error() == 0
+
+
 def test_kv_write_given_scale(qz):
     k, v = syn.kv_cache_inputs(seed=1, T=64)
     ks = torch.tensor([0.05], dtype=torch.float32, device="cuda")
