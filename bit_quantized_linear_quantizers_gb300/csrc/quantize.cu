@@ -869,7 +869,10 @@ qz_status kv_write_launch(const uint16_t* k, const uint16_t* v, int64_t n, uint8
                           float* ks, float* vs, qz_scale_mode mode, void* ws, size_t, cudaStream_t st) {
     const int np = amax_grid();
     float* partial = (mode == QZ_SCALE_COMPUTE) ? (float*)ws : nullptr;
-    const dim3 grid(stream_grid(n / 8), 2);
+    // 3 encoder CTAs per SM and tensor: every CTA first reduces all partials,
+    // so fewer, longer-lived CTAs measured faster (9.4 us at 4M elements per
+    // tensor, against 10.8 with 4 per SM and 14.0 with 16)
+    const dim3 grid(stream_grid(n / 8, 3), 2);
     if (partial) {
         const float* none = nullptr;
         float* nod = nullptr;
