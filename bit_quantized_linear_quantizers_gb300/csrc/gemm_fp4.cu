@@ -76,22 +76,19 @@ struct RelayParams {
     long long total_words;
 };
 
-__global__ void sf_relayout_kernel(const __grid_constant__ RelayParams P) {
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < P.total_words;
-         i += (long long)gridDim.x * blockDim.x) {
-        int lo = 0, hi = P.count - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (P.j[mid].word_begin <= i) lo = mid; else hi = mid - 1;
-        }
-        const RelayJob& jb = P.j[lo];
-        const long long w = i - jb.word_begin;
-        const long long a = w >> 7;
-        const int p = (int)(w & 127);
-        const long long rb = a / (jb.KS / 4), kg = a % (jb.KS / 4);
-        const long long m = rb * 128 + (p >> 2) + 32 * (p & 3);
-        const uint32_t v = m < jb.R ? __ldg(reinterpret_cast<const uint32_t*>(jb.src + m * jb.KS + kg * 4)) : 0u;
-        reinterpret_cast<uint32_t*>(jb.dst)[w] = v;
+// CTA (x, y) re-lays atoms x, x + gridDim.x, ... of job y; thread p of an atom
+// writes its word p (row m = rb*128 + p/4 + 32*(p%4), the four scales of group kg).
+__global__ void __launch_bounds__(128) sf_relayout_kernel(const __grid_constant__ RelayParams P) {
+    const RelayJob& jb = P.j[blockIdx.y];
+    const int kgn = jb.KS / 4;                                // 4-scale groups per row
+    const int atoms = ((jb.R + 127) / 128) * kgn;
+    const int p = threadIdx.x;
+    const int r_in = (p >> 2) + 32 * (p & 3);
+    for (int a = blockIdx.x; a < atoms; a += gridDim.x) {
+        const int rb = a / kgn, kg = a - rb * kgn;
+        const int m = rb * 128 + r_in;
+        const uint32_t v = m < jb.R ? __ldg(reinterpret_cast<const uint32_t*>(jb.src + (size_t)m * jb.KS + kg * 4)) : 0u;
+        reinterpret_cast<uint32_t*>(jb.dst)[(size_t)a * 128 + p] = v;
     }
 }
 
@@ -99,9 +96,10 @@ long long relay_words(int R, int KS) { return (long long)((R + 127) / 128) * (KS
 
 qz_status relayout(const RelayParams& P, cudaStream_t st) {
     if (P.total_words == 0) return QZ_OK;
-    const long long blocks = (P.total_words + 255) / 256;
-    const int grid = (int)std::min<long long>(blocks, (long long)num_sms() * 8);
-    sf_relayout_kernel<<<grid, 256, 0, st>>>(P);
+    int amax = 0;
+    for (int i = 0; i < P.count; i++) amax = std::max(amax, ((P.j[i].R + 127) / 128) * (P.j[i].KS / 4));
+    const int gx = std::max(1, std::min(amax, num_sms() * 16 / P.count + 1));
+    sf_relayout_kernel<<<dim3(gx, P.count), 128, 0, st>>>(P);
     return launch_status();
 }
 
