@@ -387,10 +387,13 @@ qz_status gemm_nvfp4_grouped_launch(const qz_nvfp4_problem* problems, int count,
         R.total_words += relay_words(q.M, q.K / 16);
     }
     QZ_TRY(relayout(R, st));
-    for (int i0 = 0; i0 < count; i0 += FP4_PER_LAUNCH) {
+    // as few launches as the parameter space allows, with equal shares of problems
+    const int launches = (count + FP4_PER_LAUNCH - 1) / FP4_PER_LAUNCH;
+    const int share = (count + launches - 1) / launches;
+    for (int i0 = 0; i0 < count; i0 += share) {
         Fp4Params P;
         int tiles = 0;
-        P.count = std::min(FP4_PER_LAUNCH, count - i0);
+        P.count = std::min(share, count - i0);
         for (int i = 0; i < P.count; i++) {
             const qz_nvfp4_problem& q = problems[i0 + i];
             if (!fill_problem(P.p[i], q.qA, wsb + (size_t)(i0 + i) * slot, q.gA, q.qB, q.sB_prepared, q.gB, q.Y,

@@ -341,10 +341,13 @@ qz_status w4a16_tc_error_read_and_clear() {
 
 // Problems with 17..64 tokens (mt = 32 or 64 padded rows), up to 80 per launch.
 qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st) {
-    for (int i0 = 0; i0 < count; i0 += TC_PER_LAUNCH) {
+    // as few launches as the parameter space allows, with equal shares of problems
+    const int launches = (count + TC_PER_LAUNCH - 1) / TC_PER_LAUNCH;
+    const int share = (count + launches - 1) / launches;
+    for (int i0 = 0; i0 < count; i0 += share) {
         TcParams P;
         int tiles = 0;
-        P.count = std::min(TC_PER_LAUNCH, count - i0);
+        P.count = std::min(share, count - i0);
         for (int i = 0; i < P.count; i++) {
             const qz_w4a16_problem& q = problems[i0 + i];
             TcProb& p = P.p[i];
