@@ -348,8 +348,13 @@ qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, c
         TcParams P;
         int tiles = 0;
         P.count = std::min(share, count - i0);
+        // deepest K first: the CTAs take tiles round-robin, so the long tiles
+        // spread over the SMs and the launch ends on short ones
+        int order[TC_PER_LAUNCH];
+        for (int i = 0; i < P.count; i++) order[i] = i0 + i;
+        std::stable_sort(order, order + P.count, [&](int a, int b) { return problems[a].K > problems[b].K; });
         for (int i = 0; i < P.count; i++) {
-            const qz_w4a16_problem& q = problems[i0 + i];
+            const qz_w4a16_problem& q = problems[order[i]];
             TcProb& p = P.p[i];
             if (!encode_tmap_2d(&p.tmW, q.qweight, 4, (uint64_t)q.N, (uint64_t)q.K / 8, (uint64_t)q.N * 4, TN,
                                 GK / 8, false) ||
