@@ -92,13 +92,14 @@ def _check(status: int, where: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain ints: ctypes converts them for c_void_p parameters (no wrapper object per call)
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _dtype_code(x: torch.Tensor) -> int:
@@ -115,8 +116,17 @@ def _rows_cols_ld(x: torch.Tensor):
     return x.shape[0], x.shape[1], (x.stride(0) if x.shape[0] > 1 else max(x.shape[1], 1))
 
 
+_WS_CACHE = {}
+
+
 def qz_workspace_size(op: int, d0: int, d1: int = 0, d2: int = 0) -> int:
-    return int(lib.qz_workspace_size(op, d0, d1, d2))
+    key = (op, d0, d1, d2)
+    n = _WS_CACHE.get(key)
+    if n is None:
+        n = int(lib.qz_workspace_size(op, d0, d1, d2))
+        if len(_WS_CACHE) < 4096:
+            _WS_CACHE[key] = n
+    return n
 
 
 def qz_status_string(status: int) -> str:
