@@ -846,18 +846,23 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     // one tile per SM (capped at the widest tile for M); grouped problems use
     // the widest tile.
     const int mt = choose_mt(mmax);
+    // as few launches as the parameter space allows (cap per launch), with equal
+    // shares of the problems: every launch pays a ramp and a tail
+    auto share = [count](int cap) { const int n = (count + cap - 1) / cap; return (count + n - 1) / n; };
     int kmax = 0;
     for (int i = 0; i < count; i++) kmax = std::max(kmax, problems[i].K);
     if (mt == 8 && kmax <= SA_KMAX) {             // up to 8 tokens: bulk-staged kernel
-        for (int i = 0; i < count; i += SA_MAX_PROBLEMS) {
-            const qz_status s = launch_bulk(problems + i, std::min(SA_MAX_PROBLEMS, count - i), st);
+        const int sh = share(SA_MAX_PROBLEMS);
+        for (int i = 0; i < count; i += sh) {
+            const qz_status s = launch_bulk(problems + i, std::min(sh, count - i), st);
             if (s != QZ_OK) return s;
         }
         return QZ_OK;
     }
     if (mt == 8) {                                // deeper K: register-direct kernel
-        for (int i = 0; i < count; i += RD_MAX_PROBLEMS) {
-            const qz_status s = launch_rd<8>(problems + i, std::min(RD_MAX_PROBLEMS, count - i), st);
+        const int sh = share(RD_MAX_PROBLEMS);
+        for (int i = 0; i < count; i += sh) {
+            const qz_status s = launch_rd<8>(problems + i, std::min(sh, count - i), st);
             if (s != QZ_OK) return s;
         }
         return QZ_OK;
@@ -868,8 +873,9 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
         const int N = problems[0].N;
         nt = std::min(nt, 32 * (int)((N + 32LL * sms - 1) / (32LL * sms)));
     }
-    for (int i = 0; i < count; i += PER_LAUNCH) {
-        const qz_status s = launch_chunk(problems + i, std::min(PER_LAUNCH, count - i), nt, mt, st);
+    const int sh = share(PER_LAUNCH);
+    for (int i = 0; i < count; i += sh) {
+        const qz_status s = launch_chunk(problems + i, std::min(sh, count - i), nt, mt, st);
         if (s != QZ_OK) return s;
     }
     return QZ_OK;
