@@ -200,3 +200,10 @@ def test_w4a16_grouped_mixed_tokens_and_depths(qz):
     8192 (the whole group then runs register-direct)."""
     grouped_case(qz, [(1, 1024, 128), (2, 384, 64), (8, 2048, 192), (1, 128, 64)], seed=50)
     grouped_case(qz, [(1, 1024, 128), (4, 8320, 64), (1, 256, 64)], seed=60)
+
+
+def test_w4a16_grouped_split_into_shares(qz):
+    """Groups larger than one launch's problem table at 9-16 tokens (70 problems: two
+    launches of 35) and at 17-64 tokens (90 problems: two launches of 45)."""
+    grouped_case(qz, [(12, 128 * (1 + i % 4), 64 * (1 + i % 3)) for i in range(70)], seed=70)
+    grouped_case(qz, [(40, 128 * (1 + i % 4), 128 * (1 + i % 2)) for i in range(90)], seed=80)
