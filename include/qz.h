@@ -218,9 +218,10 @@ typedef struct qz_w4a16_problem {
  * inputs are all ready) in as few launches as the kernel parameter space
  * allows (per launch: up to 120 problems of at most 8 tokens and K <= 8192,
  * 256 for deeper K, 56 at 9-16 tokens, 80 at 17-64), split into equal
- * shares. The kernel is chosen by the largest M of the group. Each problem obeys the rules of qz_gemm_w4a16;
- * outputs must not overlap. count <= 256. ws: qz_workspace_size(
- * QZ_OP_GEMM_W4A16, Mmax, sum of N, Kmax) bytes suffices. */
+ * shares. The kernel is chosen by the largest M of the group. Each problem
+ * obeys the rules of qz_gemm_w4a16; outputs must not overlap. count <= 256.
+ * ws: qz_workspace_size(QZ_OP_GEMM_W4A16, Mmax, sum of N, Kmax) bytes
+ * suffices. */
 qz_status qz_gemm_w4a16_grouped(const qz_w4a16_problem* problems, int count,
                                 void* ws, size_t ws_bytes, void* stream);
 
