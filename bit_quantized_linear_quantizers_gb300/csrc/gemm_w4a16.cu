@@ -45,6 +45,7 @@
 
 #include <cuda_bf16.h>
 #include <algorithm>
+#include <mutex>
 
 namespace qz {
 
@@ -746,16 +747,20 @@ qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t 
     }
     const int smem = (int)sa_smem_bytes(kmax);
     static int smem_set[64];                       // per device: largest size opted in so far
+    static std::mutex smem_mu;                     // host threads must not lower each other's opt-in
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    if (smem > smem_set[dev]) {
-        if (cudaFuncSetAttribute(w4a16_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(w4a16_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-                cudaSuccess)
-            return QZ_ERR_CUDA;
-        smem_set[dev] = smem;
+    {
+        std::lock_guard<std::mutex> lock(smem_mu);
+        if (smem > smem_set[dev]) {
+            if (cudaFuncSetAttribute(w4a16_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(w4a16_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                    cudaSuccess)
+                return QZ_ERR_CUDA;
+            smem_set[dev] = smem;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(total);
@@ -782,13 +787,18 @@ qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
     ns = std::max(2, std::min(ns, 8));
     const int smem = (int)L.smem_bytes(ns);
     static int smem_set[64];                       // per device: largest size opted in so far
+    static std::mutex smem_mu;                     // host threads must not lower each other's opt-in
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    if (smem > smem_set[dev]) {
-        if (cudaFuncSetAttribute(w4a16_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return QZ_ERR_CUDA;
-        smem_set[dev] = smem;
+    {
+        std::lock_guard<std::mutex> lock(smem_mu);
+        if (smem > smem_set[dev]) {
+            if (cudaFuncSetAttribute(w4a16_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                    cudaSuccess)
+                return QZ_ERR_CUDA;
+            smem_set[dev] = smem;
+        }
     }
     const int threads = (2 * (nt / 16) + 1) * 32;
     const int grid = std::min(P.total_tiles, num_sms());
