@@ -96,6 +96,37 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _device() -> int:
+    """The current CUDA device: libqz launches there, so every tensor must live there."""
+    return torch.cuda.current_device()
+
+
+def _arg(t, name, dev, kind, numel=None):
+    """Device pointer of a dense tensor on device `dev` whose elements are of dtype `kind`
+    (or, for an int, that many bytes), `numel` of them when given. The C ABI sees only
+    the pointer, so the layout that it assumes is checked here, before any launch."""
+    if (t.get_device() != dev or not t.is_contiguous()
+            or (t.dtype is not kind if isinstance(kind, torch.dtype) else t.element_size() != kind)
+            or (numel is not None and t.numel() != numel)):
+        want = str(kind).replace("torch.", "") if isinstance(kind, torch.dtype) else f"{kind}-byte"
+        where = "cpu" if t.get_device() < 0 else f"cuda:{t.get_device()}"
+        raise ValueError(f"{name}: expected a contiguous {want} tensor on cuda:{dev}"
+                         + ("" if numel is None else f" with {numel} elements")
+                         + f", got {t.dtype} {tuple(t.shape)} on {where}"
+                         + ("" if t.is_contiguous() else ", not contiguous"))
+    return t.data_ptr()
+
+
+def _opt(t, name, dev, kind, numel=None):
+    return None if t is None else _arg(t, name, dev, kind, numel)
+
+
+def _on(x, name, dev):
+    if x.get_device() != dev:
+        where = "cpu" if x.get_device() < 0 else f"cuda:{x.get_device()}"
+        raise ValueError(f"{name}: expected a tensor on cuda:{dev}, got one on {where}")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -152,13 +183,14 @@ class Workspace:
         return self.buf
 
 
-def _ws(ws, nbytes, device):
+def _ws(ws, nbytes, dev):
     if nbytes == 0:
         return None, 0
     if ws is None:
-        ws = Workspace(device)
+        ws = Workspace(torch.device("cuda", dev))
     buf = ws.get(nbytes) if isinstance(ws, Workspace) else ws
-    return buf, buf.numel()
+    _on(buf, "ws", dev)
+    return buf, buf.numel() * buf.element_size()
 
 
 # ------------------------------------------------------------- quantizers
@@ -168,26 +200,35 @@ def qz_quantize_fp8(x: torch.Tensor, gran: int, codes=None, scales=None, dequant
     """FP8 E4M3 quantization of a 2-D fp32/bf16 tensor. Returns (codes u8, scales f32,
     dequant f32 or None). `dequant` may be True (allocate) or an output tensor."""
     rows, cols, ld = _rows_cols_ld(x)
+    xt, d = _dtype_code(x), _device()
+    _on(x, "x", d)
     dev = x.device
+    br = min(128, rows) if rows else 1
+    shape = {FP8_PER_TENSOR: (1,), FP8_PER_ROW: (rows,),
+             FP8_BLOCK_128x128: (rows // br, cols // 128), FP8_GROUP_1x128: (rows, cols // 128)}.get(gran)
+    if shape is None:
+        raise ValueError(f"unknown FP8 granularity {gran}")
     if codes is None:
         codes = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
     if scales is None:
-        br = min(128, rows) if rows else 1
-        shape = {FP8_PER_TENSOR: (1,), FP8_PER_ROW: (rows,),
-                 FP8_BLOCK_128x128: (rows // br, cols // 128), FP8_GROUP_1x128: (rows, cols // 128)}[gran]
         scales = torch.empty(shape, dtype=torch.float32, device=dev)
     if dequant is True:
         dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     deq = dequant if isinstance(dequant, torch.Tensor) else None
-    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_FP8, rows, cols, gran), dev)
-    _check(lib.qz_quantize_fp8(_ptr(x), _dtype_code(x), rows, cols, ld, gran, _ptr(codes), _ptr(scales),
-                               _ptr(deq), _ptr(buf), nb, _stream(stream)), "qz_quantize_fp8")
+    n_sc = shape[0] * (shape[1] if len(shape) > 1 else 1)
+    args = (_arg(codes, "codes", d, 1, rows * cols), _arg(scales, "scales", d, torch.float32, n_sc),
+            _opt(deq, "dequant", d, torch.float32, rows * cols))
+    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_FP8, rows, cols, gran), d)
+    _check(lib.qz_quantize_fp8(x.data_ptr(), xt, rows, cols, ld, gran, *args, _ptr(buf), nb, _stream(stream)),
+           "qz_quantize_fp8")
     return codes, scales, deq
 
 
 def qz_quantize_mxfp4(x: torch.Tensor, codes=None, scale_e8m0=None, dequant=False, stream=None):
     """MXFP4 quantization. Returns (codes u8 [R, C/2], e8m0 u8 [R, C/32], dequant|None)."""
     rows, cols, ld = _rows_cols_ld(x)
+    xt, d = _dtype_code(x), _device()
+    _on(x, "x", d)
     dev = x.device
     if codes is None:
         codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
@@ -196,8 +237,10 @@ def qz_quantize_mxfp4(x: torch.Tensor, codes=None, scale_e8m0=None, dequant=Fals
     if dequant is True:
         dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     deq = dequant if isinstance(dequant, torch.Tensor) else None
-    _check(lib.qz_quantize_mxfp4(_ptr(x), _dtype_code(x), rows, cols, ld, _ptr(codes), _ptr(scale_e8m0),
-                                 _ptr(deq), _stream(stream)), "qz_quantize_mxfp4")
+    _check(lib.qz_quantize_mxfp4(x.data_ptr(), xt, rows, cols, ld, _arg(codes, "codes", d, 1, rows * (cols // 2)),
+                                 _arg(scale_e8m0, "scale_e8m0", d, 1, rows * (cols // 32)),
+                                 _opt(deq, "dequant", d, torch.float32, rows * cols), _stream(stream)),
+           "qz_quantize_mxfp4")
     return codes, scale_e8m0, deq
 
 
@@ -206,6 +249,8 @@ def qz_quantize_nvfp4(x: torch.Tensor, codes=None, scale_e4m3=None, global_scale
     """NVFP4 quantization. Returns (codes u8 [R, C/2], block scales u8 (E4M3) [R, C/16],
     global scale f32 [1], dequant|None)."""
     rows, cols, ld = _rows_cols_ld(x)
+    xt, d = _dtype_code(x), _device()
+    _on(x, "x", d)
     dev = x.device
     if codes is None:
         codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
@@ -216,13 +261,16 @@ def qz_quantize_nvfp4(x: torch.Tensor, codes=None, scale_e4m3=None, global_scale
     if dequant is True:
         dequant = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     deq = dequant if isinstance(dequant, torch.Tensor) else None
+    args = (_arg(codes, "codes", d, 1, rows * (cols // 2)), _arg(scale_e4m3, "scale_e4m3", d, 1, rows * (cols // 16)),
+            _arg(global_scale, "global_scale", d, torch.float32, 1),
+            _opt(global_amax_in, "global_amax_in", d, torch.float32, 1),
+            _opt(deq, "dequant", d, torch.float32, rows * cols))
     if global_amax_in is None:
-        buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4, rows, cols), dev)
+        buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4, rows, cols), d)
     else:
         buf, nb = None, 0
-    _check(lib.qz_quantize_nvfp4(_ptr(x), _dtype_code(x), rows, cols, ld, _ptr(codes), _ptr(scale_e4m3),
-                                 _ptr(global_scale), _ptr(global_amax_in), _ptr(deq), _ptr(buf), nb,
-                                 _stream(stream)), "qz_quantize_nvfp4")
+    _check(lib.qz_quantize_nvfp4(x.data_ptr(), xt, rows, cols, ld, *args, _ptr(buf), nb, _stream(stream)),
+           "qz_quantize_nvfp4")
     return codes, scale_e4m3, global_scale, deq
 
 
@@ -234,11 +282,13 @@ def qz_quantize_nvfp4_grouped(xs, outs=None, ws=None, stream=None):
     arr = (_Nvfp4Tensor * n)()
     res = []
     xt = _dtype_code(xs[0]) if n else F32
+    d = _device()
     for i, x in enumerate(xs):
         if x.dim() != 2 or not x.is_contiguous():
             raise ValueError("qz_quantize_nvfp4_grouped takes contiguous 2-D tensors")
         if _dtype_code(x) != xt:
             raise TypeError("qz_quantize_nvfp4_grouped takes tensors of one dtype")
+        _on(x, f"xs[{i}]", d)
         rows, cols = x.shape
         if outs is not None:
             codes, sc, g = outs[i]
@@ -246,10 +296,11 @@ def qz_quantize_nvfp4_grouped(xs, outs=None, ws=None, stream=None):
             codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
             sc = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
             g = torch.empty((1,), dtype=torch.float32, device=x.device)
-        arr[i] = _Nvfp4Tensor(x.data_ptr(), rows, cols, codes.data_ptr(), sc.data_ptr(), g.data_ptr())
+        arr[i] = _Nvfp4Tensor(x.data_ptr(), rows, cols, _arg(codes, f"codes[{i}]", d, 1, rows * (cols // 2)),
+                              _arg(sc, f"scale_e4m3[{i}]", d, 1, rows * (cols // 16)),
+                              _arg(g, f"global_scale[{i}]", d, torch.float32, 1))
         res.append((codes, sc, g))
-    dev = xs[0].device if n else torch.device("cuda")
-    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4_GROUPED, n) if n else 0, dev)
+    buf, nb = _ws(ws, qz_workspace_size(OP_QUANTIZE_NVFP4_GROUPED, n) if n else 0, d)
     _check(lib.qz_quantize_nvfp4_grouped(arr, n, xt, _ptr(buf), nb, _stream(stream)),
            "qz_quantize_nvfp4_grouped")
     return res
@@ -259,6 +310,8 @@ def qz_quantize_int4_g128(w: torch.Tensor, qweight=None, scale_bf16=None, dequan
     """INT4 g128 of a [K, N] weight. Returns (qweight i32 [K/8, N], scale bf16 [K/128, N],
     dequant|None)."""
     K, N, ld = _rows_cols_ld(w)
+    wt, d = _dtype_code(w), _device()
+    _on(w, "w", d)
     dev = w.device
     if qweight is None:
         qweight = torch.empty((K // 8, N), dtype=torch.int32, device=dev)
@@ -267,8 +320,10 @@ def qz_quantize_int4_g128(w: torch.Tensor, qweight=None, scale_bf16=None, dequan
     if dequant is True:
         dequant = torch.empty((K, N), dtype=torch.float32, device=dev)
     deq = dequant if isinstance(dequant, torch.Tensor) else None
-    _check(lib.qz_quantize_int4_g128(_ptr(w), _dtype_code(w), K, N, ld, _ptr(qweight), _ptr(scale_bf16),
-                                     _ptr(deq), _stream(stream)), "qz_quantize_int4_g128")
+    _check(lib.qz_quantize_int4_g128(w.data_ptr(), wt, K, N, ld, _arg(qweight, "qweight", d, 4, (K // 8) * N),
+                                     _arg(scale_bf16, "scale_bf16", d, 2, (K // 128) * N),
+                                     _opt(deq, "dequant", d, torch.float32, K * N), _stream(stream)),
+           "qz_quantize_int4_g128")
     return qweight, scale_bf16, deq
 
 
@@ -281,6 +336,9 @@ def qz_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, k_codes=None, v_codes=None
     if not (k.is_contiguous() and v.is_contiguous()):
         raise ValueError("k and v must be contiguous")
     B, H, T, D = k.shape
+    d = _device()
+    _on(k, "k", d)
+    _on(v, "v", d)
     dev = k.device
     if k_codes is None:
         k_codes = torch.empty(k.shape, dtype=torch.uint8, device=dev)
@@ -291,9 +349,11 @@ def qz_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, k_codes=None, v_codes=None
     if v_scale is None:
         v_scale = torch.empty((1,), dtype=torch.float32, device=dev)
     n = B * H * T * D
-    buf, nb = _ws(ws, qz_workspace_size(OP_KV_WRITE_FP8, n) if mode == SCALE_COMPUTE else 0, dev)
-    _check(lib.qz_kv_write_fp8(_ptr(k), _ptr(v), B, H, T, D, _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
-                               _ptr(v_scale), mode, _ptr(buf), nb, _stream(stream)), "qz_kv_write_fp8")
+    args = (_arg(k_codes, "k_codes", d, 1, n), _arg(v_codes, "v_codes", d, 1, n),
+            _arg(k_scale, "k_scale", d, torch.float32, 1), _arg(v_scale, "v_scale", d, torch.float32, 1))
+    buf, nb = _ws(ws, qz_workspace_size(OP_KV_WRITE_FP8, n) if mode == SCALE_COMPUTE else 0, d)
+    _check(lib.qz_kv_write_fp8(k.data_ptr(), v.data_ptr(), B, H, T, D, *args, mode, _ptr(buf), nb, _stream(stream)),
+           "qz_kv_write_fp8")
     return k_codes, v_codes, k_scale, v_scale
 
 
@@ -304,11 +364,13 @@ def qz_gemm_w4a16(A: torch.Tensor, qweight: torch.Tensor, scale_bf16: torch.Tens
     """Y[M, N] (bf16) = A[M, K] (bf16) @ dequant(INT4 g128 weight)."""
     M, K = A.shape
     N = qweight.shape[1]
+    d = _device()
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, M, N, K), A.device)
-    _check(lib.qz_gemm_w4a16(_ptr(A), _ptr(qweight), _ptr(scale_bf16), _ptr(Y), M, N, K, _ptr(buf), nb,
-                             _stream(stream)), "qz_gemm_w4a16")
+    args = (_arg(A, "A", d, torch.bfloat16), _arg(qweight, "qweight", d, 4, (K // 8) * N),
+            _arg(scale_bf16, "scale_bf16", d, 2, (K // 128) * N), _arg(Y, "Y", d, torch.bfloat16, M * N))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, M, N, K), d)
+    _check(lib.qz_gemm_w4a16(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_w4a16")
     return Y
 
 
@@ -316,13 +378,15 @@ def qz_gemm_w4a16_grouped(problems, ws=None, stream=None):
     """Run independent W4A16 problems [(A, qweight, scale_bf16, Y), ...] in one launch."""
     arr = (_W4A16Problem * len(problems))()
     mmax = kmax = nsum = 0
-    dev = None
+    d = _device()
     for i, (A, qw, sc, Y) in enumerate(problems):
         M, K = A.shape
         N = qw.shape[1]
-        arr[i] = _W4A16Problem(A.data_ptr(), qw.data_ptr(), sc.data_ptr(), Y.data_ptr(), M, N, K)
-        mmax, kmax, nsum, dev = max(mmax, M), max(kmax, K), nsum + N, A.device
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, mmax, nsum, kmax), dev)
+        arr[i] = _W4A16Problem(_arg(A, f"A[{i}]", d, torch.bfloat16), _arg(qw, f"qweight[{i}]", d, 4, (K // 8) * N),
+                               _arg(sc, f"scale_bf16[{i}]", d, 2, (K // 128) * N),
+                               _arg(Y, f"Y[{i}]", d, torch.bfloat16, M * N), M, N, K)
+        mmax, kmax, nsum = max(mmax, M), max(kmax, K), nsum + N
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_W4A16, mmax, nsum, kmax), d)
     _check(lib.qz_gemm_w4a16_grouped(arr, len(problems), _ptr(buf), nb, _stream(stream)),
            "qz_gemm_w4a16_grouped")
 
@@ -332,11 +396,13 @@ def qz_gemm_fp8_block(qA, sA, qB, sB, Y=None, ws=None, stream=None):
     with 128x128 scales sB."""
     M, K = qA.shape
     N = qB.shape[0]
+    d = _device()
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_FP8_BLOCK, M, N, K), qA.device)
-    _check(lib.qz_gemm_fp8_block(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), _ptr(Y), M, N, K, _ptr(buf), nb,
-                                 _stream(stream)), "qz_gemm_fp8_block")
+    args = (_arg(qA, "qA", d, 1), _arg(sA, "sA", d, torch.float32, M * (K // 128)), _arg(qB, "qB", d, 1, N * K),
+            _arg(sB, "sB", d, torch.float32, (N // 128) * (K // 128)), _arg(Y, "Y", d, torch.bfloat16, M * N))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_FP8_BLOCK, M, N, K), d)
+    _check(lib.qz_gemm_fp8_block(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_fp8_block")
     return Y
 
 
@@ -345,11 +411,14 @@ def qz_gemm_nvfp4(qA, sA, gA, qB, sB, gB, Y=None, ws=None, stream=None):
     tensor scale each)."""
     M, K = qA.shape[0], qA.shape[1] * 2
     N = qB.shape[0]
+    d = _device()
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), qA.device)
-    _check(lib.qz_gemm_nvfp4(_ptr(qA), _ptr(sA), _ptr(gA), _ptr(qB), _ptr(sB), _ptr(gB), _ptr(Y), M, N, K,
-                             _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4")
+    args = (_arg(qA, "qA", d, 1, M * K // 2), _arg(sA, "sA", d, 1, M * (K // 16)), _arg(gA, "gA", d, torch.float32, 1),
+            _arg(qB, "qB", d, 1, N * K // 2), _arg(sB, "sB", d, 1, N * (K // 16)), _arg(gB, "gB", d, torch.float32, 1),
+            _arg(Y, "Y", d, torch.bfloat16, M * N))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), d)
+    _check(lib.qz_gemm_nvfp4(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4")
     return Y
 
 
@@ -357,11 +426,13 @@ def qz_gemm_mxfp4(qA, eA, qB, eB, Y=None, ws=None, stream=None):
     """Y[M, N] (bf16) from MXFP4 A [M, K] and B^T [N, K] (codes, E8M0 block scales)."""
     M, K = qA.shape[0], qA.shape[1] * 2
     N = qB.shape[0]
+    d = _device()
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_MXFP4, M, N, K), qA.device)
-    _check(lib.qz_gemm_mxfp4(_ptr(qA), _ptr(eA), _ptr(qB), _ptr(eB), _ptr(Y), M, N, K, _ptr(buf), nb,
-                             _stream(stream)), "qz_gemm_mxfp4")
+    args = (_arg(qA, "qA", d, 1, M * K // 2), _arg(eA, "eA", d, 1, M * (K // 32)), _arg(qB, "qB", d, 1, N * K // 2),
+            _arg(eB, "eB", d, 1, N * (K // 32)), _arg(Y, "Y", d, torch.bfloat16, M * N))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_MXFP4, M, N, K), d)
+    _check(lib.qz_gemm_mxfp4(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_mxfp4")
     return Y
 
 
@@ -369,10 +440,12 @@ def qz_prepare_fp4_scales(scales, K: int, nv: bool = True, out=None, stream=None
     """Block scales [rows, K/16] (NVFP4) or [rows, K/32] (MXFP4), row-major uint8, re-laid
     into the tensor cores' scale-factor order (rows padded to a multiple of 128)."""
     rows = scales.shape[0]
+    d = _device()
+    n_out = qz_workspace_size(OP_PREPARE_FP4_SCALES, rows, K, int(nv))
     if out is None:
-        out = torch.empty(qz_workspace_size(OP_PREPARE_FP4_SCALES, rows, K, int(nv)), dtype=torch.uint8,
-                          device=scales.device)
-    _check(lib.qz_prepare_fp4_scales(_ptr(scales), rows, K, int(nv), _ptr(out), _stream(stream)),
+        out = torch.empty(n_out, dtype=torch.uint8, device=scales.device)
+    _check(lib.qz_prepare_fp4_scales(_arg(scales, "scales", d, 1, rows * (K // (16 if nv else 32))), rows, K,
+                                     int(nv), _arg(out, "out", d, 1, n_out), _stream(stream)),
            "qz_prepare_fp4_scales")
     return out
 
@@ -382,13 +455,17 @@ def qz_gemm_nvfp4_grouped(problems, ws=None, stream=None):
     shapes, M <= 128) with one scale re-layout launch and one GEMM launch per 80 problems."""
     arr = (_Nvfp4Problem * len(problems))()
     kmax = 0
-    dev = None
+    d = _device()
     for i, (qA, sA, gA, qB, sBp, gB, Y) in enumerate(problems):
         M, K = qA.shape[0], qA.shape[1] * 2
         N = qB.shape[0]
-        arr[i] = _Nvfp4Problem(qA.data_ptr(), sA.data_ptr(), gA.data_ptr(), qB.data_ptr(), sBp.data_ptr(),
-                               gB.data_ptr(), Y.data_ptr(), M, N, K)
-        kmax, dev = max(kmax, K), qA.device
-    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4_GROUPED, len(problems), kmax), dev)
+        arr[i] = _Nvfp4Problem(_arg(qA, f"qA[{i}]", d, 1, M * K // 2), _arg(sA, f"sA[{i}]", d, 1, M * (K // 16)),
+                               _arg(gA, f"gA[{i}]", d, torch.float32, 1), _arg(qB, f"qB[{i}]", d, 1, N * K // 2),
+                               _arg(sBp, f"sB_prepared[{i}]", d, 1,
+                                    qz_workspace_size(OP_PREPARE_FP4_SCALES, N, K, 1)),
+                               _arg(gB, f"gB[{i}]", d, torch.float32, 1),
+                               _arg(Y, f"Y[{i}]", d, torch.bfloat16, M * N), M, N, K)
+        kmax = max(kmax, K)
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4_GROUPED, len(problems), kmax), d)
     _check(lib.qz_gemm_nvfp4_grouped(arr, len(problems), _ptr(buf), nb, _stream(stream)),
            "qz_gemm_nvfp4_grouped")
