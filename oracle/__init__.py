@@ -26,17 +26,18 @@ _lib = None
 FP8_PER_TENSOR, FP8_PER_ROW, FP8_BLOCK_128x128, FP8_GROUP_1x128 = 0, 1, 2, 3
 
 
-def build(force: bool = False) -> str:
-    """Compile qz_oracle.c with gcc (single-threaded, no FMA contraction)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
-    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-    tmp = _LIB + f".tmp{os.getpid()}"
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile qz_oracle.c (or another copy of it, `src`, into `out`) with gcc:
+    single-threaded, no FMA contraction."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
-           "-Wall", "-o", tmp, _SRC, "-lm"]
+           "-Wall", "-o", tmp, src, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, out)
+    return out
 
 
 def _load():

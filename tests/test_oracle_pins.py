@@ -314,6 +314,13 @@ def test_nvfp4_invariants():
     unclipped = y <= 6
     hg = _grid_half_gap(E2M1_GRID, np.minimum(y, 6.0))
     assert np.all(err[unclipped] <= (hg * sf)[unclipped] * (1 + 2.0 ** -20) + 2.0 ** -24 * np.abs(x[unclipped]))
+    # each block's largest |x| encodes to magnitude 6 (E2M1 index 7): the block scale is
+    # amax16 / 6 / g rounded to E4M3, within 1/16 relative wherever that E4M3 value is normal
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(x.shape[0], -1, 16)
+    top = np.abs(x).reshape(x.shape[0], -1, 16).argmax(axis=2)
+    top_idx = np.take_along_axis(nib, top[..., None], axis=2)[..., 0] & 0x7
+    normal = b >= 2.0 ** -6
+    assert normal.sum() > normal.size // 2 and np.all(top_idx[normal] == 7)
     # given amax reproduces the computed path
     c2, s2, g2, d2 = oracle.quant_nvfp4(x, amax_in=float(amax))
     assert np.array_equal(c2, codes) and np.array_equal(s2, sb) and g2 == g
@@ -328,6 +335,9 @@ def test_nvfp4_block_scale_rounding_to_zero_keeps_codes_of_page():
     codes, sb, g, deq = oracle.quant_nvfp4(x)
     assert sb[0, 1] == 0
     assert all((codes[0, 8 + i] & 0xF) == 0x7 and (codes[0, 8 + i] >> 4) == 0x7 for i in range(8))
+    # and dequantizes to 6 * (1e-12 * g) in fp32, not to 0 (the floor applies before the product)
+    s_eff = np.float32(np.float32(1e-12) * np.float32(g))
+    assert np.all(deq[0, 16:] == np.float32(6.0) * s_eff) and s_eff > 0
 
 
 def test_int4_g128_invariants():
