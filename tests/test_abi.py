@@ -183,3 +183,27 @@ def test_grouped_nvfp4_quantize_validation(qz):
     assert L.qz_quantize_nvfp4_grouped(one(codes=0x10002), 1, 0, FAKE, ws_need, NULL) == 3
     assert L.qz_quantize_nvfp4_grouped(one(3), 3, 0, FAKE, ws_need - 1, NULL) == 7         # workspace
     assert L.qz_quantize_nvfp4_grouped(one(3), 3, 0, NULL, ws_need, NULL) == 7
+
+
+def test_grouped_w4a16_validation(qz):
+    """A group is checked whole before any launch: one bad problem anywhere (here after a
+    valid one) rejects the call."""
+    L = qz.lib
+    P = qz._W4A16Problem
+    good = dict(A=0x10000, qweight=0x10000, scale_bf16=0x10000, Y=0x10000, M=4, N=128, K=256)
+
+    def group(*changes):
+        arr = (P * len(changes))()
+        for i, ch in enumerate(changes):
+            arr[i] = P(**{**good, **ch})
+        return arr
+
+    many = (P * 257)()
+    assert L.qz_gemm_w4a16_grouped(many, 257, NULL, 0, NULL) == 1            # count > 256
+    assert L.qz_gemm_w4a16_grouped(group({}, {"M": 65}), 2, NULL, 0, NULL) == 2
+    assert L.qz_gemm_w4a16_grouped(group({}, {"K": 200}), 2, NULL, 0, NULL) == 2
+    assert L.qz_gemm_w4a16_grouped(group({}, {"N": 96}), 2, NULL, 0, NULL) == 2
+    assert L.qz_gemm_w4a16_grouped(group({}, {"N": 0}), 2, NULL, 0, NULL) == 1
+    assert L.qz_gemm_w4a16_grouped(group({}, {"Y": 0}), 2, NULL, 0, NULL) == 1
+    assert L.qz_gemm_w4a16_grouped(group({}, {"scale_bf16": 0x10008}), 2, NULL, 0, NULL) == 3
+    assert L.qz_gemm_w4a16_grouped(group({"M": 0}), 1, NULL, 0, NULL) == 1
