@@ -3,7 +3,6 @@ the roofline, the lookup of recorded DRAM traffic (valid only while the kernel's
 source is unchanged), the clock and throttle-reason summary of nvidia-smi samples,
 and the number of input copies that keeps timed inputs out of L2."""
 import hashlib
-import os
 
 import bench
 
