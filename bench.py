@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -570,19 +571,64 @@ def cpu_baseline(budget_s: float = 12.0):
     import oracle
     c = _cpu_inputs()
     done_bytes, spent, n_cols = 0.0, 0.0, 0
-    while spent < budget_s and n_cols < N_DIM:
-        cols = np.arange(n_cols, n_cols + 64)
-        for M in MS:
-            ii = np.repeat(np.arange(M), cols.size)
-            jj = np.tile(cols, M)
-            t0 = time.perf_counter()
-            oracle.gemm_w4a16(c["acts"][M], c["qw"], c["sc"], ii, jj)
-            spent += time.perf_counter() - t0
-            done_bytes += step_bytes(M) * cols.size / N_DIM
-        n_cols += cols.size
+    with _one_core() as core:
+        while spent < budget_s and n_cols < N_DIM:
+            cols = np.arange(n_cols, n_cols + 64)
+            for M in MS:
+                ii = np.repeat(np.arange(M), cols.size)
+                jj = np.tile(cols, M)
+                t0 = time.perf_counter()
+                oracle.gemm_w4a16(c["acts"][M], c["qw"], c["sc"], ii, jj)
+                spent += time.perf_counter() - t0
+                done_bytes += step_bytes(M) * cols.size / N_DIM
+            n_cols += cols.size
     return {"value": round(done_bytes / spent / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n_cols} of {N_DIM} output columns at each M in {list(MS)} (K={K_DIM}); "
-                      f"{spent:.1f} s of single-threaded oracle time"}
+                      f"{spent:.1f} s of single-threaded oracle time",
+            "host": {**host_cpu(), "pinned_core": core}}
+
+
+def host_cpu(cpuinfo: str = "/proc/cpuinfo"):
+    """Core count and CPU model of this host: /proc/cpuinfo's model name, or on Arm
+    hosts (which list none) the implementer and part numbers of the first core."""
+    fields = {}
+    try:
+        with open(cpuinfo, encoding="utf-8", errors="replace") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key and val and key not in fields:
+                    fields[key] = val
+    except OSError:
+        pass
+    if "model name" in fields:
+        model = fields["model name"]
+    elif "cpu part" in fields:
+        model = f"implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    else:
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu": model, "machine": platform.machine()}
+
+
+class _one_core:
+    """Pins this process to one of its allowed cores while the oracle is timed (the
+    oracle is single-threaded), restoring the previous affinity afterwards; yields
+    the core, or None where affinity cannot be set."""
+
+    def __enter__(self):
+        self.prev = None
+        try:
+            self.prev = os.sched_getaffinity(0)
+            core = min(self.prev)
+            os.sched_setaffinity(0, {core})
+            return core
+        except (AttributeError, OSError, ValueError):
+            self.prev = None
+            return None
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            os.sched_setaffinity(0, self.prev)
 
 
 def reference_arm(args, rank, world):
@@ -605,7 +651,7 @@ def reference_arm(args, rank, world):
             "config": {"workload": WORKLOAD, "M": list(MS), "K": K_DIM, "N": N_DIM,
                        "parallelism": "cpu single thread"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": vals[-1]["sample"]},
+                             "sample": vals[-1]["sample"], "host": vals[-1].get("host")},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -3,6 +3,7 @@ the roofline, the lookup of recorded DRAM traffic (valid only while the kernel's
 source is unchanged), the clock and throttle-reason summary of nvidia-smi samples,
 and the number of input copies that keeps timed inputs out of L2."""
 import hashlib
+import os
 
 import bench
 
@@ -89,3 +90,23 @@ def test_copies_exceed_twice_l2():
         assert c >= 2
         assert c * nbytes >= 2 * l2 or c == 2
         assert c == 2 or (c - 1) * nbytes < 2 * l2        # no more copies than needed
+
+
+def test_host_cpu_model(tmp_path):
+    x86 = tmp_path / "x86"
+    x86.write_text("processor\t: 0\nvendor_id\t: GenuineIntel\nmodel\t\t: 167\n"
+                   "model name\t: Example CPU @ 2.70GHz\n\nprocessor\t: 1\nmodel name\t: other\n")
+    got = bench.host_cpu(str(x86))
+    assert got["cpu"] == "Example CPU @ 2.70GHz" and got["nproc"] >= 1
+    arm = tmp_path / "arm"
+    arm.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\n"
+                   "CPU variant\t: 0x0\nCPU part\t: 0xd4f\nCPU revision\t: 0\n")
+    assert bench.host_cpu(str(arm))["cpu"] == "implementer 0x41 part 0xd4f"
+    assert bench.host_cpu(str(tmp_path / "missing"))["cpu"]          # falls back to the platform
+
+
+def test_oracle_timing_pins_one_core_and_restores():
+    before = os.sched_getaffinity(0)
+    with bench._one_core() as core:
+        assert core in before and os.sched_getaffinity(0) == {core}
+    assert os.sched_getaffinity(0) == before
