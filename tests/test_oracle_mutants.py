@@ -12,11 +12,12 @@ Each mutation keeps every memory access of the oracle within its buffers. The
 mutants run in one spawned child process, so that the real oracle loaded by the
 other tests is never replaced in this process.
 
-One mutation is left out on purpose: reading the two FP4 nibbles of a byte in
-the other order inside the GEMM references alone permutes k identically for
-both operands within one scale block, which leaves every GEMM result unchanged
-(the quantizers' own packing order is pinned through the int4 and FP4 cases
-below).
+Mutations that cannot change any result are left out on purpose: reading the
+two FP4 nibbles of a byte in the other order inside the GEMM references alone
+permutes k identically for both operands within one scale block, which leaves
+every GEMM result unchanged; the quantizers' leading dimension is always the
+column count (the wrapper passes contiguous arrays); an INT4 clamp of -7
+instead of -8 never binds, since |w / s| <= 7 (1 + 2^-8) with s = bf16(amax / 7).
 """
 import multiprocessing as mp
 import os
@@ -99,6 +100,23 @@ MUTANTS = {
                          ["test_gemm_scale_indexing_matches_quantizer_dequant"]),
     "mx_gemm_bias": ("(int)eB[j * (K / 32) + k / 32] - 127", "(int)eB[j * (K / 32) + k / 32] - 126",
                      ["test_gemm_fp4_integer_case_is_exact_matmul"]),
+    "e4m3_max_code_416": ("for (int c = 0; c <= 0x7E; c++) {", "for (int c = 0; c <= 0x7D; c++) {",
+                          ["test_e4m3_decode_encode_identity_all_codes", "test_e4m3_saturates_like_clamp"]),
+    "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);",
+                    ["test_e4m3_format_facts", "test_e4m3_encode_matches_torch_cast"]),
+    "e2m1_no_abs": ("uint8_t or_e2m1_encode(float y)\n{\n    double a = fabs((double)y);",
+                    "uint8_t or_e2m1_encode(float y)\n{\n    double a = (double)y;",
+                    ["test_e2m1_matches_torch_argmin_pipeline"]),
+    "mx_no_clamp_floor": ("            if (amax < or_amax_min()) amax = or_amax_min();\n            int E",
+                          "            int E", ["test_fp4_all_zero_blocks_use_clamp_floor"]),
+    "nv_block_uses_tensor_amax": ("float t = bamax / OR_FP4_MAX / g;", "float t = amax_t / OR_FP4_MAX / g;",
+                                  ["test_nvfp4_invariants"]),
+    "int4_amax_signed": ("                float a = fabsf(or_elem(w, is_bf16, k * ldw + n));",
+                         "                float a = or_elem(w, is_bf16, k * ldw + n);",
+                         ["test_int4_g128_invariants"]),
+    "kv_k_scale_into_v": ("or_quant_fp8(k, 1, 1, n, n, OR_TENSOR, k_codes, k_scale, k_deq);",
+                          "or_quant_fp8(k, 1, 1, n, n, OR_TENSOR, k_codes, v_scale, k_deq);",
+                          ["test_kv_write_is_per_tensor_on_k_and_v"]),
 }
 
 

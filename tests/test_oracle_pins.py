@@ -267,6 +267,23 @@ def test_fp8_all_zero_tensor_uses_clamp_floor():
     assert not codes.any() and not deq.any()
 
 
+def test_fp4_all_zero_blocks_use_clamp_floor():
+    # The page clamps every amax to at least 1e-12 before taking a scale. MXFP4: an all-zero
+    # block gets E = floor(log2(fp32(1e-12))) - 2 = -42, E8M0 code 85. NVFP4: an all-zero
+    # tensor gets g = fp32(1e-12) / 2688 and block scale E4M3(0) = 0.
+    x = np.zeros((2, 64), np.float32)
+    x[1, 32:] = 1.0                                                   # one non-zero block
+    codes, e8, deq = oracle.quant_mxfp4(x)
+    e_floor = int(np.floor(np.log2(np.float64(np.float32(1e-12))))) - 2
+    assert e_floor == -42
+    assert e8[0, 0] == e8[0, 1] == e8[1, 0] == e_floor + 127 and e8[1, 1] == 0 - 2 + 127
+    assert not codes[0].any() and not deq[0].any()
+    z = np.zeros((1, 32), np.float32)
+    c, sb, g, d = oracle.quant_nvfp4(z)
+    assert g == np.float32(np.float32(1e-12) / np.float32(2688.0))
+    assert not sb.any() and not c.any() and not d.any()
+
+
 def test_mxfp4_invariants():
     x = _outlier_tensor()
     codes, e8, deq = oracle.quant_mxfp4(x)
