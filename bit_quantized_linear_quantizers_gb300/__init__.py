@@ -20,7 +20,7 @@ __all__ = [
     "FP8_GROUP_1x128", "SCALE_COMPUTE", "SCALE_GIVEN", "qz_workspace_size", "qz_status_string",
     "qz_device_error", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
     "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
-    "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
+    "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_nvfp4_noalloc", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
     "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
 ]
 
@@ -419,6 +419,22 @@ def qz_gemm_nvfp4(qA, sA, gA, qB, sB, gB, Y=None, ws=None, stream=None):
             _arg(Y, "Y", d, torch.bfloat16, M * N))
     buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), d)
     _check(lib.qz_gemm_nvfp4(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4")
+    return Y
+
+
+def qz_gemm_nvfp4_noalloc(qA, sA, gA, qB, sB, gB, Y=None, stream=None):
+    """qz_gemm_nvfp4 without a workspace: the re-laid scale factors live in the library's
+    fixed device array (see include/qz.h), so calls that may overlap on the GPU must be
+    serialised by the caller."""
+    M, K = qA.shape[0], qA.shape[1] * 2
+    N = qB.shape[0]
+    d = _device()
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    args = (_arg(qA, "qA", d, 1, M * K // 2), _arg(sA, "sA", d, 1, M * (K // 16)), _arg(gA, "gA", d, torch.float32, 1),
+            _arg(qB, "qB", d, 1, N * K // 2), _arg(sB, "sB", d, 1, N * (K // 16)), _arg(gB, "gB", d, torch.float32, 1),
+            _arg(Y, "Y", d, torch.bfloat16, M * N))
+    _check(lib.qz_gemm_nvfp4_noalloc(*args, M, N, K, _stream(stream)), "qz_gemm_nvfp4_noalloc")
     return Y
 
 

@@ -103,3 +103,17 @@ def test_output_shape_mismatch_is_refused_before_the_call(monkeypatch):
     with pytest.raises(ValueError, match=r"sB_prepared\[0\]"):
         qz.qz_gemm_nvfp4_grouped([(qA, sA, g, qB, torch.zeros(100, dtype=torch.uint8), g,
                                    torch.zeros((4, 256), dtype=torch.bfloat16))])
+
+
+def test_binding_has_the_c_names():
+    """Every entry point that include/qz.h declares has a Python function of the same name."""
+    import test_abi
+    missing = [n for n in test_abi.declared_functions() if not callable(getattr(qz, n, None))]
+    assert missing == []
+
+
+def test_noalloc_wrapper_checks_like_the_others(on_device0):
+    with pytest.raises(ValueError, match="qA: .*on cpu"):
+        qz.qz_gemm_nvfp4_noalloc(torch.zeros((128, 128), dtype=torch.uint8), torch.zeros((128, 16), dtype=torch.uint8),
+                                 torch.ones(1), torch.zeros((256, 128), dtype=torch.uint8),
+                                 torch.zeros((256, 16), dtype=torch.uint8), torch.ones(1))
