@@ -207,3 +207,24 @@ def test_grouped_w4a16_validation(qz):
     assert L.qz_gemm_w4a16_grouped(group({}, {"Y": 0}), 2, NULL, 0, NULL) == 1
     assert L.qz_gemm_w4a16_grouped(group({}, {"scale_bf16": 0x10008}), 2, NULL, 0, NULL) == 3
     assert L.qz_gemm_w4a16_grouped(group({"M": 0}), 1, NULL, 0, NULL) == 1
+
+
+def test_fp4_scale_layout_sizes(qz):
+    """The prepared scale-factor layout holds whole 128-row blocks of 512-byte atoms (128 rows
+    x 4 scales): rows padded up to a multiple of 128, K/16 (NVFP4) or K/32 (MXFP4) scales a
+    row. The single-problem FP4 GEMMs' workspace holds both operands' re-laid scales, each
+    rounded up to 1 KiB (the limit the allocation-free entry point states)."""
+    size = qz.qz_workspace_size
+    for rows, K in ((1, 256), (128, 256), (129, 4096), (8192, 4096)):
+        padded = -(-rows // 128) * 128
+        assert size(qz.OP_PREPARE_FP4_SCALES, rows, K, 1) == padded * (K // 16)
+        assert size(qz.OP_PREPARE_FP4_SCALES, rows, K, 0) == padded * (K // 32)
+        assert padded * (K // 16) % 512 == 0
+    r1k = lambda b: -(-b // 1024) * 1024
+    for M, N, K in ((128, 256, 256), (8192, 4096, 4096), (384, 512, 768)):
+        want = r1k(M * K // 16) + r1k(N * K // 16)
+        assert size(qz.OP_GEMM_NVFP4, M, N, K) == want
+        assert size(qz.OP_GEMM_MXFP4, M, N, K) == want
+    # the no-alloc scratch (4 MiB) fits M + N = 16384 at K = 4096, as its header states
+    assert r1k(8192 * 4096 // 16) + r1k(8192 * 4096 // 16) <= 4 << 20
+    assert size(qz.OP_PREPARE_FP4_SCALES, 0, 256, 1) == 0                  # rejected sizes: 0
