@@ -656,7 +656,10 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def main(argv=None):
+ROW_NAMES = ("fp8", "fp4", "roundtrip", "kv", "qwen")
+
+
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -667,9 +670,17 @@ def main(argv=None):
                     help="secondary rows to measure (comma list of fp8, fp4, roundtrip, kv, qwen)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap
+
+
+def main(argv=None):
+    ap = build_parser()
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    unknown = set(args.rows.split(",")) - set(ROW_NAMES)
+    if unknown:
+        ap.error(f"unknown rows: {sorted(unknown)}")
     rank, world, local_rank = dist_setup(args.gpus)
     if args.impl == "reference":
         reference_arm(args, rank, world)

@@ -110,3 +110,33 @@ def test_oracle_timing_pins_one_core_and_restores():
     with bench._one_core() as core:
         assert core in before and os.sched_getaffinity(0) == {core}
     assert os.sched_getaffinity(0) == before
+
+
+def _recorded_commands():
+    """(file, ncu command, bench arguments) for every command recorded under profiles/."""
+    import glob
+    import re
+    import shlex
+    out = []
+    for path in sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*"))):
+        text = open(path, encoding="utf-8").read()
+        text = re.sub(r"\\\n\s*(#\s*)?", " ", text)                  # join continued lines
+        for line in text.splitlines():
+            line = line.lstrip("# ").strip()
+            if line.startswith("ncu ") and "python bench.py" in line:
+                argv = shlex.split(line.split("python bench.py", 1)[1])
+                out.append((os.path.basename(path), line, argv))
+    return out
+
+
+def test_recorded_profile_commands_run_committed_files():
+    """Every ncu command recorded under profiles/ keeps the clocks unlocked and runs
+    bench.py with arguments its parser still accepts."""
+    cmds = _recorded_commands()
+    assert {f for f, _, _ in cmds} >= {"traffic.txt", "launches_w4a16_decode_step.md",
+                                       "w4a16_bulk_kernel_llama_mlp_M1.md"}
+    for fname, line, argv in cmds:
+        assert "--clock-control none" in line, fname
+        args = bench.build_parser().parse_args(argv)
+        assert args.warmup >= 3, fname
+        assert set(args.rows.split(",")) <= set(bench.ROW_NAMES), fname
