@@ -567,25 +567,32 @@ def cpu_baseline(budget_s: float = 12.0):
     this host on a bounded sample: chunks of 64 output columns at every M in
     {1, 4, 16}, until the time budget is spent. Bytes are counted as for the GPU
     (the sampled columns' share of each GEMM's algorithmic bytes)."""
-    import numpy as np
-    import oracle
-    c = _cpu_inputs()
-    done_bytes, spent, n_cols = 0.0, 0.0, 0
     with _one_core() as core:
-        while spent < budget_s and n_cols < N_DIM:
-            cols = np.arange(n_cols, n_cols + 64)
-            for M in MS:
-                ii = np.repeat(np.arange(M), cols.size)
-                jj = np.tile(cols, M)
-                t0 = time.perf_counter()
-                oracle.gemm_w4a16(c["acts"][M], c["qw"], c["sc"], ii, jj)
-                spent += time.perf_counter() - t0
-                done_bytes += step_bytes(M) * cols.size / N_DIM
-            n_cols += cols.size
+        done_bytes, spent, n_cols = _oracle_w4a16_sample(budget_s)
     return {"value": round(done_bytes / spent / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n_cols} of {N_DIM} output columns at each M in {list(MS)} (K={K_DIM}); "
                       f"{spent:.1f} s of single-threaded oracle time",
             "host": {**host_cpu(), "pinned_core": core}}
+
+
+def _oracle_w4a16_sample(budget_s: float):
+    """(algorithmic bytes covered, oracle seconds, output columns) of the oracle's W4A16
+    reference run over chunks of 64 output columns at every M until the budget is spent."""
+    import numpy as np
+    import oracle
+    c = _cpu_inputs()
+    done_bytes, spent, n_cols = 0.0, 0.0, 0
+    while spent < budget_s and n_cols < N_DIM:
+        cols = np.arange(n_cols, n_cols + 64)
+        for M in MS:
+            ii = np.repeat(np.arange(M), cols.size)
+            jj = np.tile(cols, M)
+            t0 = time.perf_counter()
+            oracle.gemm_w4a16(c["acts"][M], c["qw"], c["sc"], ii, jj)
+            spent += time.perf_counter() - t0
+            done_bytes += step_bytes(M) * cols.size / N_DIM
+        n_cols += cols.size
+    return done_bytes, spent, n_cols
 
 
 def host_cpu(cpuinfo: str = "/proc/cpuinfo"):
@@ -631,6 +638,84 @@ class _one_core:
             os.sched_setaffinity(0, self.prev)
 
 
+def oracle_per_config():
+    """Wall time of the oracle (single-threaded C, pinned to one core) per workload: each
+    part timed on a bounded sample of its workload, with the share of the full workload
+    the sample covers and the time extrapolated to all of it (the oracle's cost is
+    linear in the elements it quantizes and in the output points it computes)."""
+    import numpy as np
+    import oracle
+    import synthetic as syn
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def part(seconds, share, sample):
+        return {"seconds": round(seconds, 3), "share": share, "sample": sample,
+                "extrapolated_seconds": round(seconds / share, 1)}
+
+    def points(M, N, n, seed):
+        rng = np.random.default_rng(seed)
+        return rng.integers(0, M, n), rng.integers(0, N, n)
+
+    out = {}
+    with _one_core() as core:
+        x = syn.quant_roundtrip_input(seed=0)
+        out["1_quantize_roundtrip_1024x1024_f32"] = part(timed(lambda: (
+            [oracle.quant_fp8(x, g) for g in range(4)], oracle.quant_mxfp4(x), oracle.quant_nvfp4(x),
+            oracle.quant_int4_g128(x))), 1.0, "the seven quantizer paths on the whole tensor")
+        _, spent, n_cols = _oracle_w4a16_sample(5.0)
+        out["2_w4a16_decode_M1_4_16"] = part(spent, n_cols / N_DIM,
+                                             f"{n_cols} of {N_DIM} output columns at each M in {list(MS)}")
+
+        a, bt = syn.fp8_block_gemm_inputs(seed=0, M=128, N=256)
+        qa, sa, _ = oracle.quant_fp8(a, oracle.FP8_GROUP_1x128, want_deq=False)
+        qb, sb, _ = oracle.quant_fp8(bt, oracle.FP8_BLOCK_128x128, want_deq=False)
+        ii, jj = points(128, 256, 4096, 3)
+        out["3_fp8_quantize_A_2048x4096"] = part(timed(
+            lambda: oracle.quant_fp8(a, oracle.FP8_GROUP_1x128, want_deq=False)), 128 / 2048, "128 of 2048 rows")
+        out["3_fp8_quantize_Bt_14336x4096"] = part(timed(
+            lambda: oracle.quant_fp8(bt, oracle.FP8_BLOCK_128x128, want_deq=False)), 256 / 14336, "256 of 14336 rows")
+        out["3_fp8_block_gemm_2048x14336x4096"] = part(timed(
+            lambda: oracle.gemm_fp8_block(qa, sa, qb, sb, ii, jj)), 4096 / (2048 * 14336), "4096 output points")
+
+        a, bt = syn.fp4_gemm_inputs(seed=0, M=128, N=256)
+        ca, sca, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+        cb, scb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+        ma, ea, _ = oracle.quant_mxfp4(a, want_deq=False)
+        mb, eb, _ = oracle.quant_mxfp4(bt, want_deq=False)
+        ii, jj = points(128, 256, 4096, 4)
+        out["4_nvfp4_quantize_A_8192x4096"] = part(timed(
+            lambda: oracle.quant_nvfp4(a, want_deq=False)), 128 / 8192, "128 of 8192 rows")
+        out["4_mxfp4_quantize_A_8192x4096"] = part(timed(
+            lambda: oracle.quant_mxfp4(a, want_deq=False)), 128 / 8192, "128 of 8192 rows")
+        out["4_nvfp4_gemm_8192x4096x4096"] = part(timed(
+            lambda: oracle.gemm_nvfp4(ca, sca, ga, cb, scb, gb, ii, jj)), 4096 / (8192 * 4096), "4096 output points")
+        out["4_mxfp4_gemm_8192x4096x4096"] = part(timed(
+            lambda: oracle.gemm_mxfp4(ma, ea, mb, eb, ii, jj)), 4096 / (8192 * 4096), "4096 output points")
+
+        w4_s = nv_s = 0.0
+        n_pts, full_pts = 0, 0
+        for _, name, a_bits, w in syn.qwen3_decode_linears(layers=1, tokens=64, seed=0):
+            K, N = w.shape
+            qw, sc, _ = oracle.quant_int4_g128(w, want_deq=False)
+            ca, sca, ga, _ = oracle.quant_nvfp4(a_bits, want_deq=False)
+            cb, scb, gb, _ = oracle.quant_nvfp4(syn.to_bf16_bits(np.ascontiguousarray(w.T)), want_deq=False)
+            ii, jj = points(64, N, 512, K + N)
+            w4_s += timed(lambda: oracle.gemm_w4a16(a_bits, qw, sc, ii, jj))
+            nv_s += timed(lambda: oracle.gemm_nvfp4(ca, sca, ga, cb, scb, gb, ii, jj))
+            n_pts += ii.size
+            full_pts += 64 * N
+        share = n_pts / (28 * full_pts)
+        out["5_qwen3_step_w4a16_196_linears"] = part(w4_s, share, "512 output points of each linear of one layer")
+        out["5_qwen3_step_nvfp4_196_linears"] = part(nv_s, share, "512 output points of each linear of one layer")
+        k, v = syn.kv_cache_inputs(seed=0)
+        out["5_kv_write_fp8_2x8x4096x128"] = part(timed(lambda: oracle.kv_write_fp8(k, v)), 1.0, "the whole K and V")
+    return {"oracle_per_config": out, "host": {**host_cpu(), "pinned_core": core}}
+
+
 def reference_arm(args, rank, world):
     """--impl reference: the CPU oracle as it stands, timed on this host's cores, on a
     bounded sample of the same workload each step. Rank 0 alone runs it."""
@@ -670,6 +755,8 @@ def build_parser() -> argparse.ArgumentParser:
                     help="secondary rows to measure (comma list of fp8, fp4, roundtrip, kv, qwen)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--oracle-per-config", action="store_true",
+                    help="only time the CPU oracle on a sample of every workload (no GPU) and print it")
     return ap
 
 
@@ -681,6 +768,9 @@ def main(argv=None):
     unknown = set(args.rows.split(",")) - set(ROW_NAMES)
     if unknown:
         ap.error(f"unknown rows: {sorted(unknown)}")
+    if args.oracle_per_config:
+        print(json.dumps(oracle_per_config()), flush=True)
+        return
     rank, world, local_rank = dist_setup(args.gpus)
     if args.impl == "reference":
         reference_arm(args, rank, world)
