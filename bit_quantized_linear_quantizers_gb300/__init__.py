@@ -18,7 +18,7 @@ from ._build import LIB, build  # noqa: F401  (build() is the in-tree build step
 __all__ = [
     "QZError", "lib", "F32", "BF16", "FP8_PER_TENSOR", "FP8_PER_ROW", "FP8_BLOCK_128x128",
     "FP8_GROUP_1x128", "SCALE_COMPUTE", "SCALE_GIVEN", "qz_workspace_size", "qz_status_string",
-    "qz_device_error", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
+    "qz_device_error", "qz_selftest_bounded_wait", "qz_quantize_fp8", "qz_quantize_mxfp4", "qz_quantize_nvfp4",
     "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
     "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_nvfp4_noalloc", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
     "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
@@ -59,6 +59,7 @@ _SIGS = {
     "qz_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
     "qz_status_string": (ctypes.c_char_p, [_I]),
     "qz_device_error": (_I, []),
+    "qz_selftest_bounded_wait": (_I, [ctypes.c_uint32, _P]),
     "qz_quantize_fp8": (_I, [_P, _I, _I64, _I64, _I64, _I, _P, _P, _P, _P, _SZ, _P]),
     "qz_quantize_mxfp4": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "qz_quantize_nvfp4": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -166,6 +167,12 @@ def qz_status_string(status: int) -> str:
 
 def qz_device_error() -> int:
     return int(lib.qz_device_error())
+
+
+def qz_selftest_bounded_wait(polls: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that nothing completes gives up after
+    `polls` polls and records QZ_ERR_TIMEOUT); read the result with qz_device_error()."""
+    _check(lib.qz_selftest_bounded_wait(int(polls), _stream(stream)), "qz_selftest_bounded_wait")
 
 
 class Workspace:

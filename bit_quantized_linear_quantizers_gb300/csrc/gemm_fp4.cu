@@ -312,16 +312,8 @@ bool fill_problem(Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA, const float
 }
 
 qz_status launch_table(bool nv, const Fp4Params& P, cudaStream_t st) {
-    static int attr_set[64][2];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
     const void* fn = nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
-    if (!attr_set[dev][nv]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-            return QZ_ERR_CUDA;
-        attr_set[dev][nv] = 1;
-    }
+    QZ_TRY(opt_in_smem(fn, SMEM_BYTES));
     const int grid = std::min(P.total_tiles, num_sms());
     if (nv)
         fp4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(P);

@@ -226,16 +226,7 @@ qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_
     CUtensorMap ta, tb;
     if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM)) return QZ_ERR_CUDA;
     if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN)) return QZ_ERR_CUDA;
-    static int attr_set[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(fp8_block_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-            return QZ_ERR_CUDA;
-        attr_set[dev] = 1;
-    }
+    QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel, SMEM_BYTES));
     const int tiles = (M / BM) * (N / BN);
     fp8_block_gemm_kernel<<<std::min(tiles, num_sms()), THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, M, N, K);
     return launch_status();

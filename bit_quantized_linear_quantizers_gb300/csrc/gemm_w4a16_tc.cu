@@ -306,16 +306,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
 template <int MT>
 qz_status launch_tc(const TcParams& P, cudaStream_t st) {
     using L = TcLayout<MT>;
-    static int attr_set[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return QZ_ERR_UNSUPPORTED;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(w4a16_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
-            cudaSuccess)
-            return QZ_ERR_CUDA;
-        attr_set[dev] = 1;
-    }
+    QZ_TRY(opt_in_smem((const void*)w4a16_tc_kernel<MT>, L::SMEM));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(P.total_tiles, num_sms()));
     cfg.blockDim = dim3(THREADS);

@@ -49,10 +49,34 @@ qz_status device_check() {
     return g_arch_ok[d] == 1 ? QZ_OK : QZ_ERR_UNSUPPORTED;
 }
 
+// Bounded-wait self-test: one CTA waits on an mbarrier that nothing ever
+// completes, with the same bounded wait every GEMM kernel uses but a short
+// limit, so the wait runs out, records QZ_ERR_TIMEOUT in this word and the
+// kernel returns normally.
+__device__ unsigned int g_selftest_err;
+
+__global__ void selftest_wait_kernel(uint32_t polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_n(smem_u32(&bar), 0, &g_selftest_err, polls);
+}
+
+qz_status selftest_error_read_and_clear() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_selftest_err, sizeof(v)) != cudaSuccess) return QZ_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_selftest_err, &z, sizeof(z)) != cudaSuccess) return QZ_ERR_CUDA;
+    return v ? QZ_ERR_TIMEOUT : QZ_OK;
+}
+
 qz_status device_error_read_and_clear() {
     // read and clear every word, report the first error found
-    const qz_status s[4] = {w4a16_error_read_and_clear(), w4a16_tc_error_read_and_clear(),
-                            fp8_block_error_read_and_clear(), fp4_error_read_and_clear()};
+    const qz_status s[5] = {w4a16_error_read_and_clear(), w4a16_tc_error_read_and_clear(),
+                            fp8_block_error_read_and_clear(), fp4_error_read_and_clear(),
+                            selftest_error_read_and_clear()};
     for (qz_status v : s)
         if (v != QZ_OK) return v;
     return QZ_OK;
@@ -63,6 +87,35 @@ qz_status launch_status() {
 }
 
 bool is_aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`. One lock covers every kernel and device, so concurrent host
+// threads neither race on the record nor lower a limit another thread raised.
+qz_status opt_in_smem(const void* fn, int bytes) {
+    struct Entry { const void* fn; int dev; int bytes; };
+    static Entry done[256];
+    static int ndone = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QZ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    Entry* e = nullptr;
+    for (int i = 0; i < ndone; i++)
+        if (done[i].fn == fn && done[i].dev == dev) e = &done[i];
+    if (e && e->bytes >= bytes) return QZ_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return QZ_ERR_CUDA;
+    }
+    if (!e) {
+        if (ndone == 256) return QZ_OK;          // record full: the attribute is set, just not cached
+        e = &done[ndone++];
+        e->fn = fn;
+        e->dev = dev;
+    }
+    e->bytes = bytes;
+    return QZ_OK;
+}
 
 } // namespace qz
 
@@ -109,6 +162,13 @@ size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2) {
 }
 
 qz_status qz_device_error(void) { return device_error_read_and_clear(); }
+
+qz_status qz_selftest_bounded_wait(uint32_t polls, void* stream) {
+    if (polls < 1 || polls > (1u << 20)) return QZ_ERR_INVALID_ARG;
+    QZ_TRY(device_check());
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(polls);
+    return launch_status();
+}
 
 qz_status qz_quantize_fp8(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
                           qz_fp8_gran gran, uint8_t* codes, float* scales, float* dequant,

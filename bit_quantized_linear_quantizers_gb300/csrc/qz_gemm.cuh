@@ -37,6 +37,7 @@ qz_status w4a16_tc_error_read_and_clear();
 qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st);
 qz_status fp8_block_error_read_and_clear();
 qz_status fp4_error_read_and_clear();
+qz_status selftest_error_read_and_clear();
 qz_status device_error_read_and_clear();
 qz_status device_check();
 
@@ -89,13 +90,20 @@ __device__ __forceinline__ bool mbar_try_wait_default(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// Waits for phase `parity` of the mbarrier; false (and *err set) on timeout.
+// Waits for phase `parity` of the mbarrier for at most `limit` polls; false (and
+// *err set to QZ_ERR_TIMEOUT) when the limit runs out.
 template <bool HINT = true>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
-    for (uint32_t i = 0; i < kWaitLimit; i++)
+__device__ __forceinline__ bool mbar_wait_n(uint32_t bar, uint32_t parity, unsigned int* err, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; i++)
         if (HINT ? mbar_try_wait(bar, parity) : mbar_try_wait_default(bar, parity)) return true;
     atomicExch(err, (unsigned int)QZ_ERR_TIMEOUT);
     return false;
+}
+
+// Waits for phase `parity` of the mbarrier; false (and *err set) on timeout.
+template <bool HINT = true>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+    return mbar_wait_n<HINT>(bar, parity, err, kWaitLimit);
 }
 
 // 1-D bulk copy global -> shared through the TMA unit, completing on `bar`.

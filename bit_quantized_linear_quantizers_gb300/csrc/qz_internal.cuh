@@ -166,6 +166,7 @@ __device__ __forceinline__ float warp_max(float v, int width) {
 int num_sms();                         // SM count of the current device (cached)
 qz_status launch_status();             // cudaGetLastError -> qz_status
 bool is_aligned(const void* p, size_t a);
+qz_status opt_in_smem(const void* fn, int bytes);   // thread-safe dynamic shared-memory opt-in
 
 } // namespace qz
 

@@ -89,6 +89,16 @@ const char* qz_status_string(qz_status s);
  * Synchronises with the legacy default stream. */
 qz_status qz_device_error(void);
 
+/* Self-test of the failure detection (the pages have no counterpart; this is
+ * a property of this library's kernels). Launches one CTA on `stream` that
+ * waits on an mbarrier nothing ever completes, using the same bounded wait as
+ * every GEMM kernel but giving up after `polls` polls (1 <= polls <= 2^20,
+ * each poll suspends for at most tens of nanoseconds). The wait runs out,
+ * records QZ_ERR_TIMEOUT in the device error word and the kernel returns, so
+ * the next qz_device_error() reports QZ_ERR_TIMEOUT and the CUDA context stays
+ * usable. Returns QZ_ERR_INVALID_ARG for polls out of range. */
+qz_status qz_selftest_bounded_wait(uint32_t polls, void* stream);
+
 /* ------------------------------------------------------------ quantizers */
 
 /* FP8 E4M3 quantization of x[rows, cols] (leading dim ldx >= cols) at one of

@@ -288,8 +288,3 @@ def gemm_mxfp4(qA, eA, qB, eB, ii=None, jj=None):
     N = qB.shape[0]
     return _run_gemm(_load().or_gemm_mxfp4, (_ptr(qA), _ptr(eA), _ptr(qB), _ptr(eB), M, N, K),
                      M, N, ii, jj, ii is None)
-
-
-def gemm_ok(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, rel: float = 1e-3) -> np.ndarray:
-    """Acceptance of a GEMM output: |y_gpu - y_ref| <= rel * sum_k |a*b|."""
-    return np.abs(y_gpu.astype(np.float64) - y_ref) <= rel * bound

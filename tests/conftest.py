@@ -42,3 +42,22 @@ def read_golden(name: str):
             if line:
                 rows.append(line.split())
     return rows
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Report how many GEMM output elements passed only because of the half-bf16-ulp
+    term of the tolerance (the rest are within 1e-3 * sum |a*b| alone)."""
+    try:
+        from gpu_util import HALF_ULP_TALLY
+    except Exception:  # pragma: no cover
+        return
+    if not HALF_ULP_TALLY:
+        return
+    total = sum(n for _, n, _ in HALF_ULP_TALLY)
+    extra = sum(h for _, _, h in HALF_ULP_TALLY)
+    terminalreporter.write_sep("-", "GEMM tolerance audit")
+    terminalreporter.write_line(f"{len(HALF_ULP_TALLY)} GEMM checks, {total} elements; {extra} pass only through "
+                                f"the half-bf16-ulp term of the tolerance")
+    for what, n, h in HALF_ULP_TALLY:
+        if h:
+            terminalreporter.write_line(f"  {what}: {h} of {n}")

@@ -56,3 +56,22 @@ def gemm_tolerance(y_ref: np.ndarray, bound: np.ndarray, rel: float = 1e-3) -> n
     exact result (the rounding of the output to bf16, which alone exceeds the first
     term wherever |y| approaches sum_k |a*b|)."""
     return rel * np.asarray(bound, np.float64) + half_ulp_bf16(y_ref)
+
+
+# Audit of the half-ulp term: per GEMM check, how many elements pass only because of it
+# (|y - y_ref| above rel * sum|ab| but within the full tolerance). Printed in the pytest
+# terminal summary, so every GPU run records how much the output-rounding term is used.
+HALF_ULP_TALLY = []        # (what, elements checked, elements passing only through the half ulp)
+
+
+def check_gemm(y_bits: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what: str, rel: float = 1e-3):
+    """Assert a bf16 GEMM output against the FP64 reference: every element within
+    rel * sum_k |a*b| + half a bf16 ulp of the exact value; tally the elements that
+    need the half-ulp term."""
+    y = bf16_bits_to_f64(y_bits)
+    err = np.abs(y - np.asarray(y_ref, np.float64))
+    strict = err <= rel * np.asarray(bound, np.float64)
+    ok = err <= gemm_tolerance(y_ref, bound, rel)
+    HALF_ULP_TALLY.append((what, int(ok.size), int(np.count_nonzero(ok & ~strict))))
+    bad = np.argwhere(~ok)
+    assert ok.all(), f"{what}: {len(bad)} outside {rel}*sum|ab| + half a bf16 ulp; first {bad[:3].tolist()}"

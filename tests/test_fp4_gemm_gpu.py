@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synthetic as syn
-from gpu_util import bf16_bits_to_f64, gemm_tolerance, host
+from gpu_util import bf16_bits_to_f64, check_gemm, host
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +27,7 @@ def dev(x):
 
 
 def check(y_bits, y_ref, bound, what):
-    y = bf16_bits_to_f64(y_bits)
-    ok = np.abs(y - y_ref) <= gemm_tolerance(y_ref, bound, REL)
-    bad = np.argwhere(~ok)
-    assert ok.all(), f"{what}: {len(bad)} outside 1e-3*sum|ab| + half a bf16 ulp; first {bad[:3].tolist()}"
+    check_gemm(y_bits, y_ref, bound, what, REL)
 
 
 def inputs(M, N, K, seed):

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synthetic as syn
-from gpu_util import bf16_bits_to_f64, gemm_tolerance, dev_bf16, host
+from gpu_util import bf16_bits_to_f64, check_gemm, dev_bf16, host
 
 import torch
 
@@ -41,10 +41,7 @@ def activations(M, K, seed):
 
 
 def check(y_gpu_bits, y_ref, bound, what):
-    y = bf16_bits_to_f64(y_gpu_bits)
-    ok = np.abs(y - y_ref) <= gemm_tolerance(y_ref, bound, REL)
-    bad = np.argwhere(~ok)
-    assert ok.all(), f"{what}: {len(bad)} outside 1e-3*sum|ab| + half a bf16 ulp, first {bad[:3].tolist()}"
+    check_gemm(y_gpu_bits, y_ref, bound, what, REL)
 
 
 def run(qz, A, qw, sc):

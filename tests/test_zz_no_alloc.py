@@ -6,10 +6,12 @@ allocator, or latency-critical loops that cannot risk cudaMalloc synchronising
 the device. Its scratch is a fixed array inside the library, shared by every
 call. This test checks, on two calls in a row with different problems (so the
 second call sees the first call's leftovers in that array), that each result
-matches the workspace entry point qz_gemm_nvfp4 within the GEMM tolerance the
-other tests use, and that a problem too large for the fixed array is rejected
-with QZ_ERR_SHAPE before anything is launched. It runs last (file name) and
-also passes on its own in a fresh process.
+equals the workspace entry point qz_gemm_nvfp4 bit for bit (the same kernels
+run on the same operands, so any difference would mean stale scratch was read)
+and lies within the GEMM tolerance the other tests use; that the Python wrapper
+of the same name gives the same bits; and that a problem too large for the
+fixed array is rejected with QZ_ERR_SHAPE before anything is launched. It runs
+last (file name) and also passes on its own in a fresh process.
 """
 import ctypes
 
@@ -56,11 +58,12 @@ def test_nvfp4_noalloc_matches_workspace_entry_point():
         rc = lib.qz_gemm_nvfp4_noalloc(*[_p(t) for t in d], _p(y_noalloc), M, N, K, stream)
         assert rc == 0, qz.qz_status_string(rc)
         y_ws = qz.qz_gemm_nvfp4(*d)                       # the workspace entry point
+        y_py = qz.qz_gemm_nvfp4_noalloc(*d)               # the Python wrapper of the C call
         torch.cuda.synchronize()
+        assert np.array_equal(host(y_noalloc), host(y_ws)), f"call {call}: differs from qz_gemm_nvfp4"
+        assert np.array_equal(host(y_py), host(y_ws)), f"call {call}: the wrapper differs from qz_gemm_nvfp4"
         y_ref, bound = oracle.gemm_nvfp4(ca, sa, ga, cb, sb, gb)
         a = bf16_bits_to_f64(host(y_noalloc))
-        b = bf16_bits_to_f64(host(y_ws))
-        assert np.all(np.abs(a - b) <= gemm_tolerance(y_ref, bound)), f"call {call}: differs from qz_gemm_nvfp4"
         assert np.all(np.abs(a - y_ref) <= gemm_tolerance(y_ref, bound)), f"call {call}: outside the GEMM tolerance"
 
 
