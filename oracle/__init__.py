@@ -66,6 +66,17 @@ def _load():
             "or_gemm_fp8_block": (None, [P, P, P, P, I64, I64, I64, P, P, I64, P, P]),
             "or_gemm_nvfp4": (None, [P, P, F, P, P, F, I64, I64, I64, P, P, I64, P, P]),
             "or_gemm_mxfp4": (None, [P, P, P, P, I64, I64, I64, P, P, I64, P, P]),
+            "or_kv_write_fp8_per_head": (None, [P, P, I64, I64, P, P, P, P, P, P]),
+            "or_kv_fp8_per_head_given": (None, [P, I64, I64, P, P, P]),
+            "or_kv_k_channel_zp": (None, [P, I64, I64, I64, P, P, P, P]),
+            "or_quant_int4_g128_zp": (I, [P, I, I64, I64, I64, P, P, P, P]),
+            "or_gemm_w4a16_zp": (None, [P, P, P, P, I64, I64, I64, P, P, I64, P, P]),
+            "or_gemm_w4a16_nvfp4": (None, [P, P, P, F, I64, I64, I64, P, P, I64, P, P]),
+            "or_gemm_w4a16_mxfp4": (None, [P, P, P, I64, I64, I64, P, P, I64, P, P]),
+            "or_col_amax": (None, [P, I, I64, I64, P]),
+            "or_smooth_factors": (None, [P, P, I64, P]),
+            "or_quant_int8_rows": (I, [P, I, I64, I64, P, I, P, P, P]),
+            "or_gemm_int8": (None, [P, P, P, P, I64, I64, I64, P, P, I64, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -288,3 +299,142 @@ def gemm_mxfp4(qA, eA, qB, eB, ii=None, jj=None):
     N = qB.shape[0]
     return _run_gemm(_load().or_gemm_mxfp4, (_ptr(qA), _ptr(eA), _ptr(qB), _ptr(eB), M, N, K),
                      M, N, ii, jj, ii is None)
+
+
+
+# ------------------------------------------------------------ next rows
+
+def kv_write_fp8_per_head(k: np.ndarray, v: np.ndarray, want_deq: bool = False):
+    """FP8 KV write with one scale per (batch, head) of bf16 bit arrays [B, H, T, D].
+    Returns (k_codes, v_codes, k_scales [B, H], v_scales [B, H], k_deq, v_deq)."""
+    assert k.dtype == np.uint16 and v.dtype == np.uint16 and k.shape == v.shape and k.ndim == 4
+    B, H, T, D = k.shape
+    k1, v1 = np.ascontiguousarray(k), np.ascontiguousarray(v)
+    kc, vc = np.empty(k.shape, np.uint8), np.empty(k.shape, np.uint8)
+    ks, vs = np.empty((B, H), np.float32), np.empty((B, H), np.float32)
+    kd = np.empty(k.shape, np.float32) if want_deq else None
+    vd = np.empty(k.shape, np.float32) if want_deq else None
+    _load().or_kv_write_fp8_per_head(_ptr(k1), _ptr(v1), B * H, T * D, _ptr(kc), _ptr(vc), _ptr(ks),
+                                     _ptr(vs), _ptr(kd), _ptr(vd))
+    return kc, vc, ks, vs, kd, vd
+
+
+def kv_fp8_per_head_given(x: np.ndarray, scales: np.ndarray, want_deq: bool = False):
+    """Per-head FP8 codes of bf16 bits [B, H, T, D] with given scales [B, H]."""
+    assert x.dtype == np.uint16 and x.ndim == 4
+    B, H, T, D = x.shape
+    x1 = np.ascontiguousarray(x)
+    sc = np.ascontiguousarray(scales, np.float32).reshape(B * H)
+    codes = np.empty(x.shape, np.uint8)
+    deq = np.empty(x.shape, np.float32) if want_deq else None
+    _load().or_kv_fp8_per_head_given(_ptr(x1), B * H, T * D, _ptr(sc), _ptr(codes), _ptr(deq))
+    return codes, deq
+
+
+def kv_k_channel_zp(k: np.ndarray, want_deq: bool = False):
+    """K per channel with a zero point (FP8 residual) of bf16 bits [B, H, T, D].
+    Returns (codes [B, H, T, D], scale [B, H, D], zero [B, H, D], deq|None)."""
+    assert k.dtype == np.uint16 and k.ndim == 4
+    B, H, T, D = k.shape
+    k1 = np.ascontiguousarray(k)
+    codes = np.empty(k.shape, np.uint8)
+    sc, zp = np.empty((B, H, D), np.float32), np.empty((B, H, D), np.float32)
+    deq = np.empty(k.shape, np.float32) if want_deq else None
+    _load().or_kv_k_channel_zp(_ptr(k1), B * H, T, D, _ptr(codes), _ptr(sc), _ptr(zp), _ptr(deq))
+    return codes, sc, zp, deq
+
+
+def quant_int4_g128_zp(w: np.ndarray, want_deq: bool = True):
+    """Asymmetric INT4 g128 of a [K, N] weight. Returns (qweight i32 [K/8, N] (codes
+    0..15), scale bf16 bits [K/128, N], zero u8 [K/128, N], deq f32 [K, N]|None)."""
+    w2, bf = _src(w)
+    K, N = w2.shape
+    qw = np.empty((K // 8, N), np.int32)
+    sc = np.empty((K // 128, N), np.uint16)
+    zp = np.empty((K // 128, N), np.uint8)
+    deq = np.empty((K, N), np.float32) if want_deq else None
+    rc = _load().or_quant_int4_g128_zp(_ptr(w2), bf, K, N, N, _ptr(qw), _ptr(sc), _ptr(zp), _ptr(deq))
+    if rc != 0:
+        raise ValueError(f"oracle rejects shape {w2.shape} for INT4 g128 with zero points")
+    return qw, sc, zp, deq
+
+
+def gemm_w4a16_zp(A_bf16, qweight, scale_bf16, zero, ii=None, jj=None):
+    A = np.ascontiguousarray(A_bf16, dtype=np.uint16)
+    qw = np.ascontiguousarray(qweight, dtype=np.int32)
+    sc = np.ascontiguousarray(scale_bf16, dtype=np.uint16)
+    zp = np.ascontiguousarray(zero, dtype=np.uint8)
+    M, K = A.shape
+    N = qw.shape[1]
+    return _run_gemm(_load().or_gemm_w4a16_zp, (_ptr(A), _ptr(qw), _ptr(sc), _ptr(zp), M, N, K), M, N,
+                     ii, jj, ii is None)
+
+
+def gemm_w4a16_nvfp4(A_bf16, qB, sB, gB, ii=None, jj=None):
+    """Weight-only NVFP4: bf16 A [M, K] times B^T [N, K] given as NVFP4 codes and scales."""
+    A = np.ascontiguousarray(A_bf16, dtype=np.uint16)
+    qB, sB = np.ascontiguousarray(qB, np.uint8), np.ascontiguousarray(sB, np.uint8)
+    M, K = A.shape
+    N = qB.shape[0]
+    return _run_gemm(_load().or_gemm_w4a16_nvfp4, (_ptr(A), _ptr(qB), _ptr(sB), float(gB), M, N, K), M, N,
+                     ii, jj, ii is None)
+
+
+def gemm_w4a16_mxfp4(A_bf16, qB, eB, ii=None, jj=None):
+    """Weight-only MXFP4: bf16 A [M, K] times B^T [N, K] given as MXFP4 codes and E8M0 scales."""
+    A = np.ascontiguousarray(A_bf16, dtype=np.uint16)
+    qB, eB = np.ascontiguousarray(qB, np.uint8), np.ascontiguousarray(eB, np.uint8)
+    M, K = A.shape
+    N = qB.shape[0]
+    return _run_gemm(_load().or_gemm_w4a16_mxfp4, (_ptr(A), _ptr(qB), _ptr(eB), M, N, K), M, N,
+                     ii, jj, ii is None)
+
+
+def col_amax(x: np.ndarray) -> np.ndarray:
+    """max |x| over the rows of each column of a 2-D fp32 or bf16-bits array."""
+    x2, bf = _src(x)
+    rows, cols = x2.shape
+    out = np.empty(cols, np.float32)
+    _load().or_col_amax(_ptr(x2), bf, rows, cols, _ptr(out))
+    return out
+
+
+def smooth_factors(xmax: np.ndarray, wmax: np.ndarray) -> np.ndarray:
+    """SmoothQuant migration factors with alpha = 0.5 from per-channel amaxes."""
+    xm = np.ascontiguousarray(xmax, np.float32)
+    wm = np.ascontiguousarray(wmax, np.float32)
+    assert xm.shape == wm.shape and xm.ndim == 1
+    s = np.empty(xm.size, np.float32)
+    _load().or_smooth_factors(_ptr(xm), _ptr(wm), xm.size, _ptr(s))
+    return s
+
+
+INT8_PLAIN, INT8_DIVIDE, INT8_MULTIPLY = 0, 1, 2
+
+
+def quant_int8_rows(x: np.ndarray, factors: np.ndarray | None = None, smooth: int = INT8_PLAIN,
+                    want_deq: bool = True):
+    """INT8 per row (token or output channel) after an optional per-column smoothing
+    factor (INT8_DIVIDE for activations, INT8_MULTIPLY for weights as B^T).
+    Returns (codes i8 [R, C], scales f32 [R], deq f32|None)."""
+    x2, bf = _src(x)
+    rows, cols = x2.shape
+    f = None if factors is None else np.ascontiguousarray(factors, np.float32)
+    codes = np.empty((rows, cols), np.int8)
+    scales = np.empty(rows, np.float32)
+    deq = np.empty((rows, cols), np.float32) if want_deq else None
+    rc = _load().or_quant_int8_rows(_ptr(x2), bf, rows, cols, _ptr(f), int(smooth), _ptr(codes), _ptr(scales),
+                                    _ptr(deq))
+    if rc != 0:
+        raise ValueError("oracle rejects the INT8 arguments")
+    return codes, scales, deq
+
+
+def gemm_int8(qA, sA, qB, sB, ii=None, jj=None):
+    """y, bound of Y = diag(sA) (qA qB^T) diag(sB) with int8 qA [M, K], qB [N, K]."""
+    qA, qB = np.ascontiguousarray(qA, np.int8), np.ascontiguousarray(qB, np.int8)
+    sA, sB = np.ascontiguousarray(sA, np.float32), np.ascontiguousarray(sB, np.float32)
+    M, K = qA.shape
+    N = qB.shape[0]
+    return _run_gemm(_load().or_gemm_int8, (_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), M, N, K), M, N, ii, jj,
+                     ii is None)

@@ -41,6 +41,41 @@
  *    rint = round half to even (torch.round). Divisor 7 = 2^(b-1) - 1, the
  *    INT8 "amax / 127" rule of [P2] carried to 4 bits.
  *  - GEMMs: y = sum over k of the exactly dequantized operands, in double.
+ *
+ * The variants of the "next" rows, with their readings:
+ *  - FP8 KV per head [P1 KV Cache 量化, per_head]: one scale per (batch, head)
+ *    over that head's T x D values, otherwise the per-tensor FP8 steps.
+ *  - K per channel with a zero point [P1 KV Cache 量化: K as "a constant bias
+ *    per channel plus a small variation"; per channel, with a zero point that
+ *    absorbs the bias; P3 5.1: asymmetric quantization adds a zero point z].
+ *    The cache stays FP8, so the zero point lives in value space: per channel
+ *    (b, h, d) over the T tokens, z = fl(0.5 * fl(max + min)) (the midpoint of
+ *    the channel's range, so the residual is symmetric), r = fl(x - z),
+ *    s = max(max|r|, 1e-12) / 448, code = E4M3(clamp(fl(r / s), +-448)),
+ *    dequant = fl(fl(v * s) + z). V is quantized per token (one scale per
+ *    (b, h, t) over D), the partner of per-channel K in the KIVI split the
+ *    pages cite.
+ *  - INT4 with a zero point [P1 格式速查 W4A16 row "+ 零点"; P3 5.1
+ *    q = clamp(round(x / s) + z, ...)]: unsigned codes 0..15 per group of 128
+ *    along K; the range is widened to include 0 (lo = min(min, 0),
+ *    hi = max(max, 0)), s = bf16(max(hi - lo, 1e-12) / 15),
+ *    z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(x / s) + z, 0, 15),
+ *    dequant = (q - z) * s.
+ *  - Weight-only FP4 (W4A16 MXFP4 / NVFP4) [P1 精度比较]: bf16 activations
+ *    times weights dequantized exactly from their E2M1 codes and scales.
+ *  - SmoothQuant [P2 路线二]: s_j = max|X_j|^a / max|W_j|^(1-a) with a = 0.5,
+ *    each amax floored at 1e-12 like every other amax here, computed as
+ *    fl(fl(sqrt(ax)) / fl(sqrt(aw))). X' = X / s (per input channel),
+ *    W' = W * s.
+ *  - INT8 per token / per output channel [P1 格式速查 W8A8 INT8 row, integers
+ *    -128..127; P2 量化在做什么: symmetric s = amax / 127]:
+ *    s = max(amax_row, 1e-12) / 127, q = clamp(rint(x / s), -128, 127).
+ *  - INT8 GEMM: y = sA[i] * sB[j] * sum_k qA[i,k] qB[j,k]; the integer sum is
+ *    exact (int64).
+ *  - Fused FP8 1x128 output quantization [P1 练习 2: the activation's (1, 128)
+ *    scales are computed at the end of the previous kernel]: the producer's
+ *    output rounded to bf16 (what the producer would have stored), then the
+ *    1x128 FP8 steps of or_quant_fp8; the tests compose the two.
  */
 #include <math.h>
 #include <stdint.h>
@@ -487,5 +522,268 @@ void or_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, cons
         }
         y[p] = acc;
         bound[p] = mag;
+    }
+}
+
+/* ----------------------------------------------------- FP8 KV variants */
+
+/* FP8 KV write with one scale per (batch, head) [P1 KV Cache 量化, per_head:
+ * amax over the last two dims (T, D)]. k, v: bf16 [B*H][T*D]. Scales
+ * [B*H] each. Each head's slice is quantized by the per-tensor FP8 steps. */
+void or_kv_write_fp8_per_head(const uint16_t* k, const uint16_t* v, int64_t BH, int64_t TD,
+                              uint8_t* k_codes, uint8_t* v_codes, float* k_scale, float* v_scale,
+                              float* k_deq, float* v_deq)
+{
+    for (int64_t h = 0; h < BH; h++) {
+        or_quant_fp8(k + h * TD, 1, 1, TD, TD, OR_TENSOR, k_codes + h * TD, k_scale + h,
+                     k_deq ? k_deq + h * TD : NULL);
+        or_quant_fp8(v + h * TD, 1, 1, TD, TD, OR_TENSOR, v_codes + h * TD, v_scale + h,
+                     v_deq ? v_deq + h * TD : NULL);
+    }
+}
+
+/* Per-head FP8 with caller-given scales (calibrated, [P1 KV Cache 量化,
+ * 实际部署时]): x bf16 [BH][TD], scale[BH]. */
+void or_kv_fp8_per_head_given(const uint16_t* x, int64_t BH, int64_t TD, const float* scale,
+                              uint8_t* codes, float* deq)
+{
+    for (int64_t h = 0; h < BH; h++)
+        or_quant_fp8_given(x + h * TD, 1, TD, scale[h], codes + h * TD, deq ? deq + h * TD : NULL);
+}
+
+/* K per channel with a zero point (FP8 residual), over the T tokens of each
+ * channel (b, h, d) of k bf16 [BH][T][D]:
+ *   z = fl(0.5 * fl(max + min));  r = fl(x - z)
+ *   s = max(max_t |r|, 1e-12) / 448;  code = E4M3(clamp(fl(r / s), +-448))
+ *   dequant = fl(fl(E4M3value(code) * s) + z)
+ * scale, zero: [BH][D]. */
+void or_kv_k_channel_zp(const uint16_t* k, int64_t BH, int64_t T, int64_t D,
+                        uint8_t* codes, float* scale, float* zero, float* deq)
+{
+    for (int64_t h = 0; h < BH; h++) {
+        const uint16_t* x = k + h * T * D;
+        for (int64_t d = 0; d < D; d++) {
+            float mn = or_bf16_to_f32(x[d]), mx = mn;
+            for (int64_t t = 1; t < T; t++) {
+                float a = or_bf16_to_f32(x[t * D + d]);
+                if (a < mn) mn = a;
+                if (a > mx) mx = a;
+            }
+            float z = 0.5f * (mx + mn);
+            float ramax = 0.0f;
+            for (int64_t t = 0; t < T; t++) {
+                float r = fabsf(or_bf16_to_f32(x[t * D + d]) - z);
+                if (r > ramax) ramax = r;
+            }
+            float s = (ramax > or_amax_min() ? ramax : or_amax_min()) / OR_FP8_MAX;
+            scale[h * D + d] = s;
+            zero[h * D + d] = z;
+            for (int64_t t = 0; t < T; t++) {
+                float r = or_bf16_to_f32(x[t * D + d]) - z;
+                float dq;
+                codes[h * T * D + t * D + d] = or_fp8_one(r, s, &dq);
+                if (deq) deq[h * T * D + t * D + d] = dq + z;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------- INT4 with a zero point */
+
+/* INT4, unsigned codes 0..15, one bf16 scale and one integer zero point per
+ * group of 128 along K, of a row-major weight w[K][N] [P1 格式速查 W4A16
+ * "+ 零点"; P3 5.1 asymmetric]:
+ *   lo = min(min_group, 0), hi = max(max_group, 0)
+ *   s = bf16(max(hi - lo, 1e-12) / 15);  z = clamp(rint(-lo / s), 0, 15)
+ *   q = clamp(rint(w / s) + z, 0, 15);    dequant = (q - z) * s
+ * qweight[K/8][N] int32: element k in bits 4*(k%8)..+3 (unsigned).
+ * scale[K/128][N] bf16 bits; zero[K/128][N] bytes. */
+int or_quant_int4_g128_zp(const void* w, int is_bf16, int64_t K, int64_t N, int64_t ldw,
+                          int32_t* qweight, uint16_t* scale, uint8_t* zero, float* deq)
+{
+    if (K <= 0 || N <= 0 || K % 128) return -1;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t g = 0; g < K / 128; g++) {
+            float lo = 0.0f, hi = 0.0f;
+            for (int64_t k = g * 128; k < g * 128 + 128; k++) {
+                float a = or_elem(w, is_bf16, k * ldw + n);
+                if (a < lo) lo = a;
+                if (a > hi) hi = a;
+            }
+            float range = hi - lo;
+            float sf = (range > or_amax_min() ? range : or_amax_min()) / 15.0f;
+            uint16_t sbits = or_f32_to_bf16(sf);
+            float sq = or_bf16_to_f32(sbits);
+            float zr = rintf(-lo / sq);
+            if (zr < 0.0f) zr = 0.0f;
+            if (zr > 15.0f) zr = 15.0f;
+            int z = (int)zr;
+            scale[g * N + n] = sbits;
+            zero[g * N + n] = (uint8_t)z;
+            for (int64_t k = g * 128; k < g * 128 + 128; k++) {
+                float y = or_elem(w, is_bf16, k * ldw + n) / sq;
+                float r = rintf(y) + (float)z;
+                if (r < 0.0f) r = 0.0f;
+                if (r > 15.0f) r = 15.0f;
+                int q = (int)r;
+                uint32_t* p = (uint32_t*)&qweight[(k / 8) * N + n];
+                if (k % 8 == 0) *p = 0;
+                *p |= ((uint32_t)q & 0xFu) << (4 * (int)(k % 8));
+                if (deq) deq[k * N + n] = (float)(q - z) * sq;
+            }
+        }
+    }
+    return 0;
+}
+
+/* W4A16 with a zero point: b = (q[k,j] - z[k/128, j]) * s[k/128, j]. */
+void or_gemm_w4a16_zp(const uint16_t* A, const int32_t* qweight, const uint16_t* scale,
+                      const uint8_t* zero, int64_t M, int64_t N, int64_t K, const int64_t* ii,
+                      const int64_t* jj, int64_t npts, double* y, double* bound)
+{
+    (void)M;
+    for (int64_t p = 0; p < npts; p++) {
+        int64_t i = ii[p], j = jj[p];
+        double acc = 0.0, mag = 0.0;
+        const uint16_t* arow = A + i * K;
+        for (int64_t k = 0; k < K; ++k) {
+            uint32_t word = (uint32_t)qweight[(k / 8) * N + j];
+            int q = (int)((word >> (4 * (k % 8))) & 0xF);
+            int z = zero[(k / 128) * N + j];
+            double b = (double)(q - z) * (double)or_bf16_to_f32(scale[(k >> 7) * N + j]);
+            double a = (double)or_bf16_to_f32(arow[k]);
+            acc += a * b;
+            mag += fabs(a * b);
+        }
+        y[p] = acc;
+        bound[p] = mag;
+    }
+}
+
+/* ------------------------------------------- weight-only FP4 (W4A16 FP4) */
+
+/* a = A[i,k] (bf16); b = e2m1(qB[j,k]) * e4m3(sB[j, k/16]) * gB, B^T [N, K]. */
+void or_gemm_w4a16_nvfp4(const uint16_t* A, const uint8_t* qB, const uint8_t* sB, float gB,
+                         int64_t M, int64_t N, int64_t K, const int64_t* ii, const int64_t* jj,
+                         int64_t npts, double* y, double* bound)
+{
+    (void)M; (void)N;
+    for (int64_t p = 0; p < npts; p++) {
+        int64_t i = ii[p], j = jj[p];
+        double acc = 0.0, mag = 0.0;
+        const uint16_t* arow = A + i * K;
+        const uint8_t* srow = sB + j * (K / 16);
+        for (int64_t k = 0; k < K; k++) {
+            double a = (double)or_bf16_to_f32(arow[k]);
+            double b = or_fp4_at(qB, j, K, k) * or_e4m3_decode(srow[k / 16]) * (double)gB;
+            acc += a * b;
+            mag += fabs(a * b);
+        }
+        y[p] = acc;
+        bound[p] = mag;
+    }
+}
+
+/* a = A[i,k] (bf16); b = e2m1(qB[j,k]) * 2^(eB[j, k/32] - 127). */
+void or_gemm_w4a16_mxfp4(const uint16_t* A, const uint8_t* qB, const uint8_t* eB,
+                         int64_t M, int64_t N, int64_t K, const int64_t* ii, const int64_t* jj,
+                         int64_t npts, double* y, double* bound)
+{
+    (void)M; (void)N;
+    for (int64_t p = 0; p < npts; p++) {
+        int64_t i = ii[p], j = jj[p];
+        double acc = 0.0, mag = 0.0;
+        const uint16_t* arow = A + i * K;
+        const uint8_t* erow = eB + j * (K / 32);
+        for (int64_t k = 0; k < K; k++) {
+            double a = (double)or_bf16_to_f32(arow[k]);
+            double b = ldexp(or_fp4_at(qB, j, K, k), (int)erow[k / 32] - 127);
+            acc += a * b;
+            mag += fabs(a * b);
+        }
+        y[p] = acc;
+        bound[p] = mag;
+    }
+}
+
+/* ----------------------------------------------- SmoothQuant + INT8 W8A8 */
+
+/* max |x[r, c]| over the rows r of each column c (the per-channel statistic
+ * of SmoothQuant [P2 路线二]): out[cols]. */
+void or_col_amax(const void* x, int is_bf16, int64_t rows, int64_t cols, float* out)
+{
+    for (int64_t c = 0; c < cols; c++) {
+        float m = 0.0f;
+        for (int64_t r = 0; r < rows; r++) {
+            float a = fabsf(or_elem(x, is_bf16, r * cols + c));
+            if (a > m) m = a;
+        }
+        out[c] = m;
+    }
+}
+
+/* s_j = max|X_j|^0.5 / max|W_j|^0.5 [P2 路线二, alpha = 0.5], each amax
+ * floored at 1e-12: s = fl(fl(sqrt(ax)) / fl(sqrt(aw))). */
+void or_smooth_factors(const float* xmax, const float* wmax, int64_t n, float* s)
+{
+    for (int64_t j = 0; j < n; j++) {
+        float ax = xmax[j] > or_amax_min() ? xmax[j] : or_amax_min();
+        float aw = wmax[j] > or_amax_min() ? wmax[j] : or_amax_min();
+        s[j] = sqrtf(ax) / sqrtf(aw);
+    }
+}
+
+/* INT8 per row of x[rows][cols] (tokens of an activation, or output channels
+ * of a weight stored as B^T), after the optional per-column smoothing factor:
+ *   x' = fl(x / f[c]) (smooth = 1, activations) or fl(x * f[c]) (smooth = 2,
+ *   weights); smooth = 0: x' = x.
+ *   s = max(amax_row(x'), 1e-12) / 127;  q = clamp(rint(fl(x' / s)), -128, 127)
+ * codes[rows][cols] int8, scales[rows], deq = q * s (nullable). */
+int or_quant_int8_rows(const void* x, int is_bf16, int64_t rows, int64_t cols, const float* f, int smooth,
+                       int8_t* codes, float* scales, float* deq)
+{
+    if (rows <= 0 || cols <= 0 || smooth < 0 || smooth > 2 || (smooth && !f)) return -1;
+    for (int64_t r = 0; r < rows; r++) {
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; c++) {
+            float v = or_elem(x, is_bf16, r * cols + c);
+            if (smooth == 1) v = v / f[c];
+            else if (smooth == 2) v = v * f[c];
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float s = (amax > or_amax_min() ? amax : or_amax_min()) / 127.0f;
+        scales[r] = s;
+        for (int64_t c = 0; c < cols; c++) {
+            float v = or_elem(x, is_bf16, r * cols + c);
+            if (smooth == 1) v = v / f[c];
+            else if (smooth == 2) v = v * f[c];
+            float d;
+            int q = or_int_quant_one(v, s, -128, 127, &d);
+            codes[r * cols + c] = (int8_t)q;
+            if (deq) deq[r * cols + c] = d;
+        }
+    }
+    return 0;
+}
+
+/* INT8 GEMM: y[i,j] = sA[i] * sB[j] * sum_k qA[i,k] * qB[j,k] (B^T [N, K]),
+ * the integer sum exact in int64; bound = sum_k |a * b| of the dequantized
+ * operands. */
+void or_gemm_int8(const int8_t* qA, const float* sA, const int8_t* qB, const float* sB,
+                  int64_t M, int64_t N, int64_t K, const int64_t* ii, const int64_t* jj,
+                  int64_t npts, double* y, double* bound)
+{
+    (void)M; (void)N;
+    for (int64_t p = 0; p < npts; p++) {
+        int64_t i = ii[p], j = jj[p];
+        int64_t acc = 0, mag = 0;
+        for (int64_t k = 0; k < K; k++) {
+            int64_t t = (int64_t)qA[i * K + k] * (int64_t)qB[j * K + k];
+            acc += t;
+            mag += t < 0 ? -t : t;
+        }
+        double sc = (double)sA[i] * (double)sB[j];
+        y[p] = (double)acc * sc;
+        bound[p] = (double)mag * fabs(sc);
     }
 }

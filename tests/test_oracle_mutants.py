@@ -17,7 +17,10 @@ two FP4 nibbles of a byte in the other order inside the GEMM references alone
 permutes k identically for both operands within one scale block, which leaves
 every GEMM result unchanged; the quantizers' leading dimension is always the
 column count (the wrapper passes contiguous arrays); an INT4 clamp of -7
-instead of -8 never binds, since |w / s| <= 7 (1 + 2^-8) with s = bf16(amax / 7).
+instead of -8 never binds, since |w / s| <= 7 (1 + 2^-8) with s = bf16(amax / 7);
+and in the K-per-channel zero-point function, the amax of the centred residual
+is reached at both ends of the channel's range, so leaving one extreme out of
+that amax changes nothing beyond a rounding of the midpoint.
 """
 import multiprocessing as mp
 import os
@@ -114,6 +117,50 @@ MUTANTS = {
     "int4_amax_signed": ("                float a = fabsf(or_elem(w, is_bf16, k * ldw + n));",
                          "                float a = or_elem(w, is_bf16, k * ldw + n);",
                          ["test_int4_g128_invariants"]),
+    "kvh_v_uses_k": ("or_quant_fp8(v + h * TD, 1, 1, TD, TD,", "or_quant_fp8(k + h * TD, 1, 1, TD, TD,",
+                     ["test_kv_per_head_reduces_to_per_tensor_per_head"]),
+    "kvh_head_stride_halved": ("or_quant_fp8(k + h * TD, 1, 1, TD, TD,", "or_quant_fp8(k + h * (TD / 2), 1, 1, TD, TD,",
+                               ["test_kv_per_head_reduces_to_per_tensor_per_head"]),
+    "kvh_given_scale_of_head_0": ("scale[h], codes + h * TD", "scale[0], codes + h * TD",
+                                  ["test_kv_per_head_given_matches_per_tensor_given"]),
+    "kzp_zero_is_min": ("            float z = 0.5f * (mx + mn);", "            float z = mn;",
+                        ["test_k_channel_zero_point_extremes_map_to_full_range"]),
+    "kzp_zero_half_missing": ("            float z = 0.5f * (mx + mn);", "            float z = (mx + mn);",
+                              ["test_k_channel_zero_point_extremes_map_to_full_range",
+                               "test_k_channel_zero_point_is_translation_invariant"]),
+    "kzp_deq_drops_zero": ("if (deq) deq[h * T * D + t * D + d] = dq + z;", "if (deq) deq[h * T * D + t * D + d] = dq;",
+                           ["test_k_channel_zero_point_error_tracks_the_variation"]),
+    "kzp_scale_divisor_447": ("/ OR_FP8_MAX;\n            scale[h * D + d] = s;", "/ 447.0f;\n            scale[h * D + d] = s;",
+                              ["test_k_channel_zero_point_unit_scale_reduces_to_plain_cast"]),
+    "i4zp_no_zero_inclusion": ("            float lo = 0.0f, hi = 0.0f;", "            float lo = 1e30f, hi = -1e30f;",
+                               ["test_int4_zp_invariants"]),
+    "i4zp_divisor_16": ("/ 15.0f;", "/ 16.0f;", ["test_int4_zp_worked_example"]),
+    "i4zp_zero_sign": ("float zr = rintf(-lo / sq);", "float zr = rintf(lo / sq);",
+                       ["test_int4_zp_worked_example", "test_int4_zp_invariants"]),
+    "i4zp_zero_added_twice": ("float r = rintf(y) + (float)z;", "float r = rintf(y) + (float)(2 * z);",
+                              ["test_int4_zp_worked_example", "test_int4_zp_invariants"]),
+    "i4zp_gemm_ignores_zero": ("double b = (double)(q - z) *", "double b = (double)q *",
+                               ["test_gemm_w4a16_zp_integer_case_is_exact_matmul"]),
+    "i4zp_gemm_zero_per_row": ("int z = zero[(k / 128) * N + j];", "int z = zero[(j % (K / 128)) * N + j];",
+                               ["test_gemm_w4a16_zp_integer_case_is_exact_matmul"]),
+    "w4nv_drops_gB": ("or_e4m3_decode(srow[k / 16]) * (double)gB;", "or_e4m3_decode(srow[k / 16]);",
+                      ["test_gemm_w4a16_fp4_equals_matmul_of_decoded_weights"]),
+    "w4mx_bias": ("(int)erow[k / 32] - 127", "(int)erow[k / 32] - 126",
+                  ["test_gemm_w4a16_fp4_equals_matmul_of_decoded_weights"]),
+    "col_amax_signed": ("float a = fabsf(or_elem(x, is_bf16, r * cols + c));\n            if (a > m) m = a;",
+                        "float a = or_elem(x, is_bf16, r * cols + c);\n            if (a > m) m = a;",
+                        ["test_col_amax_matches_numpy"]),
+    "smooth_alpha_swapped": ("s[j] = sqrtf(ax) / sqrtf(aw);", "s[j] = sqrtf(aw) / sqrtf(ax);",
+                             ["test_smooth_factors_closed_forms", "test_smoothquant_int8_pipeline_preserves_the_product"]),
+    "smooth_no_floor": ("float ax = xmax[j] > or_amax_min() ? xmax[j] : or_amax_min();", "float ax = xmax[j];",
+                        ["test_smooth_factors_closed_forms"]),
+    "int8_divisor_128": ("/ 127.0f;", "/ 128.0f;", ["test_int8_rows_worked_example", "test_int8_rows_invariants_and_smoothing"]),
+    "int8_smooth_ops_swapped": ("            if (smooth == 1) v = v / f[c];\n            else if (smooth == 2) v = v * f[c];\n            if (fabsf(v) > amax)",
+                                "            if (smooth == 1) v = v * f[c];\n            else if (smooth == 2) v = v / f[c];\n            if (fabsf(v) > amax)",
+                                ["test_int8_rows_invariants_and_smoothing"]),
+    "int8_gemm_B_transposed": ("(int64_t)qB[j * K + k]", "(int64_t)qB[k * N + j]", ["test_gemm_int8_is_scaled_integer_matmul"]),
+    "int8_gemm_drops_sB": ("double sc = (double)sA[i] * (double)sB[j];", "double sc = (double)sA[i];",
+                           ["test_gemm_int8_is_scaled_integer_matmul"]),
     "kv_k_scale_into_v": ("or_quant_fp8(k, 1, 1, n, n, OR_TENSOR, k_codes, k_scale, k_deq);",
                           "or_quant_fp8(k, 1, 1, n, n, OR_TENSOR, k_codes, v_scale, k_deq);",
                           ["test_kv_write_is_per_tensor_on_k_and_v"]),

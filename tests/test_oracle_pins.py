@@ -490,3 +490,302 @@ def test_gemm_sampled_points_match_full():
     ii, jj = rng.integers(0, 16, 50), rng.integers(0, 128, 50)
     ys, bs = oracle.gemm_fp8_block(qa, sa, qb, sb, ii, jj)
     assert np.array_equal(ys, yf[ii, jj]) and np.array_equal(bs, bf[ii, jj])
+
+
+# ------------------------------------------------------ next rows: KV variants
+
+def _kv_small(seed, B=2, H=3, T=16, D=64, bias_std=4.0):
+    import synthetic as syn
+    return syn.kv_cache_inputs(seed=seed, B=B, H=H, T=T, D=D, bias_std=bias_std)
+
+
+def test_kv_per_head_reduces_to_per_tensor_per_head():
+    """Each head's slice quantized alone by the per-tensor FP8 steps (pinned above) gives
+    exactly the per-head result; the largest element of every head maps to +-448."""
+    k, v = _kv_small(3)
+    kc, vc, ks, vs, kd, vd = oracle.kv_write_fp8_per_head(k, v, want_deq=True)
+    B, H, T, D = k.shape
+    for b in range(B):
+        for h in range(H):
+            for x, c, s in ((k, kc, ks), (v, vc, vs)):
+                rc, rs, _ = oracle.quant_fp8(x[b, h], oracle.FP8_PER_TENSOR, want_deq=False)
+                assert np.array_equal(c[b, h], rc) and np.float32(s[b, h]) == rs[0]
+                xf = (x[b, h].astype(np.uint32) << 16).view(np.float32)
+                i = np.unravel_index(np.argmax(np.abs(xf)), xf.shape)
+                assert c[b, h][i] & 0x7F == 0x7E
+
+
+def test_kv_per_head_power_of_two_head_scaling():
+    """Scaling one head by 2^3 multiplies only that head's scale by 8; all codes stay."""
+    import synthetic as syn
+    k, v = _kv_small(4)
+    kf = (k.astype(np.uint32) << 16).view(np.float32).copy()
+    kf[1, 2] *= np.float32(8.0)
+    k2 = syn.to_bf16_bits(kf)
+    a = oracle.kv_write_fp8_per_head(k, v)
+    b = oracle.kv_write_fp8_per_head(k2, v)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    ratio = b[2] / a[2]
+    assert ratio[1, 2] == 8.0 and np.all(np.delete(ratio.ravel(), 1 * 3 + 2) == 1.0)
+
+
+def test_kv_per_head_given_matches_per_tensor_given():
+    k, _ = _kv_small(5)
+    scales = np.array([[0.01, 0.02, 0.5], [1.0, 0.003, 0.25]], np.float32)
+    codes, _ = oracle.kv_fp8_per_head_given(k, scales)
+    for b in range(2):
+        for h in range(3):
+            rc, _ = oracle.quant_fp8_given(k[b, h], float(scales[b, h]), want_deq=False)
+            assert np.array_equal(codes[b, h], rc)
+
+
+def test_k_channel_zero_point_extremes_map_to_full_range():
+    """Per channel the residual is centred: the channel's largest and smallest values map
+    to +448 and -448 (codes 0x7E and 0xFE), whatever the channel's constant bias."""
+    k, _ = _kv_small(6, T=32)
+    codes, sc, zp, _ = oracle.kv_k_channel_zp(k)
+    kf = (k.astype(np.uint32) << 16).view(np.float32)
+    B, H, T, D = k.shape
+    for b in range(B):
+        for h in range(H):
+            for d in range(D):
+                col = kf[b, h, :, d]
+                if col.max() == col.min():
+                    continue
+                assert codes[b, h, np.argmax(col), d] == 0x7E
+                assert codes[b, h, np.argmin(col), d] == 0xFE
+
+
+def test_k_channel_zero_point_unit_scale_reduces_to_plain_cast():
+    """Channels spanning exactly [-448, 448]: zero point 0 and scale 1, so the codes are
+    the plain E4M3 cast of the values (torch's float8_e4m3fn)."""
+    import synthetic as syn
+    rng = np.random.default_rng(19)
+    x = rng.uniform(-448, 448, (1, 2, 40, 16)).astype(np.float32)
+    x[:, :, 3, :] = 448.0
+    x[:, :, 17, :] = -448.0
+    xb = syn.to_bf16_bits(x)
+    codes, sc, zp, _ = oracle.kv_k_channel_zp(xb)
+    assert np.all(sc == 1.0) and np.all(zp == 0.0)
+    xf = torch.from_numpy((xb.astype(np.uint32) << 16).view(np.float32))
+    assert np.array_equal(codes, xf.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_k_channel_zero_point_is_translation_invariant():
+    """Adding an exactly representable constant to every value of a channel moves its
+    zero point by that constant and leaves codes and scales unchanged (values on a
+    grid where every sum involved is exact in fp32 and bf16)."""
+    import synthetic as syn
+    rng = np.random.default_rng(7)
+    i = rng.integers(-16, 17, (1, 2, 24, 8)).astype(np.float32) / 16.0      # steps of 1/16 in [-1, 1]
+    c0, s0, z0, _ = oracle.kv_k_channel_zp(syn.to_bf16_bits(i))
+    c4, s4, z4, _ = oracle.kv_k_channel_zp(syn.to_bf16_bits(i + np.float32(4.0)))
+    assert np.array_equal(c0, c4) and np.array_equal(s0, s4)
+    assert np.array_equal(z4 - z0, np.full_like(z0, 4.0))
+
+
+def test_k_channel_zero_point_error_tracks_the_variation():
+    """The dequantized K is within half an E4M3 step of the residual (plus the final
+    rounding), so its error scales with each channel's variation, not its bias: on K
+    with a per-channel bias of std 4 it is far below the per-tensor error."""
+    import synthetic as syn
+    k, _ = _kv_small(8, T=64)
+    kf32 = (k.astype(np.uint32) << 16).view(np.float32).copy()
+    kf32[:, :, 0, :8] += np.float32(6.0)               # some channels peak at the first token,
+    kf32[:, :, -1, 8:16] -= np.float32(6.0)            # some bottom out at the last
+    k = syn.to_bf16_bits(kf32)
+    codes, sc, zp, deq = oracle.kv_k_channel_zp(k, want_deq=True)
+    kf = (k.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = np.abs(kf - zp[:, :, None, :])
+    s = sc[:, :, None, :].astype(np.float64)
+    bound = 2.0 ** -4 * r + 2.0 ** -10 * s + 2.0 ** -22 * (np.abs(kf) + np.abs(zp[:, :, None, :]))
+    assert np.all(np.abs(deq - kf) <= bound)
+    _, _, _, _, kd_t, _ = oracle.kv_write_fp8(k, k, want_deq=True)
+    assert np.mean(np.abs(deq - kf)) < 0.5 * np.mean(np.abs(kd_t - kf))
+
+
+# ------------------------------------------------- next rows: INT4 zero point
+
+def test_int4_zp_worked_example():
+    """A group spanning [-0.75, 3.0] in steps of 0.25: s = 3.75 / 15 = 0.25 exactly,
+    z = 3, and each value x maps to x / 0.25 + 3."""
+    vals = np.tile(np.arange(-3, 13, dtype=np.float32) * np.float32(0.25), 8)      # 128 values
+    w = vals.reshape(128, 1).repeat(64, axis=1)
+    qw, sc, zp, deq = oracle.quant_int4_g128_zp(w)
+    assert np.all(sc == 0x3E80) and np.all(zp == 3)                                 # bf16 0.25
+    codes = (qw.view(np.uint32)[:, :, None] >> (4 * np.arange(8))[None, None, :]) & 0xF
+    codes = codes.transpose(0, 2, 1).reshape(128, 64)
+    assert np.array_equal(codes[:, 0], (vals / np.float32(0.25) + 3).astype(np.int64))
+    assert np.array_equal(deq, w)
+
+
+def test_int4_zp_invariants():
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal((512, 96)) * 0.02).astype(np.float32)
+    w[:, 5] = np.abs(w[:, 5])                          # an all-positive column: z = 0
+    w[:, 6] = np.float32(1.0) + np.abs(w[:, 6])        # all values far above 0: the range still starts at 0
+    w[:128, 7] = 0.0                                   # an all-zero group
+    qw, sc, zp, deq = oracle.quant_int4_g128_zp(w)
+    s = (sc.astype(np.uint32) << 16).view(np.float32)
+    codes = ((qw.view(np.uint32)[:, :, None] >> (4 * np.arange(8))[None, None, :]) & 0xF)
+    codes = codes.transpose(0, 2, 1).reshape(512, 96)
+    assert np.all(zp <= 15)
+    assert np.all(zp[:, 5] == 0) and np.all(zp[:, 6] == 0) and zp[0, 7] == 0 and np.all(codes[:128, 7] == 0)
+    srep = np.repeat(s, 128, axis=0)
+    assert np.all(np.abs(deq.astype(np.float64) - w) <= 0.55 * srep)
+    for g in range(4):
+        grp, cg, z = w[g * 128:(g + 1) * 128], codes[g * 128:(g + 1) * 128], zp[g]
+        for n in range(96):
+            if grp[:, n].min() < 0:
+                assert cg[np.argmin(grp[:, n]), n] == 0          # the minimum sits on code 0
+            if grp[:, n].max() > 0:
+                assert cg[np.argmax(grp[:, n]), n] >= 14         # the maximum on the top codes
+    # quantizing the dequantized weight again reproduces codes, scales and zero points
+    # in every group whose codes reach both ends of the range
+    qw2, sc2, zp2, _ = oracle.quant_int4_g128_zp(deq)
+    full = np.zeros((4, 96), bool)
+    for g in range(4):
+        cg = codes[g * 128:(g + 1) * 128]
+        full[g] = (cg.min(axis=0) == 0) & (cg.max(axis=0) == 15)
+    assert full.sum() > 50
+    assert np.array_equal(sc2[full], sc[full]) and np.array_equal(zp2[full], zp[full])
+    codes2 = ((qw2.view(np.uint32)[:, :, None] >> (4 * np.arange(8))[None, None, :]) & 0xF)
+    codes2 = codes2.transpose(0, 2, 1).reshape(512, 96)
+    fullk = np.repeat(full, 128, axis=0)
+    assert np.array_equal(codes2[fullk], codes[fullk])
+
+
+def test_gemm_w4a16_zp_integer_case_is_exact_matmul():
+    """Unit scales, integer activations: the reference equals the integer matmul
+    A (q - z) exactly (numpy, int64)."""
+    import synthetic as syn
+    rng = np.random.default_rng(12)
+    M, K, N = 5, 256, 24
+    A = rng.integers(-20, 21, (M, K)).astype(np.float32)
+    q = rng.integers(0, 16, (K, N)).astype(np.int64)
+    z = rng.integers(0, 16, (K // 128, N)).astype(np.uint8)
+    qw = np.zeros((K // 8, N), np.uint32)
+    for k in range(K):
+        qw[k // 8] |= (q[k].astype(np.uint32) << np.uint32(4 * (k % 8)))
+    sc = np.full((K // 128, N), 0x3F80, np.uint16)
+    y, bound = oracle.gemm_w4a16_zp(syn.to_bf16_bits(A), qw.view(np.int32), sc, z)
+    deq = q - np.repeat(z.astype(np.int64), 128, axis=0)
+    ref = A.astype(np.int64) @ deq
+    assert np.array_equal(y, ref.astype(np.float64))
+    assert np.array_equal(bound, (np.abs(A.astype(np.int64))[:, :, None] * np.abs(deq)[None]).sum(1))
+
+
+# --------------------------------------------- next rows: weight-only FP4 GEMM
+
+def test_gemm_w4a16_fp4_equals_matmul_of_decoded_weights():
+    """Weight-only NVFP4 and MXFP4 references against a numpy matmul of the weights
+    decoded element by element with the (pinned) E2M1 / E4M3 decoders."""
+    import synthetic as syn
+    rng = np.random.default_rng(13)
+    M, N, K = 3, 20, 128
+    A = syn.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    Af = (A.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qB = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    codes = np.stack([qB & 0xF, qB >> 4], axis=-1).reshape(N, K)
+    e2 = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    sB = rng.integers(0x10, 0x70, (N, K // 16)).astype(np.uint8)
+    e4 = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    gB = 0.375
+    W = e2[codes] * np.repeat(e4[sB], 16, axis=1) * gB
+    y, bound = oracle.gemm_w4a16_nvfp4(A, qB, sB, gB)
+    np.testing.assert_allclose(y, Af @ W.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(bound, np.abs(Af) @ np.abs(W).T, rtol=1e-12)
+    eB = rng.integers(110, 140, (N, K // 32)).astype(np.uint8)
+    W = e2[codes] * np.repeat(np.ldexp(1.0, eB.astype(np.int64) - 127), 32, axis=1)
+    y, bound = oracle.gemm_w4a16_mxfp4(A, qB, eB)
+    np.testing.assert_allclose(y, Af @ W.T, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------- next rows: SmoothQuant + INT8
+
+def test_col_amax_matches_numpy():
+    import synthetic as syn
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((37, 50)).astype(np.float32)
+    assert np.array_equal(oracle.col_amax(x), np.abs(x).max(axis=0))
+    b = syn.to_bf16_bits(x)
+    assert np.array_equal(oracle.col_amax(b), np.abs((b.astype(np.uint32) << 16).view(np.float32)).max(axis=0))
+
+
+def test_smooth_factors_closed_forms():
+    """alpha = 0.5: equal amaxes give 1, a ratio of 4 gives 2 (exactly), a zero amax
+    takes the 1e-12 floor, and s^2 = ax / aw to a few fp32 ulps."""
+    xm = np.array([3.0, 12.0, 0.5, 0.0, 7.0], np.float32)
+    wm = np.array([3.0, 3.0, 2.0, 4.0, 0.0], np.float32)
+    s = oracle.smooth_factors(xm, wm)
+    assert s[0] == 1.0 and s[1] == 2.0 and s[2] == 0.5
+    assert s[3] == np.float32(np.sqrt(np.float32(1e-12))) / np.float32(2.0)
+    rng = np.random.default_rng(15)
+    xm = rng.uniform(0.01, 100, 1000).astype(np.float32)
+    wm = rng.uniform(0.001, 1, 1000).astype(np.float32)
+    s = oracle.smooth_factors(xm, wm).astype(np.float64)
+    np.testing.assert_allclose(s * s, xm.astype(np.float64) / wm, rtol=4e-7)
+
+
+def test_int8_rows_worked_example():
+    """amax 127 gives s = 1, so q = rint(x) with halves to even, and -127 at the minimum."""
+    x = np.array([[2.5, 3.5, -2.5, 127.0, -127.0, 0.4, -0.6, 126.5]], np.float32)
+    q, s, deq = oracle.quant_int8_rows(x)
+    assert s[0] == 1.0
+    assert q.tolist() == [[2, 4, -2, 127, -127, 0, -1, 126]]
+
+
+def test_int8_rows_invariants_and_smoothing():
+    rng = np.random.default_rng(16)
+    x = rng.standard_normal((20, 256)).astype(np.float32)
+    x[:, 9] *= np.float32(40.0)
+    q, s, deq = oracle.quant_int8_rows(x)
+    assert np.all(np.abs(q).max(axis=1) == 127)
+    assert np.all(np.abs(deq.astype(np.float64) - x) <= 0.5 * s[:, None] * (1 + 2.0 ** -20))
+    ones = np.ones(256, np.float32)
+    for mode in (oracle.INT8_DIVIDE, oracle.INT8_MULTIPLY):
+        q1, s1, _ = oracle.quant_int8_rows(x, ones, mode)
+        assert np.array_equal(q1, q) and np.array_equal(s1, s)
+    four = np.full(256, 4.0, np.float32)
+    qm, sm, _ = oracle.quant_int8_rows(x, four, oracle.INT8_MULTIPLY)
+    qd, sd, _ = oracle.quant_int8_rows(x, four, oracle.INT8_DIVIDE)
+    assert np.array_equal(qm, q) and np.array_equal(sm, 4 * s)
+    assert np.array_equal(qd, q) and np.array_equal(sd, s / 4)
+
+
+def test_smoothquant_int8_pipeline_preserves_the_product():
+    """X / s and W^T * s quantized per token and per output channel: the INT8 GEMM
+    reference stays close to X W (the migration leaves the product unchanged), and
+    closer than without smoothing on activations with outlier channels."""
+    rng = np.random.default_rng(17)
+    M, K, N = 32, 256, 48
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    X[:, rng.choice(K, 3, replace=False)] *= np.float32(60.0)
+    Wt = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)       # B^T [N, K]
+    s = oracle.smooth_factors(oracle.col_amax(X), oracle.col_amax(Wt))
+    qa, sa, _ = oracle.quant_int8_rows(X, s, oracle.INT8_DIVIDE)
+    qb, sb, _ = oracle.quant_int8_rows(Wt, s, oracle.INT8_MULTIPLY)
+    y, _ = oracle.gemm_int8(qa, sa, qb, sb)
+    exact = X.astype(np.float64) @ Wt.T.astype(np.float64)
+    err_smooth = np.abs(y - exact).mean()
+    qa0, sa0, _ = oracle.quant_int8_rows(X)
+    qb0, sb0, _ = oracle.quant_int8_rows(Wt)
+    y0, _ = oracle.gemm_int8(qa0, sa0, qb0, sb0)
+    err_plain = np.abs(y0 - exact).mean()
+    assert err_smooth < 0.05 * np.abs(exact).mean()
+    assert err_smooth < 0.7 * err_plain
+
+
+def test_gemm_int8_is_scaled_integer_matmul():
+    rng = np.random.default_rng(18)
+    M, N, K = 9, 14, 384
+    qa = rng.integers(-128, 128, (M, K)).astype(np.int8)
+    qb = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    sa = rng.uniform(0.001, 1, M).astype(np.float32)
+    sb = rng.uniform(0.001, 1, N).astype(np.float32)
+    y, bound = oracle.gemm_int8(qa, sa, qb, sb)
+    acc = qa.astype(np.int64) @ qb.T.astype(np.int64)
+    sc = sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :]
+    np.testing.assert_allclose(y, acc * sc, rtol=1e-15)
+    np.testing.assert_allclose(bound, (np.abs(qa.astype(np.int64)) @ np.abs(qb.T.astype(np.int64))) * sc,
+                               rtol=1e-15)
