@@ -22,6 +22,9 @@ __all__ = [
     "qz_quantize_int4_g128", "qz_kv_write_fp8", "qz_gemm_w4a16", "qz_gemm_w4a16_grouped",
     "qz_gemm_fp8_block", "qz_gemm_nvfp4", "qz_gemm_nvfp4_noalloc", "qz_gemm_mxfp4", "qz_prepare_fp4_scales",
     "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
+    "qz_kv_write_fp8_per_head", "qz_kv_write_fp8_channel_zp", "qz_quantize_int4_g128_zp", "qz_gemm_w4a16_zp",
+    "qz_gemm_w4a16_nvfp4", "qz_gemm_w4a16_mxfp4", "qz_col_amax", "qz_smooth_factors", "qz_quantize_int8_rows",
+    "qz_gemm_int8", "qz_gemm_fp8_block_quant", "SMOOTH_NONE", "SMOOTH_DIVIDE", "SMOOTH_MULTIPLY",
 ]
 
 F32, BF16 = 0, 1
@@ -30,6 +33,8 @@ SCALE_COMPUTE, SCALE_GIVEN = 0, 1
 OP_QUANTIZE_FP8, OP_QUANTIZE_NVFP4, OP_KV_WRITE_FP8 = 0, 1, 2
 OP_GEMM_W4A16, OP_GEMM_FP8_BLOCK, OP_GEMM_NVFP4, OP_GEMM_MXFP4 = 3, 4, 5, 6
 OP_GEMM_NVFP4_GROUPED, OP_PREPARE_FP4_SCALES, OP_QUANTIZE_NVFP4_GROUPED = 7, 8, 9
+OP_KV_WRITE_FP8_PER_HEAD, OP_KV_WRITE_FP8_CHANNEL_ZP, OP_COL_AMAX = 10, 11, 12
+SMOOTH_NONE, SMOOTH_DIVIDE, SMOOTH_MULTIPLY = 0, 1, 2
 
 if not os.path.exists(LIB):
     raise ImportError(f"libqz.so is not built ({LIB}); run bit_quantized_linear_quantizers_gb300.build() "
@@ -74,6 +79,17 @@ _SIGS = {
     "qz_prepare_fp4_scales": (_I, [_P, _I, _I, _I, _P, _P]),
     "qz_gemm_nvfp4_grouped": (_I, [ctypes.POINTER(_Nvfp4Problem), _I, _P, _SZ, _P]),
     "qz_quantize_nvfp4_grouped": (_I, [ctypes.POINTER(_Nvfp4Tensor), _I, _I, _P, _SZ, _P]),
+    "qz_kv_write_fp8_per_head": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "qz_kv_write_fp8_channel_zp": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qz_quantize_int4_g128_zp": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "qz_gemm_w4a16_zp": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_gemm_w4a16_nvfp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_gemm_w4a16_mxfp4": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_col_amax": (_I, [_P, _I, _I64, _I64, _P, _P, _SZ, _P]),
+    "qz_smooth_factors": (_I, [_P, _P, _I64, ctypes.c_float, _P, _P]),
+    "qz_quantize_int8_rows": (_I, [_P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P]),
+    "qz_gemm_int8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_gemm_fp8_block_quant": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -492,3 +508,202 @@ def qz_gemm_nvfp4_grouped(problems, ws=None, stream=None):
     buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4_GROUPED, len(problems), kmax), d)
     _check(lib.qz_gemm_nvfp4_grouped(arr, len(problems), _ptr(buf), nb, _stream(stream)),
            "qz_gemm_nvfp4_grouped")
+
+
+# ------------------------------------------------ variants of the base formats
+
+def _kv_inputs(k, v):
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16 or k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must be bf16 tensors of the same [B, H, T, D] shape")
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous")
+    d = _device()
+    _on(k, "k", d)
+    _on(v, "v", d)
+    return d
+
+
+def qz_kv_write_fp8_per_head(k: torch.Tensor, v: torch.Tensor, k_codes=None, v_codes=None, k_scale=None,
+                             v_scale=None, mode: int = SCALE_COMPUTE, ws=None, stream=None):
+    """FP8 KV write with one scale per (batch, head) of bf16 [B, H, T, D] tensors.
+    Returns (k_codes, v_codes, k_scale [B, H], v_scale [B, H]); in SCALE_GIVEN mode the
+    scales are inputs."""
+    d = _kv_inputs(k, v)
+    B, H, T, D = k.shape
+    dev = k.device
+    k_codes = torch.empty(k.shape, dtype=torch.uint8, device=dev) if k_codes is None else k_codes
+    v_codes = torch.empty(v.shape, dtype=torch.uint8, device=dev) if v_codes is None else v_codes
+    k_scale = torch.empty((B, H), dtype=torch.float32, device=dev) if k_scale is None else k_scale
+    v_scale = torch.empty((B, H), dtype=torch.float32, device=dev) if v_scale is None else v_scale
+    n = B * H * T * D
+    args = (_arg(k_codes, "k_codes", d, 1, n), _arg(v_codes, "v_codes", d, 1, n),
+            _arg(k_scale, "k_scale", d, torch.float32, B * H), _arg(v_scale, "v_scale", d, torch.float32, B * H))
+    need = qz_workspace_size(OP_KV_WRITE_FP8_PER_HEAD, B * H, T * D) if mode == SCALE_COMPUTE else 0
+    buf, nb = _ws(ws, need, d)
+    _check(lib.qz_kv_write_fp8_per_head(k.data_ptr(), v.data_ptr(), B, H, T, D, *args, mode, _ptr(buf), nb,
+                                        _stream(stream)), "qz_kv_write_fp8_per_head")
+    return k_codes, v_codes, k_scale, v_scale
+
+
+def qz_kv_write_fp8_channel_zp(k: torch.Tensor, v: torch.Tensor, k_codes=None, v_codes=None, k_scale=None,
+                               k_zero=None, v_scale=None, ws=None, stream=None):
+    """FP8 KV write with K per channel and a zero point (over the tokens) and V per token.
+    Returns (k_codes, v_codes, k_scale [B, H, D], k_zero [B, H, D], v_scale [B, H, T])."""
+    d = _kv_inputs(k, v)
+    B, H, T, D = k.shape
+    dev = k.device
+    k_codes = torch.empty(k.shape, dtype=torch.uint8, device=dev) if k_codes is None else k_codes
+    v_codes = torch.empty(v.shape, dtype=torch.uint8, device=dev) if v_codes is None else v_codes
+    k_scale = torch.empty((B, H, D), dtype=torch.float32, device=dev) if k_scale is None else k_scale
+    k_zero = torch.empty((B, H, D), dtype=torch.float32, device=dev) if k_zero is None else k_zero
+    v_scale = torch.empty((B, H, T), dtype=torch.float32, device=dev) if v_scale is None else v_scale
+    n = B * H * T * D
+    args = (_arg(k_codes, "k_codes", d, 1, n), _arg(v_codes, "v_codes", d, 1, n),
+            _arg(k_scale, "k_scale", d, torch.float32, B * H * D), _arg(k_zero, "k_zero", d, torch.float32, B * H * D),
+            _arg(v_scale, "v_scale", d, torch.float32, B * H * T))
+    buf, nb = _ws(ws, qz_workspace_size(OP_KV_WRITE_FP8_CHANNEL_ZP, B * H, T, D), d)
+    _check(lib.qz_kv_write_fp8_channel_zp(k.data_ptr(), v.data_ptr(), B, H, T, D, *args, _ptr(buf), nb,
+                                          _stream(stream)), "qz_kv_write_fp8_channel_zp")
+    return k_codes, v_codes, k_scale, k_zero, v_scale
+
+
+def qz_quantize_int4_g128_zp(w: torch.Tensor, qweight=None, scale_bf16=None, zero=None, dequant=False, stream=None):
+    """INT4 with a zero point (codes 0..15) of a [K, N] weight. Returns (qweight i32 [K/8, N],
+    scale bf16 [K/128, N], zero u8 [K/128, N], dequant f32 [K, N] or None)."""
+    K, N, ld = _rows_cols_ld(w)
+    wt = _dtype_code(w)
+    d = _device()
+    _on(w, "w", d)
+    if qweight is None:
+        qweight = torch.empty((K // 8, N), dtype=torch.int32, device=w.device)
+    if scale_bf16 is None:
+        scale_bf16 = torch.empty((K // 128, N), dtype=torch.bfloat16, device=w.device)
+    if zero is None:
+        zero = torch.empty((K // 128, N), dtype=torch.uint8, device=w.device)
+    deq = torch.empty((K, N), dtype=torch.float32, device=w.device) if dequant else None
+    _check(lib.qz_quantize_int4_g128_zp(w.data_ptr(), wt, K, N, ld, _arg(qweight, "qweight", d, 4, (K // 8) * N),
+                                        _arg(scale_bf16, "scale_bf16", d, 2, (K // 128) * N),
+                                        _arg(zero, "zero", d, 1, (K // 128) * N),
+                                        _opt(deq, "dequant", d, torch.float32, K * N), _stream(stream)),
+           "qz_quantize_int4_g128_zp")
+    return qweight, scale_bf16, zero, deq
+
+
+def qz_gemm_w4a16_zp(A: torch.Tensor, qweight, scale_bf16, zero, Y=None, stream=None):
+    """Y[M, N] (bf16) = A[M, K] (bf16) @ dequant(INT4 weight with zero points), M <= 16."""
+    M, K = A.shape
+    N = qweight.shape[1]
+    d = _device()
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    args = (_arg(A, "A", d, torch.bfloat16), _arg(qweight, "qweight", d, 4, (K // 8) * N),
+            _arg(scale_bf16, "scale_bf16", d, 2, (K // 128) * N), _arg(zero, "zero", d, 1, (K // 128) * N),
+            _arg(Y, "Y", d, torch.bfloat16, M * N))
+    _check(lib.qz_gemm_w4a16_zp(*args, M, N, K, _stream(stream)), "qz_gemm_w4a16_zp")
+    return Y
+
+
+def qz_gemm_w4a16_nvfp4(A: torch.Tensor, qB, sB, gB, Y=None, stream=None):
+    """Weight-only NVFP4: Y[M, N] (bf16) = A[M, K] (bf16) @ dequant(B^T [N, K]), M <= 16."""
+    M, K = A.shape
+    N = qB.shape[0]
+    d = _device()
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    args = (_arg(A, "A", d, torch.bfloat16), _arg(qB, "qB", d, 1, N * K // 2), _arg(sB, "sB", d, 1, N * (K // 16)),
+            _arg(gB, "gB", d, torch.float32, 1), _arg(Y, "Y", d, torch.bfloat16, M * N))
+    _check(lib.qz_gemm_w4a16_nvfp4(*args, M, N, K, _stream(stream)), "qz_gemm_w4a16_nvfp4")
+    return Y
+
+
+def qz_gemm_w4a16_mxfp4(A: torch.Tensor, qB, eB, Y=None, stream=None):
+    """Weight-only MXFP4: Y[M, N] (bf16) = A[M, K] (bf16) @ dequant(B^T [N, K]), M <= 16."""
+    M, K = A.shape
+    N = qB.shape[0]
+    d = _device()
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    args = (_arg(A, "A", d, torch.bfloat16), _arg(qB, "qB", d, 1, N * K // 2), _arg(eB, "eB", d, 1, N * (K // 32)),
+            _arg(Y, "Y", d, torch.bfloat16, M * N))
+    _check(lib.qz_gemm_w4a16_mxfp4(*args, M, N, K, _stream(stream)), "qz_gemm_w4a16_mxfp4")
+    return Y
+
+
+def qz_col_amax(x: torch.Tensor, out=None, ws=None, stream=None):
+    """max |x[r, c]| over the rows of each column of a contiguous 2-D fp32/bf16 tensor."""
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("qz_col_amax takes a contiguous 2-D tensor")
+    rows, cols = x.shape
+    d = _device()
+    _on(x, "x", d)
+    if out is None:
+        out = torch.empty((cols,), dtype=torch.float32, device=x.device)
+    buf, nb = _ws(ws, qz_workspace_size(OP_COL_AMAX, rows, cols), d)
+    _check(lib.qz_col_amax(x.data_ptr(), _dtype_code(x), rows, cols, _arg(out, "out", d, torch.float32, cols),
+                           _ptr(buf), nb, _stream(stream)), "qz_col_amax")
+    return out
+
+
+def qz_smooth_factors(x_amax: torch.Tensor, w_amax: torch.Tensor, alpha: float = 0.5, out=None, stream=None):
+    """SmoothQuant migration factors s_j = max|X_j|^a / max|W_j|^(1-a), a = 0.5."""
+    n = x_amax.numel()
+    d = _device()
+    if out is None:
+        out = torch.empty((n,), dtype=torch.float32, device=x_amax.device)
+    _check(lib.qz_smooth_factors(_arg(x_amax, "x_amax", d, torch.float32, n), _arg(w_amax, "w_amax", d, torch.float32, n),
+                                 n, float(alpha), _arg(out, "out", d, torch.float32, n), _stream(stream)),
+           "qz_smooth_factors")
+    return out
+
+
+def qz_quantize_int8_rows(x: torch.Tensor, factors=None, op: int = SMOOTH_NONE, codes=None, scales=None,
+                          dequant=False, stream=None):
+    """INT8 per row of a contiguous 2-D fp32/bf16 tensor after the optional per-column
+    SmoothQuant factor (SMOOTH_DIVIDE for activations, SMOOTH_MULTIPLY for weights as
+    B^T). Returns (codes int8 [R, C], scales f32 [R], dequant f32 or None)."""
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("qz_quantize_int8_rows takes a contiguous 2-D tensor")
+    rows, cols = x.shape
+    d = _device()
+    _on(x, "x", d)
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=x.device) if codes is None else codes
+    scales = torch.empty((rows,), dtype=torch.float32, device=x.device) if scales is None else scales
+    deq = torch.empty((rows, cols), dtype=torch.float32, device=x.device) if dequant else None
+    _check(lib.qz_quantize_int8_rows(x.data_ptr(), _dtype_code(x), rows, cols,
+                                     _opt(factors, "factors", d, torch.float32, cols), int(op),
+                                     _arg(codes, "codes", d, 1, rows * cols), _arg(scales, "scales", d, torch.float32, rows),
+                                     _opt(deq, "dequant", d, torch.float32, rows * cols), _stream(stream)),
+           "qz_quantize_int8_rows")
+    return codes, scales, deq
+
+
+def qz_gemm_int8(qA, sA, qB, sB, Y=None, stream=None):
+    """Y[M, N] (bf16) = diag(sA) (qA qB^T) diag(sB): INT8 A [M, K] and B^T [N, K]."""
+    M, K = qA.shape
+    N = qB.shape[0]
+    d = _device()
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    args = (_arg(qA, "qA", d, 1, M * K), _arg(sA, "sA", d, torch.float32, M), _arg(qB, "qB", d, 1, N * K),
+            _arg(sB, "sB", d, torch.float32, N), _arg(Y, "Y", d, torch.bfloat16, M * N))
+    _check(lib.qz_gemm_int8(*args, M, N, K, _stream(stream)), "qz_gemm_int8")
+    return Y
+
+
+def qz_gemm_fp8_block_quant(qA, sA, qB, sB, Y=None, y_codes=None, y_scales=None, want_y: bool = False, stream=None):
+    """The FP8 block-scaled GEMM with the output quantized to FP8 1x128 in its epilogue.
+    Returns (y_codes u8 [M, N], y_scales f32 [M, N/128], Y bf16 [M, N] or None)."""
+    M, K = qA.shape
+    N = qB.shape[0]
+    d = _device()
+    if y_codes is None:
+        y_codes = torch.empty((M, N), dtype=torch.uint8, device=qA.device)
+    if y_scales is None:
+        y_scales = torch.empty((M, N // 128), dtype=torch.float32, device=qA.device)
+    if Y is None and want_y:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=qA.device)
+    args = (_arg(qA, "qA", d, 1, M * K), _arg(sA, "sA", d, torch.float32, M * (K // 128)), _arg(qB, "qB", d, 1, N * K),
+            _arg(sB, "sB", d, torch.float32, (N // 128) * (K // 128)), _opt(Y, "Y", d, torch.bfloat16, M * N),
+            _arg(y_codes, "y_codes", d, 1, M * N), _arg(y_scales, "y_scales", d, torch.float32, M * (N // 128)))
+    _check(lib.qz_gemm_fp8_block_quant(*args, M, N, K, _stream(stream)), "qz_gemm_fp8_block_quant")
+    return y_codes, y_scales, Y

@@ -46,10 +46,16 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
 
+// QOUT: the epilogue also quantizes its output for the next layer, FP8 E4M3
+// with one scale per row and 128 columns ("量化部署实战", 练习 2: the
+// activation's (1, 128) scales are computed at the end of the previous
+// kernel): each thread's 128 bf16 outputs are exactly one such group. Y (bf16)
+// is then stored only when non-null.
+template <bool QOUT>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const float* __restrict__ sA, const float* __restrict__ sB, uint16_t* __restrict__ Y,
-                      int M, int N, int K) {
+                      uint8_t* __restrict__ Yq, float* __restrict__ Yqs, int M, int N, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -188,6 +194,32 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
             }
             if (!ok) break;
+            if (QOUT) {
+                // the bf16 output (what this kernel would store), then its 1x128 FP8 group:
+                // s = max(amax, 1e-12) / 448, code = E4M3(y / s), quotients correctly rounded
+                float am = 0.0f;
+#pragma unroll
+                for (int i = 0; i < EPI_COLS; i++) {
+                    acc[i] = __bfloat162float(__float2bfloat16_rn(acc[i]));
+                    am = fmaxf(am, fabsf(acc[i]));
+                }
+                const float sq = div1(fmaxf(am, kAmaxMin), Recip(kFp8Max));
+                const Recip dq(sq);
+                uint4* qrow = reinterpret_cast<uint4*>(Yq + (size_t)(m0 + r) * N + n0 + h * EPI_COLS);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 16; j++) {
+                    uint32_t p[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const float a = acc[j * 16 + 2 * e], b = acc[j * 16 + 2 * e + 1];
+                        p[e] = e4m3x2(sign_of(div1(a, dq), a), sign_of(div1(b, dq), b));
+                    }
+                    qrow[j] = make_uint4(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410),
+                                         __byte_perm(p[4], p[5], 0x5410), __byte_perm(p[6], p[7], 0x5410));
+                }
+                Yqs[(size_t)(m0 + r) * (N / 128) + (n0 + h * EPI_COLS) / 128] = sq;
+                if (Y == nullptr) continue;
+            }
             uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * EPI_COLS);
 #pragma unroll
             for (int j = 0; j < EPI_COLS / 8; j++) {
@@ -223,12 +255,23 @@ qz_status fp8_block_error_read_and_clear() {
 
 qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
                                 uint16_t* Y, int M, int N, int K, void*, size_t, cudaStream_t st) {
+    return gemm_fp8_block_quant_launch(qA, sA, qB, sB, Y, nullptr, nullptr, M, N, K, st);
+}
+
+qz_status gemm_fp8_block_quant_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                                      uint16_t* Y, uint8_t* Yq, float* Yqs, int M, int N, int K, cudaStream_t st) {
     CUtensorMap ta, tb;
     if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM)) return QZ_ERR_CUDA;
     if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN)) return QZ_ERR_CUDA;
-    QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel, SMEM_BYTES));
     const int tiles = (M / BM) * (N / BN);
-    fp8_block_gemm_kernel<<<std::min(tiles, num_sms()), THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, M, N, K);
+    const int grid = std::min(tiles, num_sms());
+    if (Yq) {
+        QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<true>, SMEM_BYTES));
+        fp8_block_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, Yq, Yqs, M, N, K);
+    } else {
+        QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<false>, SMEM_BYTES));
+        fp8_block_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, nullptr, nullptr, M, N, K);
+    }
     return launch_status();
 }
 

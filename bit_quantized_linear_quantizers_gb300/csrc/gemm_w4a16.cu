@@ -125,6 +125,7 @@ struct RdProb {
     const uint16_t* A;                  // bf16 [M, K]
     const uint4* W;                     // qweight [K/8, N] int32, as 16-byte quads of columns
     const uint16_t* S;                  // bf16 [K/128, N]
+    const uint8_t* Z;                   // zero points [K/128, N] (unsigned codes only)
     uint16_t* Y;                        // bf16 [M, N]
     int M, N, K;
     int cta_begin;                      // first CTA of this problem
@@ -135,12 +136,17 @@ struct RdParams {
     int count;
 };
 
-// Biased unpack: bf16x2 (q_even + 136, q_odd + 136) of byte B of w (w4 = w >> 4).
-template <int B>
+// Biased unpack: bf16x2 (q_even + 136, q_odd + 136) of byte B of w (w4 = w >> 4)
+// for two's-complement codes; with UNSIGNED codes (0..15, used with a zero
+// point) the sign flip is left out and the halves hold u + 128.
+template <int B, bool UNSIGNED = false>
 __device__ __forceinline__ uint32_t nib_pair_biased(uint32_t w, uint32_t w4) {
     const uint32_t r = __byte_perm(w, w4, (uint32_t)B | ((uint32_t)(4 + B) << 8));
     uint32_t v;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43084308u));
+    if (UNSIGNED)
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43004300u));
+    else
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(r), "r"(0x000F000Fu), "r"(0x43084308u));
     return v;
 }
 
@@ -149,8 +155,10 @@ __device__ __forceinline__ uint32_t nib_pair_biased(uint32_t w, uint32_t w4) {
 struct RdGroup {
     uint4 w[4];
     uint2 s;
+    uint32_t z;                         // the 4 columns' zero points (unsigned codes only)
 };
 
+template <bool ZP = false>
 __device__ __forceinline__ void rd_load(RdGroup& G, const RdProb& pr, int n0, int grp, int g, int t) {
     const int nq = pr.N >> 2;                                     // 16-byte quads per row
     const uint4* base = pr.W + (size_t)(grp * 16 + t) * nq + ((n0 >> 2) + g);
@@ -161,9 +169,12 @@ __device__ __forceinline__ void rd_load(RdGroup& G, const RdProb& pr, int n0, in
                      : "=r"(G.w[c].x), "=r"(G.w[c].y), "=r"(G.w[c].z), "=r"(G.w[c].w) : "l"(q));
     }
     G.s = __ldg(reinterpret_cast<const uint2*>(pr.S + (size_t)grp * pr.N + n0 + 4 * g));
+    if (ZP) G.z = __ldg(reinterpret_cast<const uint32_t*>(pr.Z + (size_t)grp * pr.N + n0 + 4 * g));
 }
 
-template <int MT>
+// ZP: unsigned codes with one zero point per group and column; the group sum
+// is sum(a * (u + 128)) - (128 + z) * sum(a).
+template <int MT, bool ZP = false>
 __global__ void __launch_bounds__(RD_WARPS * 32, MT <= 8 ? 3 : 2)
 w4a16_rd_kernel(const __grid_constant__ RdParams P) {
     constexpr int MB = MT / 8;
@@ -191,8 +202,10 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
         const int rows = pr.K >> 3;
         for (int r = threadIdx.x; r < rows; r += RD_WARPS * 32)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(pr.W + (size_t)r * nq + (n0 >> 2)));
-        for (int r = threadIdx.x; r < ngroups; r += RD_WARPS * 32)
+        for (int r = threadIdx.x; r < ngroups; r += RD_WARPS * 32) {
             asm volatile("prefetch.global.L2 [%0];" ::"l"(pr.S + (size_t)r * pr.N + n0));
+            if (ZP) asm volatile("prefetch.global.L2 [%0];" ::"l"(pr.Z + (size_t)r * pr.N + n0));
+        }
     }
 
     float acc[2][MB][4];
@@ -203,7 +216,7 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
 
     RdGroup cur;
     int grp = warp;
-    if (grp < ngroups) rd_load(cur, pr, n0, grp, g, t);
+    if (grp < ngroups) rd_load<ZP>(cur, pr, n0, grp, g, t);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint16_t* arow[MB];
     bool live[MB];
@@ -234,10 +247,10 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
             for (int sl = 0; sl < 2; sl++) {                       // MMA rows g, g+8 = columns 4g+2sl, 4g+2sl+1
                 const uint32_t w0 = wq[2 * sl], w1 = wq[2 * sl + 1];
                 const uint32_t x0 = w0 >> 4, x1 = w1 >> 4;
-                const uint32_t f0[4] = {nib_pair_biased<0>(w0, x0), nib_pair_biased<0>(w1, x1),
-                                        nib_pair_biased<1>(w0, x0), nib_pair_biased<1>(w1, x1)};
-                const uint32_t f1[4] = {nib_pair_biased<2>(w0, x0), nib_pair_biased<2>(w1, x1),
-                                        nib_pair_biased<3>(w0, x0), nib_pair_biased<3>(w1, x1)};
+                const uint32_t f0[4] = {nib_pair_biased<0, ZP>(w0, x0), nib_pair_biased<0, ZP>(w1, x1),
+                                        nib_pair_biased<1, ZP>(w0, x0), nib_pair_biased<1, ZP>(w1, x1)};
+                const uint32_t f1[4] = {nib_pair_biased<2, ZP>(w0, x0), nib_pair_biased<2, ZP>(w1, x1),
+                                        nib_pair_biased<3, ZP>(w0, x0), nib_pair_biased<3, ZP>(w1, x1)};
 #pragma unroll
                 for (int mb = 0; mb < MB; mb++) {
                     mma_bf16(ag[sl][mb], f0, bv[mb].x, bv[mb].y);
@@ -252,17 +265,22 @@ w4a16_rd_kernel(const __grid_constant__ RdParams P) {
         }
         const float sc[4] = {bf16_bits_to_f32(cur.s.x & 0xFFFFu), bf16_bits_to_f32(cur.s.x >> 16),
                              bf16_bits_to_f32(cur.s.y & 0xFFFFu), bf16_bits_to_f32(cur.s.y >> 16)};
+        float nb[4] = {-136.0f, -136.0f, -136.0f, -136.0f};       // minus the bias of each column
+        if (ZP) {
+#pragma unroll
+            for (int c = 0; c < 4; c++) nb[c] = -(128.0f + (float)((cur.z >> (8 * c)) & 0xFFu));
+        }
 #pragma unroll
         for (int sl = 0; sl < 2; sl++)
 #pragma unroll
             for (int mb = 0; mb < MB; mb++) {                      // remove the bias, scale, accumulate
-                acc[sl][mb][0] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[mb][0], ag[sl][mb][0]), acc[sl][mb][0]);
-                acc[sl][mb][1] = fmaf(sc[2 * sl], fmaf(-136.0f, sg[mb][1], ag[sl][mb][1]), acc[sl][mb][1]);
-                acc[sl][mb][2] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][0], ag[sl][mb][2]), acc[sl][mb][2]);
-                acc[sl][mb][3] = fmaf(sc[2 * sl + 1], fmaf(-136.0f, sg[mb][1], ag[sl][mb][3]), acc[sl][mb][3]);
+                acc[sl][mb][0] = fmaf(sc[2 * sl], fmaf(nb[2 * sl], sg[mb][0], ag[sl][mb][0]), acc[sl][mb][0]);
+                acc[sl][mb][1] = fmaf(sc[2 * sl], fmaf(nb[2 * sl], sg[mb][1], ag[sl][mb][1]), acc[sl][mb][1]);
+                acc[sl][mb][2] = fmaf(sc[2 * sl + 1], fmaf(nb[2 * sl + 1], sg[mb][0], ag[sl][mb][2]), acc[sl][mb][2]);
+                acc[sl][mb][3] = fmaf(sc[2 * sl + 1], fmaf(nb[2 * sl + 1], sg[mb][1], ag[sl][mb][3]), acc[sl][mb][3]);
             }
         // the next group's loads (already requested from L2 by the prefetch above)
-        if (grp + RD_WARPS < ngroups) rd_load(cur, pr, n0, grp + RD_WARPS, g, t);
+        if (grp + RD_WARPS < ngroups) rd_load<ZP>(cur, pr, n0, grp + RD_WARPS, g, t);
     }
     // partial sums of this warp -> shared memory; fixed-order sum over warps
 #pragma unroll
@@ -694,8 +712,8 @@ int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
 // Register-direct launch for up to 8 tokens: one CTA per 32 columns of every
 // problem, programmatic dependent launch.
-template <int MT>
-qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+template <int MT, bool ZP = false>
+qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros = nullptr) {
     RdParams P;                                   // the kernel parameter block (copied at launch)
     int total = 0;
     P.count = count;
@@ -705,6 +723,7 @@ qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st
         p.A = q.A;
         p.W = reinterpret_cast<const uint4*>(q.qweight);
         p.S = q.scale_bf16;
+        p.Z = zeros ? zeros[i] : nullptr;
         p.Y = q.Y;
         p.M = q.M; p.N = q.N; p.K = q.K;
         p.cta_begin = total;
@@ -720,7 +739,7 @@ qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT>, P) != cudaSuccess) return QZ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT, ZP>, P) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
@@ -840,6 +859,15 @@ qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int 
 } // namespace
 
 size_t ws_gemm_w4a16(int, int, int) { return 0; }
+
+// W4A16 with unsigned codes and a zero point per group and column, up to 16
+// tokens: the register-direct kernel.
+qz_status gemm_w4a16_zp_launch(const uint16_t* A, const int32_t* qweight, const uint16_t* scale, const uint8_t* zero,
+                               uint16_t* Y, int M, int N, int K, cudaStream_t st) {
+    const qz_w4a16_problem p = {A, qweight, scale, Y, M, N, K};
+    const uint8_t* z[1] = {zero};
+    return M <= 8 ? launch_rd<8, true>(&p, 1, st, z) : launch_rd<16, true>(&p, 1, st, z);
+}
 
 qz_status w4a16_error_read_and_clear() {
     unsigned int v = 0, z = 0;

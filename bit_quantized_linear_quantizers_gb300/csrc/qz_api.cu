@@ -3,6 +3,7 @@
 // memory; a call that fails validation enqueues nothing.
 #include "qz_internal.cuh"
 #include "qz_gemm.cuh"
+#include "qz_next.cuh"
 
 #include <mutex>
 
@@ -74,9 +75,9 @@ qz_status selftest_error_read_and_clear() {
 
 qz_status device_error_read_and_clear() {
     // read and clear every word, report the first error found
-    const qz_status s[5] = {w4a16_error_read_and_clear(), w4a16_tc_error_read_and_clear(),
+    const qz_status s[6] = {w4a16_error_read_and_clear(), w4a16_tc_error_read_and_clear(),
                             fp8_block_error_read_and_clear(), fp4_error_read_and_clear(),
-                            selftest_error_read_and_clear()};
+                            int8_error_read_and_clear(), selftest_error_read_and_clear()};
     for (qz_status v : s)
         if (v != QZ_OK) return v;
     return QZ_OK;
@@ -154,6 +155,9 @@ size_t qz_workspace_size(qz_op op, int64_t d0, int64_t d1, int64_t d2) {
                                                                                  : 0;
     case QZ_OP_QUANTIZE_NVFP4_GROUPED:
         return d0 >= 1 && d0 <= kNvfp4GroupMax ? ws_quantize_nvfp4_grouped((int)d0) : 0;
+    case QZ_OP_KV_WRITE_FP8_PER_HEAD: return d0 >= 1 && d1 >= 1 ? ws_kv_per_head(d0, d1) : 0;
+    case QZ_OP_KV_WRITE_FP8_CHANNEL_ZP: return d0 >= 1 && d1 >= 1 && d2 >= 1 ? ws_kv_channel_zp(d0, d1, d2) : 0;
+    case QZ_OP_COL_AMAX: return d0 >= 1 && d1 >= 1 ? ws_col_amax(d0, d1) : 0;
     case QZ_OP_PREPARE_FP4_SCALES:
         return d0 >= 1 && d0 <= (1 << 24) && d1 >= 1 && d1 <= (1 << 24) ? prepared_fp4_scale_bytes((int)d0, (int)d1, d2 != 0)
                                                                          : 0;

@@ -18,6 +18,8 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void* w
                             cudaStream_t st);
 qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
                                 uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
+qz_status gemm_fp8_block_quant_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                                      uint16_t* Y, uint8_t* Yq, float* Yqs, int M, int N, int K, cudaStream_t st);
 size_t ws_gemm_nvfp4_grouped(int count, int kmax);
 size_t prepared_fp4_scale_bytes(int rows, int K, bool nv);
 qz_status gemm_nvfp4_grouped_launch(const qz_nvfp4_problem* problems, int count, void* ws, size_t ws_bytes,

@@ -44,6 +44,21 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
                  ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D (TMEM, fp32) (+)= A (smem desc) x B (smem desc), kind::f16 (f16 or bf16
+// operands, per the instruction descriptor).
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (the tensor cores) before it signals them ready.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // D (TMEM, fp32) (+)= A x B with hardware block scaling, E2M1 operands:
 // NVFP4 = kind::mxf4nvf4 with one UE4M3 scale per 16 (scale_vec::4X),
 // MXFP4 = kind::mxf4 with one UE8M0 scale per 32 (scale_vec::2X). The scale

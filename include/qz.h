@@ -72,8 +72,17 @@ typedef enum qz_op {
     QZ_OP_GEMM_NVFP4_GROUPED = 7, /* d0 = problem count, d1 = largest K    */
     QZ_OP_PREPARE_FP4_SCALES = 8, /* d0 = rows, d1 = K, d2 = 1 NVFP4 / 0 MXFP4:
                                      bytes of the prepared output (not scratch) */
-    QZ_OP_QUANTIZE_NVFP4_GROUPED = 9 /* d0 = tensor count                    */
+    QZ_OP_QUANTIZE_NVFP4_GROUPED = 9, /* d0 = tensor count                   */
+    QZ_OP_KV_WRITE_FP8_PER_HEAD = 10, /* d0 = B*H, d1 = T*D                   */
+    QZ_OP_KV_WRITE_FP8_CHANNEL_ZP = 11, /* d0 = B*H, d1 = T, d2 = D           */
+    QZ_OP_COL_AMAX = 12                 /* d0 = rows, d1 = cols               */
 } qz_op;
+
+typedef enum qz_smooth_op {
+    QZ_SMOOTH_NONE = 0,       /* x' = x                                          */
+    QZ_SMOOTH_DIVIDE = 1,     /* x' = x / f[col]  (activations, SmoothQuant)     */
+    QZ_SMOOTH_MULTIPLY = 2    /* x' = x * f[col]  (weights as B^T, SmoothQuant)  */
+} qz_smooth_op;
 
 /* Bytes of workspace the call `op` needs for the given sizes (0 if none).
  * Returns 0 for an unknown op. Sizes that the call itself would reject still
@@ -301,6 +310,124 @@ typedef struct qz_nvfp4_problem {
  * largest K, 0) bytes. */
 qz_status qz_gemm_nvfp4_grouped(const qz_nvfp4_problem* problems, int count, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/* -------------------------------------------- variants (zero points, KV, INT8) */
+
+/* FP8 KV-cache write with one scale per (batch, head) for K and for V
+ * ("量化部署实战", KV Cache 量化: per_head, the amax over the head's T x D
+ * values; calibrated scales per 实际部署时):
+ *   scale[b, h] = max(amax over k[b, h, :, :], 1e-12) / 448; code = E4M3(x / scale)
+ * k, v: bf16 [B, H, T, D] contiguous; codes: n bytes each; k_scale, v_scale:
+ * fp32 [B, H] (device). mode COMPUTE writes the scales and needs
+ * qz_workspace_size(QZ_OP_KV_WRITE_FP8_PER_HEAD, B*H, T*D, 0) bytes of ws; mode
+ * GIVEN reads them (finite, > 0) and needs no workspace.
+ * Shapes: B, H, T >= 1, D % 8 == 0. Alignment: k, v 16 B; codes 8 B. */
+qz_status qz_kv_write_fp8_per_head(const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
+                                   uint8_t* k_codes, uint8_t* v_codes, float* k_scale, float* v_scale,
+                                   qz_scale_mode mode, void* ws, size_t ws_bytes, void* stream);
+
+/* FP8 KV-cache write with K per channel and a zero point, V per token
+ * ("量化部署实战", KV Cache 量化: K carries a constant bias per channel plus a
+ * small variation; quantizing K per channel with a zero point absorbs the bias,
+ * and the KIVI split quantizes K per channel and V per token; "LLM 推理优化 ·
+ * 量化学习笔记" 5.1: asymmetric quantization adds a zero point). The codes stay
+ * E4M3, so the zero point lives in value space. For each channel (b, h, d), over
+ * its T tokens:
+ *   z = fl(0.5 * fl(max + min));  s = max(max_t |fl(x - z)|, 1e-12) / 448
+ *   k_code = E4M3(clamp(fl(x - z) / s, +-448)); dequant = fl(fl(value * s) + z)
+ * and for each token (b, h, t): v_scale = max(amax over its D values, 1e-12) / 448,
+ * v_code = E4M3(v / v_scale).
+ * k_scale, k_zero: fp32 [B, H, D]; v_scale: fp32 [B, H, T]; codes [B, H, T, D].
+ * ws: qz_workspace_size(QZ_OP_KV_WRITE_FP8_CHANNEL_ZP, B*H, T, D) bytes.
+ * Shapes: B, H, T >= 1, D one of 8, 16, 32, 64, 128, 256. Alignment: k, v 16 B,
+ * codes 8 B. */
+qz_status qz_kv_write_fp8_channel_zp(const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
+                                     uint8_t* k_codes, uint8_t* v_codes, float* k_scale, float* k_zero,
+                                     float* v_scale, void* ws, size_t ws_bytes, void* stream);
+
+/* INT4 weight quantization with a zero point: unsigned codes 0..15, one bf16
+ * scale and one integer zero point per group of 128 along K ("量化部署实战",
+ * 格式速查: W4A16, a scale per 128 "+ 零点"; "LLM 推理优化 · 量化学习笔记" 5.1:
+ * q = clamp(round(x / s) + z, ...)). Per group and column the range is widened
+ * to include 0 (lo = min(min, 0), hi = max(max, 0)):
+ *   s = bf16_rne(max(hi - lo, 1e-12) / 15);  z = clamp(rint(-lo / s), 0, 15)
+ *   q = clamp(rint(w / s) + z, 0, 15);         dequant = (q - z) * s
+ * qweight: int32 [K/8, N], element k in bits 4*(k%8)..+3 (unsigned);
+ * scale_bf16: [K/128, N]; zero: uint8 [K/128, N]; dequant nullable fp32 [K, N].
+ * Shapes: K % 128 == 0, N % 64 == 0. Alignment as qz_quantize_int4_g128. */
+qz_status qz_quantize_int4_g128_zp(const void* w, qz_dtype wt, int64_t K, int64_t N, int64_t ldw,
+                                   int32_t* qweight, uint16_t* scale_bf16, uint8_t* zero, float* dequant,
+                                   void* stream);
+
+/* W4A16 GEMM with zero points (the fused unpack + dequant + matmul of
+ * "量化：让每一步搬更少的字节", 路线一, on the codes of qz_quantize_int4_g128_zp):
+ *   Y[m, n] = bf16_rne( sum_g s[g, n] * sum_{k in g} A[m, k] * (q[k, n] - z[g, n]) )
+ * fp32 accumulation. Shapes: 1 <= M <= 16, K % 128 == 0, N % 64 == 0.
+ * Alignment: A, qweight, scale, Y 16 B; zero 4 B. */
+qz_status qz_gemm_w4a16_zp(const uint16_t* A, const int32_t* qweight, const uint16_t* scale_bf16,
+                           const uint8_t* zero, uint16_t* Y, int M, int N, int K, void* stream);
+
+/* Weight-only FP4 GEMMs ("量化部署实战", 精度比较: W4A16 NVFP4 and W4A16
+ * MXFP4): bf16 activations times FP4 weights given as B^T [N, K] exactly as the
+ * FP4 quantizers write them, fp32 accumulation, bf16 output:
+ *   NVFP4: Y[m, n] = bf16_rne( gB * sum_k A[m, k] * e2m1(q[n, k]) * e4m3(s[n, k/16]) )
+ *   MXFP4: Y[m, n] = bf16_rne( sum_k A[m, k] * e2m1(q[n, k]) * 2^(e[n, k/32] - 127) )
+ * qB: [N, K/2]; sB: E4M3 [N, K/16]; gB: fp32 device scalar; eB: E8M0 [N, K/32].
+ * MXFP4 scale codes must lie in 66..192 (scales 2^-61 .. 2^65).
+ * Shapes: 1 <= M <= 16, K % 128 == 0, N % 32 == 0. Alignment: A, qB, Y 16 B;
+ * sB 2 B. */
+qz_status qz_gemm_w4a16_nvfp4(const uint16_t* A, const uint8_t* qB, const uint8_t* sB, const float* gB,
+                              uint16_t* Y, int M, int N, int K, void* stream);
+qz_status qz_gemm_w4a16_mxfp4(const uint16_t* A, const uint8_t* qB, const uint8_t* eB,
+                              uint16_t* Y, int M, int N, int K, void* stream);
+
+/* Per-column amax of x[rows, cols] (the per-channel statistic of SmoothQuant,
+ * "量化：让每一步搬更少的字节", 路线二: max|X_j| over the tokens, max|W_j| over
+ * the output channels of a weight stored as B^T): out[c] = max_r |x[r, c]|.
+ * ws: qz_workspace_size(QZ_OP_COL_AMAX, rows, cols, 0) bytes.
+ * Shapes: rows >= 1, cols % 8 == 0. Alignment: x, out 16 B. */
+qz_status qz_col_amax(const void* x, qz_dtype xt, int64_t rows, int64_t cols, float* out, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* SmoothQuant migration factors ("量化：让每一步搬更少的字节", 路线二:
+ * s_j = max|X_j|^a / max|W_j|^(1-a), a = 0.5 for most models):
+ *   s[j] = fl(sqrt(max(x_amax[j], 1e-12))) / fl(sqrt(max(w_amax[j], 1e-12)))
+ * alpha must be 0.5 (QZ_ERR_UNSUPPORTED otherwise). n >= 1. */
+qz_status qz_smooth_factors(const float* x_amax, const float* w_amax, int64_t n, float alpha, float* s,
+                            void* stream);
+
+/* INT8 quantization per row ("量化部署实战", 格式速查: W8A8 INT8, integers
+ * -128..127, per token for activations and per output channel for weights;
+ * "量化：让每一步搬更少的字节", 量化在做什么: s = amax / 127), after the optional
+ * SmoothQuant factor of each column (op DIVIDE for activations, MULTIPLY for
+ * a weight stored as B^T [N, K]; factors nullable for op NONE):
+ *   x' = fl(x / f[c]) or fl(x * f[c]);  s = max(amax_row(x'), 1e-12) / 127
+ *   q = clamp(rint(x' / s), -128, 127);  dequant = q * s
+ * codes int8 [rows, cols]; scales fp32 [rows]; dequant nullable fp32.
+ * Shapes: cols % 8 == 0. Alignment: x, factors, dequant 16 B; codes 8 B. */
+qz_status qz_quantize_int8_rows(const void* x, qz_dtype xt, int64_t rows, int64_t cols, const float* factors,
+                                qz_smooth_op op, int8_t* codes, float* scales, float* dequant, void* stream);
+
+/* INT8 W8A8 GEMM ("量化：让每一步搬更少的字节", 路线二):
+ *   Y[i, j] = bf16_rne( sA[i] * sB[j] * sum_k qA[i, k] * qB[j, k] )
+ * qA int8 [M, K], qB int8 [N, K] (B^T), sA fp32 [M], sB fp32 [N]; the integer
+ * products are summed exactly while |sum| < 2^24 (fp16 tensor cores on the
+ * widened codes, fp32 accumulation). Shapes: M % 128 == 0, N % 256 == 0,
+ * K % 64 == 0. Alignment: all pointers 16 B. */
+qz_status qz_gemm_int8(const int8_t* qA, const float* sA, const int8_t* qB, const float* sB, uint16_t* Y,
+                       int M, int N, int K, void* stream);
+
+/* FP8 block-scaled GEMM whose epilogue also quantizes its output for the next
+ * layer ("量化部署实战", 练习 2: the activation's (1, 128) scales are computed at
+ * the end of the previous kernel, avoiding another read and write): the same
+ * arithmetic as qz_gemm_fp8_block, then each row's 128-column groups of the
+ * bf16 output y are quantized exactly as qz_quantize_fp8(GROUP_1x128) would:
+ *   y_scale = max(amax(y_group), 1e-12) / 448;  y_code = E4M3(y / y_scale)
+ * y_codes: [M, N] bytes; y_scales: fp32 [M, N/128]; Y (bf16 [M, N]) nullable:
+ * stored too when given. Shapes, layouts and alignment as qz_gemm_fp8_block. */
+qz_status qz_gemm_fp8_block_quant(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
+                                  uint16_t* Y, uint8_t* y_codes, float* y_scales, int M, int N, int K,
+                                  void* stream);
 
 /* NVFP4 GEMM that allocates nothing and takes no workspace. (The surveyed
  * pages have no counterpart: this is an interface convenience of this library.)

@@ -712,14 +712,12 @@ void or_gemm_w4a16_mxfp4(const uint16_t* A, const uint8_t* qB, const uint8_t* eB
  * of SmoothQuant [P2 路线二]): out[cols]. */
 void or_col_amax(const void* x, int is_bf16, int64_t rows, int64_t cols, float* out)
 {
-    for (int64_t c = 0; c < cols; c++) {
-        float m = 0.0f;
-        for (int64_t r = 0; r < rows; r++) {
+    for (int64_t c = 0; c < cols; c++) out[c] = 0.0f;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) {
             float a = fabsf(or_elem(x, is_bf16, r * cols + c));
-            if (a > m) m = a;
+            if (a > out[c]) out[c] = a;
         }
-        out[c] = m;
-    }
 }
 
 /* s_j = max|X_j|^0.5 / max|W_j|^0.5 [P2 路线二, alpha = 0.5], each amax

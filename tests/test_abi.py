@@ -228,3 +228,42 @@ def test_fp4_scale_layout_sizes(qz):
     # the no-alloc scratch (4 MiB) fits M + N = 16384 at K = 4096, as its header states
     assert r1k(8192 * 4096 // 16) + r1k(8192 * 4096 // 16) <= 4 << 20
     assert size(qz.OP_PREPARE_FP4_SCALES, 0, 256, 1) == 0                  # rejected sizes: 0
+
+
+def test_variant_entry_points_reject_bad_arguments_before_any_launch(qz):
+    """The zero-point, KV, weight-only FP4, SmoothQuant/INT8 and fused-output entry points
+    validate on the host: null pointers, shapes and alignment are refused before the
+    device is even queried."""
+    lib = qz.lib
+    P = ctypes.c_void_p(0x1000)          # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p(0x1002)        # misaligned
+    INV, SHAPE, ALIGN, UNSUP = 1, 2, 3, 4
+    assert lib.qz_kv_write_fp8_per_head(None, P, 1, 8, 16, 128, P, P, P, P, 0, P, 1 << 20, None) == INV
+    assert lib.qz_kv_write_fp8_per_head(P, P, 1, 8, 16, 12, P, P, P, P, 0, P, 1 << 20, None) == SHAPE
+    assert lib.qz_kv_write_fp8_per_head(odd, P, 1, 8, 16, 128, P, P, P, P, 0, P, 1 << 20, None) == ALIGN
+    assert lib.qz_kv_write_fp8_per_head(P, P, 1, 8, 16, 128, P, P, P, P, 7, P, 1 << 20, None) == INV
+    assert lib.qz_kv_write_fp8_channel_zp(P, P, 1, 8, 16, 96, P, P, P, P, P, P, 1 << 20, None) == SHAPE
+    assert lib.qz_kv_write_fp8_channel_zp(P, P, 1, 8, 0, 128, P, P, P, P, P, P, 1 << 20, None) == INV
+    assert lib.qz_quantize_int4_g128_zp(P, 0, 100, 64, 64, P, P, P, None, None) == SHAPE
+    assert lib.qz_quantize_int4_g128_zp(P, 0, 128, 64, 64, P, P, None, None, None) == INV
+    assert lib.qz_gemm_w4a16_zp(P, P, P, P, P, 17, 64, 128, None) == SHAPE
+    assert lib.qz_gemm_w4a16_zp(P, P, P, odd, P, 1, 64, 128, None) == ALIGN
+    assert lib.qz_gemm_w4a16_nvfp4(P, P, P, None, P, 1, 64, 128, None) == INV
+    assert lib.qz_gemm_w4a16_nvfp4(P, P, P, P, P, 1, 48, 128, None) == SHAPE
+    assert lib.qz_gemm_w4a16_mxfp4(P, P, P, P, 1, 64, 96, None) == SHAPE
+    assert lib.qz_col_amax(P, 0, 10, 12, P, P, 1 << 20, None) == SHAPE
+    assert lib.qz_smooth_factors(P, P, 16, ctypes.c_float(0.75), P, None) == UNSUP
+    assert lib.qz_smooth_factors(None, P, 16, ctypes.c_float(0.5), P, None) == INV
+    assert lib.qz_quantize_int8_rows(P, 0, 4, 64, None, 1, P, P, None, None) == INV
+    assert lib.qz_quantize_int8_rows(P, 0, 4, 60, None, 0, P, P, None, None) == SHAPE
+    assert lib.qz_gemm_int8(P, P, P, P, P, 128, 256, 96, None) == SHAPE
+    assert lib.qz_gemm_int8(P, P, P, P, odd, 128, 256, 64, None) == ALIGN
+    assert lib.qz_gemm_fp8_block_quant(P, P, P, P, None, None, P, 128, 256, 128, None) == INV
+    assert lib.qz_gemm_fp8_block_quant(P, P, P, P, None, P, P, 128, 200, 128, None) == SHAPE
+
+
+def test_variant_workspace_sizes(qz):
+    assert qz.qz_workspace_size(qz.OP_KV_WRITE_FP8_PER_HEAD, 8, 4096 * 128) >= 16 * 4
+    assert qz.qz_workspace_size(qz.OP_KV_WRITE_FP8_CHANNEL_ZP, 8, 4096, 128) >= 8 * 2 * 128 * 4
+    assert qz.qz_workspace_size(qz.OP_COL_AMAX, 2048, 4096) >= 4096 * 4
+    assert qz.qz_workspace_size(qz.OP_KV_WRITE_FP8_PER_HEAD, 0, 0) == 0

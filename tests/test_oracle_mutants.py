@@ -147,8 +147,8 @@ MUTANTS = {
                       ["test_gemm_w4a16_fp4_equals_matmul_of_decoded_weights"]),
     "w4mx_bias": ("(int)erow[k / 32] - 127", "(int)erow[k / 32] - 126",
                   ["test_gemm_w4a16_fp4_equals_matmul_of_decoded_weights"]),
-    "col_amax_signed": ("float a = fabsf(or_elem(x, is_bf16, r * cols + c));\n            if (a > m) m = a;",
-                        "float a = or_elem(x, is_bf16, r * cols + c);\n            if (a > m) m = a;",
+    "col_amax_signed": ("float a = fabsf(or_elem(x, is_bf16, r * cols + c));\n            if (a > out[c]) out[c] = a;",
+                        "float a = or_elem(x, is_bf16, r * cols + c);\n            if (a > out[c]) out[c] = a;",
                         ["test_col_amax_matches_numpy"]),
     "smooth_alpha_swapped": ("s[j] = sqrtf(ax) / sqrtf(aw);", "s[j] = sqrtf(aw) / sqrtf(ax);",
                              ["test_smooth_factors_closed_forms", "test_smoothquant_int8_pipeline_preserves_the_product"]),
