@@ -157,12 +157,16 @@ class ClockSampler:
 
 class Timer:
     """Kernel time per call: `reps` calls captured in one CUDA graph on the launching
-    stream, replayed after warm-up, timed with CUDA events on that stream."""
+    stream, replayed `replays` (>= 20) times after warm-up, each replay timed with CUDA
+    events on that stream. Returns the median over the replays of the time per call;
+    `last` keeps the median, the mean and the replay count of the latest measurement."""
 
-    def __init__(self, stream):
+    def __init__(self, stream, replays: int = 20):
         import torch
         self.torch = torch
         self.stream = stream
+        self.replays = max(20, replays)
+        self.last = {}
 
     def __call__(self, fn, reps: int, warm: int = 3) -> float:
         """fn(i) runs call i; rows rotate i over input copies whose total exceeds L2."""
@@ -178,13 +182,17 @@ class Timer:
             for _ in range(warm):
                 g.replay()
         torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(self.replays + 1)]
         with torch.cuda.stream(self.stream):
-            s.record(self.stream)
-            g.replay()
-            e.record(self.stream)
+            ev[0].record(self.stream)
+            for r in range(self.replays):
+                g.replay()
+                ev[r + 1].record(self.stream)
         torch.cuda.synchronize()
-        return s.elapsed_time(e) * 1e3 / reps          # us per call
+        per_call = [ev[r].elapsed_time(ev[r + 1]) * 1e3 / reps for r in range(self.replays)]
+        self.last = {"median_us": statistics.median(per_call), "mean_us": statistics.fmean(per_call),
+                     "replays": self.replays, "calls_per_replay": reps}
+        return self.last["median_us"]
 
 
 def gpu_arm(args, rank, world, local_rank):
@@ -275,14 +283,18 @@ def gpu_arm(args, rank, world, local_rank):
     barrier(world)
     e_steps = max(3, args.steps // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e_steps):
             step_e2e()
         e1.record(stream)
     torch.cuda.synchronize()
+    wall_s = reduce_max(time.perf_counter() - w0, world, dev)
     te_ms = reduce_max(e0.elapsed_time(e1), world, dev)
     e2e_value = world * bytes_per_step * e_steps / (te_ms * 1e-3) / 1e9
+    e2e_wall = world * bytes_per_step * e_steps / wall_s / 1e9
     h2d = sum(host_a[M].numel() * host_a[M].element_size() for M in MS)
     d2h = sum(host_y[M].numel() * host_y[M].element_size() for M in MS)
 
@@ -298,6 +310,7 @@ def gpu_arm(args, rank, world, local_rank):
             qz.qz_gemm_w4a16(acts[M], q, s, Y=outs[M], stream=stream)
         us = timer(one, reps=200, warm=10)
         per_m[M] = {"kernel": "w4a16_bulk_kernel" if M <= 8 else "w4a16_kernel", "us": round(us, 3),
+                    "us_mean": round(timer.last["mean_us"], 3), "replays": timer.last["replays"],
                     "algorithmic_bytes": step_bytes(M), "gbps": round(step_bytes(M) / us / 1e3, 1),
                     "frac_of_hbm": round(step_bytes(M) / us / 1e3 / pk["hbm_gbs"], 4)}
     achieved = per_m[1]["gbps"]
@@ -321,7 +334,9 @@ def gpu_arm(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (8 rotating weight copies, 242 MB)",
                    "parallelism": f"replicas{world}"},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "host_wall_value": round(e2e_wall, 1),
+                "timing": "value: CUDA events on the stream; host_wall_value: host clock around the same "
+                          "steps, synchronised on both sides (includes enqueue cost)"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
         "clocks": clk.summary(),
@@ -363,6 +378,8 @@ def secondary_rows(qz, syn, stream, dev, pk, which):
         rows["quantizers"] = q
     if "qwen" in which:
         rows["qwen3_decode_step"] = qwen3_step(qz, syn, stream, dev, pk, timer, ws)
+    if "next" in which:
+        rows["variants"] = next_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows)
     return rows
 
 
@@ -542,6 +559,173 @@ def qwen3_step(qz, syn, stream, dev, pk, timer, ws):
     gws = qz.Workspace(dev)
     us = timer(lambda i: qz.qz_quantize_nvfp4_grouped(xs, outs=outs, ws=gws, stream=stream), 20)
     out["nvfp4_activation_quant_grouped_us"] = round(us, 2)
+
+    # the whole step as one CUDA graph: every linear of the 28 layers plus the FP8 KV write
+    # (the NVFP4 GEMMs read the activation codes the grouped quantizer writes in the same graph)
+    k, v = syn.kv_cache_inputs(seed=0)
+    k_d = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).to(dev)
+    v_d = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev)
+    kws = qz.Workspace(dev)
+    kv_out = qz.qz_kv_write_fp8(k_d, v_d, ws=kws, stream=stream)
+    kv_bytes = 2 * (k.size * 2 + k.size) + 8
+
+    def kv(i):
+        qz.qz_kv_write_fp8(k_d, v_d, k_codes=kv_out[0], v_codes=kv_out[1], k_scale=kv_out[2], v_scale=kv_out[3],
+                           ws=kws, stream=stream)
+
+    def step_w4(i):
+        qz.qz_gemm_w4a16_grouped(probs, stream=stream)
+        kv(i)
+
+    def step_nv(i):
+        qz.qz_quantize_nvfp4_grouped(xs, outs=outs, ws=gws, stream=stream)
+        qz.qz_gemm_nvfp4_grouped(nv_probs, ws=nws, stream=stream)
+        kv(i)
+    us = timer(step_w4, 10)
+    out["w4a16_step_with_kv_one_graph_us"] = round(us, 2)
+    out["w4a16_step_with_kv_frac_of_hbm"] = round((wbytes + kv_bytes) / us / 1e3 / pk["hbm_gbs"], 3)
+    act_bytes = sum(x.numel() * 2 + x.numel() // 2 + x.numel() // 16 + 4 for x in xs)
+    us = timer(step_nv, 10)
+    out["nvfp4_step_with_act_quant_and_kv_one_graph_us"] = round(us, 2)
+    out["nvfp4_step_with_act_quant_and_kv_frac_of_hbm"] = round(
+        (nvbytes + act_bytes + kv_bytes) / us / 1e3 / pk["hbm_gbs"], 3)
+    return out
+
+
+def next_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows):
+    """The variants beyond the base formats: INT4 with zero points and weight-only FP4 at
+    the decode shape, the per-head and per-channel-zero-point KV writes, SmoothQuant INT8
+    W8A8 at the prefill shape, the FP8 GEMM with its output quantized in the epilogue, and
+    W4A16 at prefill batch sizes (against cuBLAS bf16 and the FP8 GEMM)."""
+    import numpy as np
+    import torch
+    out = {}
+    fp16_peak = pk["bf16_tflops"]                 # the fp16 tensor rate equals the bf16 one
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+
+    # ---- decode shape (Llama-3.1-8B MLP 4096 x 14336): zero points and weight-only FP4
+    _, w = syn.w4a16_decode_inputs(M=1, seed=0)
+    w_d = torch.from_numpy(w).to(dev)
+    del w
+    with torch.cuda.stream(stream):
+        zq = qz.qz_quantize_int4_g128_zp(w_d, stream=stream)[:3]
+        bt = w_d.t().contiguous().to(torch.bfloat16)
+        nvw = qz.qz_quantize_nvfp4(bt, ws=ws, stream=stream)[:3]
+        mxw = qz.qz_quantize_mxfp4(bt, stream=stream)[:2]
+    stream.synchronize()
+    del w_d, bt
+    zc = [tuple(t.clone() for t in zq) for _ in range(COPIES)]
+    nvc = [tuple(t.clone() for t in nvw) for _ in range(COPIES)]
+    mxc = [tuple(t.clone() for t in mxw) for _ in range(COPIES)]
+    for M in (1, 16):
+        a_bits, _ = syn.w4a16_decode_inputs(M=M, seed=0, N=128)
+        A = bf(a_bits)
+        Y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=dev)
+        io = M * K_DIM * 2 + M * N_DIM * 2
+        cases = (
+            ("w4a16_zp", K_DIM * N_DIM // 2 + (K_DIM // 128) * N_DIM * 3 + io,
+             lambda i: qz.qz_gemm_w4a16_zp(A, *zc[i % COPIES], Y=Y, stream=stream)),
+            ("w4a16_nvfp4", K_DIM * N_DIM // 2 + K_DIM * N_DIM // 16 + 4 + io,
+             lambda i: qz.qz_gemm_w4a16_nvfp4(A, *nvc[i % COPIES], Y=Y, stream=stream)),
+            ("w4a16_mxfp4", K_DIM * N_DIM // 2 + K_DIM * N_DIM // 32 + io,
+             lambda i: qz.qz_gemm_w4a16_mxfp4(A, *mxc[i % COPIES], Y=Y, stream=stream)))
+        for name, by, fn in cases:
+            us = timer(fn, 8 * COPIES)
+            out[f"{name}_llama_mlp_M{M}"] = {"us": round(us, 3), "gbps": round(by / us / 1e3, 1),
+                                             "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3),
+                                             "algorithmic_bytes": by}
+    del zc, nvc, mxc
+
+    # ---- KV variants, 2 x [1, 8, 4096, 128] bf16
+    k, v = syn.kv_cache_inputs(seed=0)
+    n = copies_for(k.size * 2 * 3)
+    KV = [(bf(k), bf(v)) for _ in range(n)]
+    ph = [qz.qz_kv_write_fp8_per_head(a, b, ws=ws, stream=stream) for a, b in KV]
+    us = timer(lambda i: qz.qz_kv_write_fp8_per_head(*KV[i % n], k_codes=ph[i % n][0], v_codes=ph[i % n][1],
+                                                     k_scale=ph[i % n][2], v_scale=ph[i % n][3], ws=ws,
+                                                     stream=stream), 2 * n)
+    by = 2 * (k.size * 2 + k.size) + 2 * 8 * 4
+    out["kv_write_fp8_per_head_2x8x4096x128"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                                 "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    cz = [qz.qz_kv_write_fp8_channel_zp(a, b, ws=ws, stream=stream) for a, b in KV]
+    us = timer(lambda i: qz.qz_kv_write_fp8_channel_zp(*KV[i % n], *cz[i % n], ws=ws, stream=stream), 2 * n)
+    by = 2 * (k.size * 2 + k.size) + 8 * 128 * 8 + 8 * 4096 * 4
+    out["kv_write_fp8_k_channel_zp_v_token_2x8x4096x128"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                                             "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    del KV, ph, cz
+
+    # ---- SmoothQuant INT8 W8A8 at the prefill shape 2048 x 14336 x 4096
+    a, bt = syn.fp8_block_gemm_inputs(seed=0)
+    a_d, bt_d = bf(a), bf(bt)
+    M3, K3 = a_d.shape
+    N3 = bt_d.shape[0]
+    with torch.cuda.stream(stream):
+        s = qz.qz_smooth_factors(qz.qz_col_amax(a_d, ws=ws, stream=stream), qz.qz_col_amax(bt_d, ws=ws, stream=stream),
+                                 stream=stream)
+        qa, sa, _ = qz.qz_quantize_int8_rows(a_d, s, qz.SMOOTH_DIVIDE, stream=stream)
+        qb, sb, _ = qz.qz_quantize_int8_rows(bt_d, s, qz.SMOOTH_MULTIPLY, stream=stream)
+    stream.synchronize()
+    na = copies_for(a_d.numel() * 3)
+    As = [a_d] + [a_d.clone() for _ in range(na - 1)]
+    qas = [(torch.empty_like(qa), torch.empty_like(sa)) for _ in range(na)]
+    us = timer(lambda i: qz.qz_quantize_int8_rows(As[i % na], s, qz.SMOOTH_DIVIDE, codes=qas[i % na][0],
+                                                  scales=qas[i % na][1], stream=stream), 2 * na)
+    by = M3 * K3 * 2 + M3 * K3 + M3 * 4 + K3 * 4
+    out["int8_smooth_quantize_A_2048x4096_bf16"] = {"us": round(us, 2), "gbps": round(by / us / 1e3, 1),
+                                                    "frac_of_hbm": round(by / us / 1e3 / pk["hbm_gbs"], 3)}
+    del As, qas
+    ng = copies_for(M3 * K3 + N3 * K3 + M3 * N3 * 2)
+    ops = [(qa, sa, qb.clone(), sb) for _ in range(ng)]
+    ys = [torch.empty((M3, N3), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    us = timer(lambda i: qz.qz_gemm_int8(*ops[i % ng], Y=ys[i % 2], stream=stream), 2 * ng)
+    fl = 2.0 * M3 * N3 * K3
+    out["int8_w8a8_gemm_2048x14336x4096"] = {"us": round(us, 2), "tops": round(fl / us / 1e6, 1),
+                                             "peak_tflops_fp16_tensor": fp16_peak,
+                                             "frac_of_fp16_peak": round(fl / us / 1e6 / fp16_peak, 4)}
+    del ops
+
+    # ---- FP8 GEMM with the output quantized in the epilogue, against GEMM + 1x128 quantizer
+    ca, sca, _ = qz.qz_quantize_fp8(a_d, qz.FP8_GROUP_1x128, stream=stream)
+    cb, scb, _ = qz.qz_quantize_fp8(bt_d, qz.FP8_BLOCK_128x128, stream=stream)
+    del a_d, bt_d
+    cbs = [cb] + [cb.clone() for _ in range(ng - 1)]
+    yq = qz.qz_gemm_fp8_block_quant(ca, sca, cb, scb, stream=stream)
+    us_fused = timer(lambda i: qz.qz_gemm_fp8_block_quant(ca, sca, cbs[i % ng], scb, y_codes=yq[0], y_scales=yq[1],
+                                                          stream=stream), 2 * ng)
+    ysep = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+    sep_out = qz.qz_quantize_fp8(ysep, qz.FP8_GROUP_1x128, stream=stream)
+
+    def separate(i):
+        qz.qz_gemm_fp8_block(ca, sca, cbs[i % ng], scb, Y=ysep, stream=stream)
+        qz.qz_quantize_fp8(ysep, qz.FP8_GROUP_1x128, codes=sep_out[0], scales=sep_out[1], stream=stream)
+    us_sep = timer(separate, 2 * ng)
+    out["fp8_gemm_with_quantized_output_2048x14336x4096"] = {
+        "fused_us": round(us_fused, 2), "gemm_then_quantizer_us": round(us_sep, 2),
+        "tflops_fused": round(fl / us_fused / 1e6, 1), "frac_of_fp8_peak_fused": round(fl / us_fused / 1e6 / fp8_peak, 4),
+        "hbm_bytes_saved_per_call": M3 * N3 * 2 * 2,
+        "note": "fused: codes + scales only; separate: bf16 output written, read back and quantized"}
+    del cbs
+
+    # ---- W4A16 at prefill batch sizes: 2048 tokens as 32 slices of 64 through the grouped
+    # tcgen05 kernel (same weight, re-read from L2), against cuBLAS bf16 and the FP8 GEMM
+    _, wq = syn.w4a16_decode_inputs(M=1, seed=0)
+    wq_d = torch.from_numpy(wq).to(dev)
+    del wq
+    qw, sc, _ = qz.qz_quantize_int4_g128(wq_d, stream=stream)
+    wb = wq_d.to(torch.bfloat16)
+    del wq_d
+    Ap = bf(syn.fp8_block_gemm_inputs(seed=0, N=256)[0])
+    Yp = torch.empty((M3, N_DIM), dtype=torch.bfloat16, device=dev)
+    slices = [(Ap[i * 64:(i + 1) * 64], qw, sc, Yp[i * 64:(i + 1) * 64]) for i in range(M3 // 64)]
+    us_w4 = timer(lambda i: qz.qz_gemm_w4a16_grouped(slices, stream=stream), 4)
+    with torch.cuda.stream(stream):
+        torch.matmul(Ap, wb, out=Yp)
+    us_bf16 = timer(lambda i: torch.matmul(Ap, wb, out=Yp), 4)
+    out["w4a16_prefill_2048x14336x4096"] = {
+        "w4a16_us": round(us_w4, 2), "w4a16_tflops": round(fl / us_w4 / 1e6, 1),
+        "cublas_bf16_us": round(us_bf16, 2), "cublas_bf16_tflops": round(fl / us_bf16 / 1e6, 1),
+        "fp8_block_gemm_us": rows.get("fp8_block_gemm_2048x14336x4096", {}).get("us"),
+        "note": "W4A16 runs the 2048 tokens as 32 grouped slices of 64 (the kernel's widest token tile)"}
     return out
 
 
@@ -741,7 +925,7 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-ROW_NAMES = ("fp8", "fp4", "roundtrip", "kv", "qwen")
+ROW_NAMES = ("fp8", "fp4", "roundtrip", "kv", "qwen", "next")
 
 
 def build_parser() -> argparse.ArgumentParser:
@@ -751,8 +935,8 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qz", "reference"], default="qz")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary per-row measurements")
-    ap.add_argument("--rows", default="fp8,fp4,roundtrip,kv,qwen",
-                    help="secondary rows to measure (comma list of fp8, fp4, roundtrip, kv, qwen)")
+    ap.add_argument("--rows", default="fp8,fp4,roundtrip,kv,qwen,next",
+                    help="secondary rows to measure (comma list of fp8, fp4, roundtrip, kv, qwen, next)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--oracle-per-config", action="store_true",
