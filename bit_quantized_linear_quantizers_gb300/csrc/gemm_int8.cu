@@ -16,13 +16,13 @@
 //
 // Design (one CTA per SM, persistent over 128 x 256 output tiles, M fastest):
 //  warp 0      TMA producer: 64-byte-wide int8 boxes of A (128 rows) and B
-//              (256 rows) into a 4-stage ring.
-//  warps 2-5   converters: each int8 stage becomes an fp16 operand stage in the
+//              (256 rows) into a 3-stage ring.
+//  warps 2-9   converters: each int8 stage becomes an fp16 operand stage in the
 //              128-byte-swizzled K-major layout the tensor core reads (16-byte
-//              chunk c of row r at chunk c ^ (r & 7)); 2-stage ring.
+//              chunk c of row r at chunk c ^ (r & 7)); 3-stage ring.
 //  warp 1      MMA issuer (one thread): 4 x kind::f16 MMAs (M=128, N=256,
 //              K=16) per stage into one of two TMEM accumulators.
-//  warps 6-13  epilogue: each thread owns one row and 128 columns; loads the
+//  warps 10-17 epilogue: each thread owns one row and 128 columns; loads the
 //              accumulator (tcgen05.ld), applies sA * sB, rounds to bf16.
 #include "qz_tc.cuh"
 #include "qz_next.cuh"
@@ -36,12 +36,12 @@ namespace {
 __device__ unsigned int g_int8_err;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int IST = 4;                            // int8 stages
-constexpr int HST = 2;                            // fp16 stages
+constexpr int IST = 3;                            // int8 stages
+constexpr int HST = 3;                            // fp16 stages
 constexpr int IA = BM * BK, IB = BN * BK;         // int8 bytes per stage: 8 KB + 16 KB
 constexpr int HA = BM * BK * 2, HB = BN * BK * 2; // fp16 bytes per stage: 16 KB + 32 KB
 constexpr int I_STAGE = IA + IB, H_STAGE = HA + HB;
-constexpr int CONV_WARPS = 4, EPI_WARPS = 8;
+constexpr int CONV_WARPS = 8, EPI_WARPS = 8;
 constexpr int THREADS = (2 + CONV_WARPS + EPI_WARPS) * 32;
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -153,7 +153,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         __syncwarp();
     } else if (warp < 2 + CONV_WARPS) {
         // --------------------------------------------------------- converters
-        const int ct = threadIdx.x - 64;                            // 0..127
+        const int ct = threadIdx.x - 64;                            // 0 .. 32 * CONV_WARPS - 1
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -164,7 +164,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const uint8_t* src = smem + HST * H_STAGE + si * I_STAGE;
                 uint8_t* dst = smem + sh * H_STAGE;
                 // 384 rows (A's 128, then B's 256) x 4 input chunks of 16 bytes
-#pragma unroll 4
+#pragma unroll 2
                 for (int j = ct; j < (BM + BN) * 4; j += CONV_WARPS * 32) {
                     const int row = j >> 2, c = j & 3;
                     const uint4 v = *reinterpret_cast<const uint4*>(src + row * BK + c * 16);

@@ -211,6 +211,7 @@ kv_head_encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict
 __global__ void __launch_bounds__(kT)
 kzp_stats_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, float* __restrict__ partial) {
     __shared__ float smn[kT * 8], smx[kT * 8];
+    pdl_wait();
     const int oc = D / 8, lanes = kT / oc;
     const int o = threadIdx.x % oc, tl = threadIdx.x / oc;
     const int64_t y = blockIdx.y;
@@ -220,11 +221,16 @@ kzp_stats_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, float
 #pragma unroll
     for (int j = 0; j < 8; j++) { mn[j] = INFINITY; mx[j] = -INFINITY; }
     if (tl < lanes) {
-        for (int64_t t = t0 + tl; t < t1; t += lanes) {
-            float val[8];
-            Load8<uint16_t>::run(x + t * D + o * 8, val);
+        for (int64_t t = t0 + tl; t < t1; t += 4 * lanes) {     // four token rows in flight
+            float val[4][8];
 #pragma unroll
-            for (int j = 0; j < 8; j++) { mn[j] = fminf(mn[j], val[j]); mx[j] = fmaxf(mx[j], val[j]); }
+            for (int u = 0; u < 4; u++)
+                if (t + u * lanes < t1) Load8<uint16_t>::run(x + (t + u * lanes) * D + o * 8, val[u]);
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (t + u * lanes < t1)
+#pragma unroll
+                    for (int j = 0; j < 8; j++) { mn[j] = fminf(mn[j], val[u][j]); mx[j] = fmaxf(mx[j], val[u][j]); }
         }
     }
 #pragma unroll
@@ -247,34 +253,42 @@ kzp_stats_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, float
     pdl_trigger();
 }
 
-// Kernel 2: per head y, every CTA folds the token chunks' min/max into the
-// channel's zero point and scale (chunk 0 stores them), then encodes its
-// tokens: code = E4M3(fl(x - z) / s).
+// Kernel 2: one thread per channel folds the token chunks' min and max into
+// the channel's zero point and scale.
 __global__ void __launch_bounds__(kT)
-kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, const float* __restrict__ partial,
-                  uint8_t* __restrict__ codes, float* __restrict__ k_scale, float* __restrict__ k_zero) {
+kzp_finalize_kernel(const float* __restrict__ partial, int64_t BH, int D, int tc, float* __restrict__ k_scale,
+                    float* __restrict__ k_zero) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;          // channel (y, d)
+    if (i >= BH * D) return;
+    const int64_t y = i / D;
+    const int d = (int)(i - y * D);
+    float a = INFINITY, b = -INFINITY;
+    for (int c = 0; c < tc; c++) {
+        const float* p = partial + (y * tc + c) * 2 * D;
+        a = fminf(a, __ldg(p + d));
+        b = fmaxf(b, __ldg(p + D + d));
+    }
+    const float z = __fmul_rn(0.5f, __fadd_rn(b, a));
+    // fl(x - z) is monotone in x, so the largest |fl(x - z)| sits at an end of the range
+    const float amax = fmaxf(__fsub_rn(b, z), __fsub_rn(z, a));
+    k_zero[i] = z;
+    k_scale[i] = div1(fmaxf(amax, kAmaxMin), Recip(kFp8Max));
+}
+
+// Kernel 3: every CTA encodes its tokens of head y: code = E4M3(fl(x - z) / s).
+__global__ void __launch_bounds__(kT)
+kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, const float* __restrict__ k_scale,
+                  const float* __restrict__ k_zero, uint8_t* __restrict__ codes) {
     __shared__ float zs[256], ss[256], rs[256];
     pdl_wait();
     const int64_t y = blockIdx.y;
     if (threadIdx.x < D) {
-        const int d = threadIdx.x;
-        float a = INFINITY, b = -INFINITY;
-        for (int c = 0; c < tc; c++) {
-            const float* p = partial + (y * tc + c) * 2 * D;
-            a = fminf(a, __ldg(p + d));
-            b = fmaxf(b, __ldg(p + D + d));
-        }
-        const float z = __fmul_rn(0.5f, __fadd_rn(b, a));
-        // fl(x - z) is monotone in x, so the largest |fl(x - z)| sits at an end of the range
-        const float amax = fmaxf(__fsub_rn(b, z), __fsub_rn(z, a));
-        const float s = div1(fmaxf(amax, kAmaxMin), Recip(kFp8Max));
-        zs[d] = z;
-        ss[d] = s;
-        rs[d] = __frcp_rn(s);
-        if (blockIdx.x == 0) {
-            k_zero[y * D + d] = z;
-            k_scale[y * D + d] = s;
-        }
+        const float sv = __ldg(k_scale + y * D + threadIdx.x);
+        zs[threadIdx.x] = __ldg(k_zero + y * D + threadIdx.x);
+        ss[threadIdx.x] = sv;
+        rs[threadIdx.x] = __frcp_rn(sv);
     }
     __syncthreads();
     const int oc = D / 8, lanes = kT / oc;
@@ -298,6 +312,36 @@ kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, cons
         for (int j = 0; j < 4; j++) p[j] = e4m3x2(yq[2 * j], yq[2 * j + 1]);
         *reinterpret_cast<uint2*>(cy + t * D + o * 8) =
             make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
+    }
+}
+
+// V per token in one pass: D/8 threads per token row each hold 8 values; the
+// row's amax is a shuffle over those threads, then each encodes its 8 values.
+template <int TPR>
+__global__ void __launch_bounds__(kT)
+v_token_kernel(const uint16_t* __restrict__ v, int64_t rows, uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int D = TPR * 8;
+    const int64_t tid = (int64_t)blockIdx.x * kT + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * kT;
+    const int sub = threadIdx.x % TPR;
+    for (int64_t i = tid; i < ((rows * TPR + kT - 1) / kT) * kT; i += nthreads) {   // warp-uniform trip count
+        const int64_t r = i / TPR;
+        const bool live = r < rows;
+        float val[8];
+        if (live) Load8<uint16_t>::run(v + r * D + sub * 8, val);
+        else for (int j = 0; j < 8; j++) val[j] = 0.0f;
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(val[j]));
+#pragma unroll
+        for (int o = TPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float s = div1(fmaxf(m, kAmaxMin), Recip(kFp8Max));
+        if (live) {
+            reinterpret_cast<uint2*>(codes + r * D)[sub] = e4m3x8(val, Recip(s));
+            if (sub == 0) scales[r] = s;
+        }
     }
 }
 
@@ -345,11 +389,12 @@ smooth_factors_kernel(const float* __restrict__ xm, const float* __restrict__ wm
 
 // ------------------------------------------------------- INT8 per row
 
-// One warp per row: pass 1 the amax of x' (x / f or x * f per column, IEEE
-// rounded), pass 2 q = clamp(rint(x' / s), -128, 127) with s = max(amax,
-// 1e-12) / 127. Rows with cols % 8 == 0, 16-byte aligned.
-template <typename T, int OP>
-__device__ __forceinline__ void smooth8(float v[8], const float* f, int64_t c) {
+// Rows of up to 8192 columns: one CTA per row, the row read once into
+// registers (VPT values per thread), x' = x / f or x * f (IEEE rounded), the
+// row's amax reduced across the CTA, then q = clamp(rint(x' / s), -128, 127)
+// with s = max(amax, 1e-12) / 127 encoded from the registers.
+template <int OP>
+__device__ __forceinline__ void smooth8(float v[8], const float* __restrict__ f, int64_t c) {
     if (OP == QZ_SMOOTH_NONE) return;
     const float4 a = __ldg(reinterpret_cast<const float4*>(f + c));
     const float4 b = __ldg(reinterpret_cast<const float4*>(f + c) + 1);
@@ -358,6 +403,56 @@ __device__ __forceinline__ void smooth8(float v[8], const float* f, int64_t c) {
     for (int j = 0; j < 8; j++) v[j] = (OP == QZ_SMOOTH_DIVIDE) ? __fdiv_rn(v[j], fv[j]) : __fmul_rn(v[j], fv[j]);
 }
 
+__device__ __forceinline__ void int8_encode8(const float v[8], const Recip& d, float s, int8_t* codes, float* deq) {
+    uint32_t w[2] = {0u, 0u};
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float q = fminf(fmaxf(rintf(div1(v[j], d)), -128.0f), 127.0f);
+        w[j >> 2] |= ((uint32_t)(int)q & 0xFFu) << (8 * (j & 3));
+        o[j] = __fmul_rn(q, s);
+    }
+    *reinterpret_cast<uint2*>(codes) = make_uint2(w[0], w[1]);
+    if (deq) {
+        reinterpret_cast<float4*>(deq)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(deq)[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+template <typename T, int OP, int CPT>                // CPT: 8-element chunks per thread
+__global__ void __launch_bounds__(kT)
+int8_row_cta_kernel(const T* __restrict__ x, int64_t cols, const float* __restrict__ f,
+                    int8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    __shared__ float red[kW];
+    const int64_t r = blockIdx.x;
+    const T* xr = x + r * cols;
+    float v[CPT][8];
+#pragma unroll
+    for (int u = 0; u < CPT; u++) {
+        const int64_t c = ((int64_t)u * kT + threadIdx.x) * 8;
+        if (c < cols) Load8<T>::run(xr + c, v[u]);
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int u = 0; u < CPT; u++) {
+        const int64_t c = ((int64_t)u * kT + threadIdx.x) * 8;
+        if (c < cols) {
+            smooth8<OP>(v[u], f, c);
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+        }
+    }
+    const float s = div1(fmaxf(cta_max(m, red), kAmaxMin), Recip(127.0f));
+    if (threadIdx.x == 0) scales[r] = s;
+    const Recip d(s);
+#pragma unroll
+    for (int u = 0; u < CPT; u++) {
+        const int64_t c = ((int64_t)u * kT + threadIdx.x) * 8;
+        if (c < cols) int8_encode8(v[u], d, s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
+    }
+}
+
+// Wider rows: one warp per row, two passes (the second re-reads the row).
 template <typename T, int OP>
 __global__ void __launch_bounds__(kT)
 int8_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ f,
@@ -371,7 +466,7 @@ int8_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, const floa
         for (int64_t c = lane * 8; c < cols; c += 256) {
             float v[8];
             Load8<T>::run(xr + c, v);
-            smooth8<T, OP>(v, f, c);
+            smooth8<OP>(v, f, c);
 #pragma unroll
             for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[j]));
         }
@@ -381,20 +476,8 @@ int8_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, const floa
         for (int64_t c = lane * 8; c < cols; c += 256) {
             float v[8];
             Load8<T>::run(xr + c, v);
-            smooth8<T, OP>(v, f, c);
-            uint32_t w[2] = {0u, 0u};
-            float o[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const float q = fminf(fmaxf(rintf(div1(v[j], d)), -128.0f), 127.0f);
-                w[j >> 2] |= ((uint32_t)(int)q & 0xFFu) << (8 * (j & 3));
-                o[j] = __fmul_rn(q, s);
-            }
-            *reinterpret_cast<uint2*>(codes + r * cols + c) = make_uint2(w[0], w[1]);
-            if (deq) {
-                reinterpret_cast<float4*>(deq + r * cols + c)[0] = make_float4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<float4*>(deq + r * cols + c)[1] = make_float4(o[4], o[5], o[6], o[7]);
-            }
+            smooth8<OP>(v, f, c);
+            int8_encode8(v, d, s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
         }
     }
 }
@@ -456,13 +539,26 @@ qz_status kv_channel_zp_launch(const uint16_t* k, const uint16_t* v, int64_t B, 
     const int tc = kzp_chunks(BH, T);
     const dim3 grid(tc, (unsigned)BH);
     float* partial = (float*)ws;
-    kzp_stats_kernel<<<grid, kT, 0, st>>>(k, T, (int)D, tc, partial);
-    QZ_TRY(launch_status());
-    QZ_TRY(launch_pdl(kzp_encode_kernel, grid, dim3(kT), st, k, T, (int)D, tc, (const float*)partial, kc, k_scale,
-                      k_zero));
-    QZ_TRY(launch_status());
-    // V per token: one scale per (b, h, t) over its D values
-    return quantize_fp8_launch(v, QZ_BF16, BH * T, D, D, QZ_FP8_PER_ROW, vc, v_scale, nullptr, nullptr, 0, st);
+    // V per token (one pass), then K per channel: min/max per chunk, fold, encode
+    const int64_t vrows = BH * T;
+    const int tpr = (int)(D / 8);
+    const int vgrid = (int)std::max<int64_t>(1, std::min<int64_t>((vrows * tpr + kT - 1) / kT, (int64_t)num_sms() * 8));
+    qz_status sv;
+    switch (tpr) {
+    case 1: sv = launch_pdl(v_token_kernel<1>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    case 2: sv = launch_pdl(v_token_kernel<2>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    case 4: sv = launch_pdl(v_token_kernel<4>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    case 8: sv = launch_pdl(v_token_kernel<8>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    case 16: sv = launch_pdl(v_token_kernel<16>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    default: sv = launch_pdl(v_token_kernel<32>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    }
+    QZ_TRY(sv);
+    QZ_TRY(launch_pdl(kzp_stats_kernel, grid, dim3(kT), st, k, T, (int)D, tc, partial));
+    QZ_TRY(launch_pdl(kzp_finalize_kernel, dim3((unsigned)((BH * D + kT - 1) / kT)), dim3(kT), st,
+                      (const float*)partial, BH, (int)D, tc, k_scale, k_zero));
+    QZ_TRY(launch_pdl(kzp_encode_kernel, grid, dim3(kT), st, k, T, (int)D, tc, (const float*)k_scale,
+                      (const float*)k_zero, kc));
+    return launch_status();
 }
 
 qz_status col_amax_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, float* out, void* ws,
@@ -485,22 +581,34 @@ qz_status smooth_factors_launch(const float* xm, const float* wm, int64_t n, flo
     return launch_status();
 }
 
+template <typename T, int OP>
+qz_status launch_i8(const void* x, int64_t rows, int64_t cols, const float* f, int8_t* codes, float* scales,
+                    float* deq, cudaStream_t st) {
+    const int64_t cpt = (cols / 8 + kT - 1) / kT;               // chunks per thread, one CTA per row
+    switch (cpt) {
+    case 1: int8_row_cta_kernel<T, OP, 1><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
+    case 2: int8_row_cta_kernel<T, OP, 2><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
+    case 3: int8_row_cta_kernel<T, OP, 3><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
+    case 4: int8_row_cta_kernel<T, OP, 4><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
+    default: {
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kW - 1) / kW, (int64_t)num_sms() * 8));
+        int8_rows_kernel<T, OP><<<grid, kT, 0, st>>>((const T*)x, rows, cols, f, codes, scales, deq);
+    }
+    }
+    return launch_status();
+}
+
 qz_status int8_rows_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, const float* f, int op,
                            int8_t* codes, float* scales, float* deq, cudaStream_t st) {
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kW - 1) / kW, (int64_t)num_sms() * 8));
-#define QZ_INT8_LAUNCH(T, OPV)                                                                               \
-    int8_rows_kernel<T, OPV><<<grid, kT, 0, st>>>((const T*)x, rows, cols, f, codes, scales, deq)
+    if (rows > 0x7FFFFFFF) return QZ_ERR_SHAPE;
     if (xt == QZ_F32) {
-        if (op == QZ_SMOOTH_NONE) QZ_INT8_LAUNCH(float, QZ_SMOOTH_NONE);
-        else if (op == QZ_SMOOTH_DIVIDE) QZ_INT8_LAUNCH(float, QZ_SMOOTH_DIVIDE);
-        else QZ_INT8_LAUNCH(float, QZ_SMOOTH_MULTIPLY);
-    } else {
-        if (op == QZ_SMOOTH_NONE) QZ_INT8_LAUNCH(uint16_t, QZ_SMOOTH_NONE);
-        else if (op == QZ_SMOOTH_DIVIDE) QZ_INT8_LAUNCH(uint16_t, QZ_SMOOTH_DIVIDE);
-        else QZ_INT8_LAUNCH(uint16_t, QZ_SMOOTH_MULTIPLY);
+        if (op == QZ_SMOOTH_NONE) return launch_i8<float, QZ_SMOOTH_NONE>(x, rows, cols, f, codes, scales, deq, st);
+        if (op == QZ_SMOOTH_DIVIDE) return launch_i8<float, QZ_SMOOTH_DIVIDE>(x, rows, cols, f, codes, scales, deq, st);
+        return launch_i8<float, QZ_SMOOTH_MULTIPLY>(x, rows, cols, f, codes, scales, deq, st);
     }
-#undef QZ_INT8_LAUNCH
-    return launch_status();
+    if (op == QZ_SMOOTH_NONE) return launch_i8<uint16_t, QZ_SMOOTH_NONE>(x, rows, cols, f, codes, scales, deq, st);
+    if (op == QZ_SMOOTH_DIVIDE) return launch_i8<uint16_t, QZ_SMOOTH_DIVIDE>(x, rows, cols, f, codes, scales, deq, st);
+    return launch_i8<uint16_t, QZ_SMOOTH_MULTIPLY>(x, rows, cols, f, codes, scales, deq, st);
 }
 
 } // namespace qz

@@ -445,7 +445,9 @@ qz_status qz_gemm_fp8_block_quant(const uint8_t* qA, const float* sA, const uint
  *   larger sizes return QZ_ERR_SHAPE and launch nothing.
  * Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture on the device.
+ *   before any stream capture on the device. The address belongs to the
+ *   device's primary context (the CUDA runtime's); it is not looked up again,
+ *   so it is stale after cudaDeviceReset or under another context.
  * Sharing: every call uses the same array and leaves its last contents there;
  *   nothing in it needs to start at zero (each call writes every byte it later
  *   reads). Calls whose executions overlap on the GPU (different streams, no
