@@ -56,11 +56,13 @@ def pack(codes):
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
 
 
+@pytest.mark.parametrize("M", [128, 256, 640])
 @pytest.mark.parametrize("fmt", ["nv", "mx"])
-def test_fp4_gemm_integer_exact(qz, fmt):
-    """Unit scales and E2M1 codes of small integers: an exact integer matmul."""
-    rng = np.random.default_rng(1)
-    M, N, K = 128, 256, 256
+def test_fp4_gemm_integer_exact(qz, fmt, M):
+    """Unit scales and E2M1 codes of small integers: an exact integer matmul, over one and
+    several 128-row tiles."""
+    rng = np.random.default_rng(1 + M)
+    N, K = 256, 256
     mag = np.array([0, 2, 4, 5, 6, 7])                    # 0, 1, 2, 3, 4, 6
     ca = (rng.choice(mag, (M, K)) | (rng.integers(0, 2, (M, K)) << 3)).astype(np.uint8)
     cb = (rng.choice(mag, (N, K)) | (rng.integers(0, 2, (N, K)) << 3)).astype(np.uint8)
@@ -78,7 +80,8 @@ def test_fp4_gemm_integer_exact(qz, fmt):
     assert np.array_equal(bf16_bits_to_f64(y), bf16_bits_to_f64(syn.to_bf16_bits(ref)))
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256),
+                                   (256, 256, 256), (640, 256, 512), (1152, 1024, 768)])
 def test_nvfp4_gemm(qz, M, N, K):
     a, bt = inputs(M, N, K, seed=M + N + K)
     y, ops = nv_run(qz, a, bt)
@@ -86,7 +89,8 @@ def test_nvfp4_gemm(qz, M, N, K):
     check(y, y_ref, bound, f"nvfp4 {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 1024), (256, 512, 512), (384, 768, 256),
+                                   (256, 256, 256), (640, 256, 512), (1152, 1024, 768)])
 def test_mxfp4_gemm(qz, M, N, K):
     a, bt = inputs(M, N, K, seed=M + N + K + 1)
     y, ops = mx_run(qz, a, bt)
