@@ -8,18 +8,23 @@
 // MMA's M side, the tokens its N side (N = MT = 32 or 64), so one staged
 // activation slice serves 128 weight columns. Per CTA (one per SM, persistent
 // over tiles of 128 weight columns x all of K, several problems per launch):
-//  warp 0       TMA producer: per 128-deep K group, the packed weights (16
-//               k-octet rows x 128 columns of int32, 8 KB) and the activations
-//               (two 64-element x MT boxes, 128-byte swizzle) into a ring.
+//  The pipeline moves in units of GU = 2 groups of 128 K (one stage, one TMEM
+//  weight buffer, one hand-off between the warps per unit): each hand-off
+//  costs a few hundred ns of mbarrier wake-up whatever the work behind it.
+//  warp 0       TMA producer: per unit, for each of its 128-deep K groups the
+//               packed weights (16 k-octet rows x 128 columns of int32, 8 KB)
+//               and the activations (two 64-element x MT boxes, 128-byte
+//               swizzle) into a ring.
 //  warps 2-9    unpack: thread = one weight column (its TMEM lane); each of
 //               its packed words (8 consecutive k) becomes 8 exact bf16
 //               integers q in [-8, 7], and the 64 K of the thread's half of
-//               the group go straight from registers into tensor memory
+//               each group go straight from registers into tensor memory
 //               (tcgen05.st), which is where the MMA reads its A operand from
 //               (double-buffered, 64 TMEM columns per group).
 //  warp 1       MMA issuer (one thread): per group 8 x tcgen05.mma kind::f16
 //               with A in TMEM and the activations from shared memory
-//               (M = 128, N = MT, K = 16) into one of four TMEM accumulators.
+//               (M = 128, N = MT, K = 16) into the group's own TMEM
+//               accumulator (two units of accumulators in flight).
 //  warps 10-13  promotion + epilogue: thread = one weight column (its TMEM
 //               lane); per group it loads the MT partial sums, multiplies them
 //               by the group's bf16 scale and adds them into fp32 registers
@@ -40,10 +45,11 @@ namespace {
 __device__ unsigned int g_w4tc_err;
 
 constexpr int TN = 128;                           // weight columns per tile (MMA M)
-constexpr int GK = 128;                           // K per group = per pipeline stage
+constexpr int GK = 128;                           // K per group (one bf16 scale per column)
+constexpr int GU = 2;                             // groups per pipeline unit
 constexpr int W_BYTES = (GK / 8) * TN * 4;        // packed weights of one group: 8 KB
-constexpr int NWT = 2;                            // unpacked weight tiles (in TMEM) in flight
-constexpr int NACC = 4;                           // TMEM accumulators in flight
+constexpr int NWT = 2;                            // unpacked weight units (in TMEM) in flight
+constexpr int NAU = 2;                            // accumulator units in flight (GU accumulators each)
 constexpr int UNPACK_WARPS = 8, PROMO_WARPS = 4;
 constexpr int THREADS = (2 + UNPACK_WARPS + PROMO_WARPS) * 32;
 constexpr int TC_PER_LAUNCH = 80;                 // problems per launch (kernel parameter space)
@@ -65,12 +71,15 @@ struct TcParams {
 
 template <int MT>
 struct TcLayout {
-    static constexpr int A_BYTES = MT * GK * 2;                       // two 64 x MT boxes
-    static constexpr int STAGE = (W_BYTES + A_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = MT == 64 ? 8 : 12;      // 196 KB of ring
+    static constexpr int A_BYTES = MT * GK * 2;                       // two 64 x MT boxes per group
+    static constexpr int A_OFF = GU * W_BYTES;                        // activations after the weights
+    static constexpr int STAGE = (GU * (W_BYTES + A_BYTES) + 1023) / 1024 * 1024;
+    static constexpr int STAGES = MT == 64 ? 4 : 6;       // 192 KB of ring
     static constexpr int SMEM = STAGES * STAGE + 512 + 1024;
-    static constexpr uint32_t ACC_COLS = NACC * MT;                     // accumulators first
-    static constexpr uint32_t TMEM_COLS = ACC_COLS + NWT * 64 <= 128 ? 128 : ACC_COLS + NWT * 64 <= 256 ? 256 : 512;
+    static constexpr uint32_t ACC_COLS = NAU * GU * MT;                 // accumulators first
+    static constexpr uint32_t WCOLS = GU * 64;                          // TMEM columns of one weight unit
+    static constexpr uint32_t TMEM_COLS = ACC_COLS + NWT * WCOLS <= 128 ? 128
+                                        : ACC_COLS + NWT * WCOLS <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC = idesc_dense(1u, 1u, TN, MT);   // bf16 x bf16 -> fp32
 };
 
@@ -123,8 +132,8 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
     auto wfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
     auto wempty = [&](int b) { return smem_u32(bars + 2 * S + NWT + b); };
     auto afull = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + b); };
-    auto aempty = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + NACC + b); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NWT + 2 * NACC);
+    auto aempty = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + NAU + b); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NWT + 2 * NAU);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto find = [&](int tile) {                   // last problem with tile_begin <= tile
@@ -145,7 +154,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
             mbar_init(wfull(b), UNPACK_WARPS);
             mbar_init(wempty(b), 1);
         }
-        for (int b = 0; b < NACC; b++) {
+        for (int b = 0; b < NAU; b++) {
             mbar_init(afull(b), 1);
             mbar_init(aempty(b), PROMO_WARPS);
         }
@@ -174,18 +183,22 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
                 const int ng = pr.K / GK;
                 prefetch_tmap(&pr.tmW);
                 prefetch_tmap(&pr.tmA);
-                for (int g = 0; g < ng; g++, it++) {
-                    const int s = it % S;
+                for (int g0 = 0; g0 < ng; g0 += GU, it++) {
+                    const int s = it % S, gu = min(GU, ng - g0);
                     if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
                     const uint32_t st = sbase + s * L::STAGE;
-                    mbar_arrive_expect_tx(full(s), W_BYTES + L::A_BYTES);
-                    tma_load_2d(st, &pr.tmW, n0, g * (GK / 8), full(s));              // columns past N: zeros
+                    mbar_arrive_expect_tx(full(s), (uint32_t)gu * (W_BYTES + L::A_BYTES));
+                    for (int j = 0; j < gu; j++)                                    // columns past N: zeros
+                        tma_load_2d(st + j * W_BYTES, &pr.tmW, n0, (g0 + j) * (GK / 8), full(s));
                     if (!waited) {
                         asm volatile("griddepcontrol.wait;" ::: "memory");
                         waited = true;
                     }
-                    tma_load_2d(st + W_BYTES, &pr.tmA, g * GK, 0, full(s));           // tokens past M: zeros
-                    tma_load_2d(st + W_BYTES + MT * 128, &pr.tmA, g * GK + 64, 0, full(s));
+                    for (int j = 0; j < gu; j++) {                                  // tokens past M: zeros
+                        const uint32_t sa = st + L::A_OFF + j * L::A_BYTES;
+                        tma_load_2d(sa, &pr.tmA, (g0 + j) * GK, 0, full(s));
+                        tma_load_2d(sa + MT * 128, &pr.tmA, (g0 + j) * GK + 64, 0, full(s));
+                    }
                 }
             }
             for (uint32_t j = it > (uint32_t)S ? it - S : 0; j < it; j++)
@@ -198,26 +211,29 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
             bool ok = true;
             for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
                 const int ng = P.p[find(tile)].K / GK;
-                for (int g = 0; g < ng; g++, it++) {
-                    const int s = it % S, wb = it % NWT, ab = it % NACC;
-                    if (!mbar_wait(aempty(ab), ((it / NACC) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
+                for (int g0 = 0; g0 < ng; g0 += GU, it++) {
+                    const int s = it % S, wb = it % NWT, ab = it % NAU, gu = min(GU, ng - g0);
+                    if (!mbar_wait(aempty(ab), ((it / NAU) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
                     if (!mbar_wait(full(s), (it / S) & 1, &g_w4tc_err)) { ok = false; break; }
                     if (!mbar_wait(wfull(wb), (it / NWT) & 1, &g_w4tc_err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d = tmem_base + ab * MT;
+                    for (int j = 0; j < gu; j++) {
+                        const uint32_t d = tmem_base + (uint32_t)(ab * GU + j) * MT;
+                        const uint32_t sa = sbase + s * L::STAGE + L::A_OFF + j * L::A_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < GK / 16; ks++) {               // K = 16 per MMA = 8 TMEM columns
-                        const int slab = ks >> 2, kk = ks & 3;           // 64-element slab, 32-byte step
-                        const uint32_t at = tmem_base + L::ACC_COLS + wb * 64 + ks * 8;
-                        const uint64_t bd = sdesc_k_sw128(sbase + s * L::STAGE + W_BYTES + slab * (MT * 128)) + kk * 2;
-                        mma_bf16_ts(d, at, bd, L::IDESC, ks > 0);
+                        for (int ks = 0; ks < GK / 16; ks++) {           // K = 16 per MMA = 8 TMEM columns
+                            const int slab = ks >> 2, kk = ks & 3;       // 64-element slab, 32-byte step
+                            const uint32_t at = tmem_base + L::ACC_COLS + wb * L::WCOLS + j * 64 + ks * 8;
+                            const uint64_t bd = sdesc_k_sw128(sa + slab * (MT * 128)) + kk * 2;
+                            mma_bf16_ts(d, at, bd, L::IDESC, ks > 0);
+                        }
                     }
                     tc_commit(empty(s));
                     tc_commit(wempty(wb));
                     tc_commit(afull(ab));
                 }
             }
-            if (it > 0) mbar_wait(afull((it - 1) % NACC), ((it - 1) / NACC) & 1, &g_w4tc_err);
+            if (it > 0) mbar_wait(afull((it - 1) % NAU), ((it - 1) / NAU) & 1, &g_w4tc_err);
         }
         __syncwarp();
     } else if (warp < 2 + UNPACK_WARPS) {
@@ -228,22 +244,24 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
         bool ok = true;
         for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
             const int ng = P.p[find(tile)].K / GK;
-            for (int g = 0; g < ng; g++, it++) {
-                const int s = it % S, wb = it % NWT;
+            for (int g0 = 0; g0 < ng; g0 += GU, it++) {
+                const int s = it % S, wb = it % NWT, gu = min(GU, ng - g0);
                 if (!mbar_wait(full(s), (it / S) & 1, &g_w4tc_err)) { ok = false; break; }
                 if (!mbar_wait(wempty(wb), ((it / NWT) & 1) ^ 1, &g_w4tc_err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(smem + s * L::STAGE);
-                uint32_t o[32];
+                for (int j = 0; j < gu; j++) {
+                    const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(smem + s * L::STAGE + j * W_BYTES);
+                    uint32_t o[32];
 #pragma unroll
-                for (int i = 0; i < 8; i++) {                    // k-octet rows 8h .. 8h+7
-                    const uint32_t w = wsrc[(8 * h + i) * TN + n], w4 = w >> 4;
-                    o[4 * i + 0] = unpack_pair<0>(w, w4);
-                    o[4 * i + 1] = unpack_pair<1>(w, w4);
-                    o[4 * i + 2] = unpack_pair<2>(w, w4);
-                    o[4 * i + 3] = unpack_pair<3>(w, w4);
+                    for (int i = 0; i < 8; i++) {                // k-octet rows 8h .. 8h+7
+                        const uint32_t w = wsrc[(8 * h + i) * TN + n], w4 = w >> 4;
+                        o[4 * i + 0] = unpack_pair<0>(w, w4);
+                        o[4 * i + 1] = unpack_pair<1>(w, w4);
+                        o[4 * i + 2] = unpack_pair<2>(w, w4);
+                        o[4 * i + 3] = unpack_pair<3>(w, w4);
+                    }
+                    tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + L::ACC_COLS + wb * L::WCOLS + j * 64 + h * 32, o);
                 }
-                tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + L::ACC_COLS + wb * 64 + h * 32, o);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -265,21 +283,31 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
             float acc[MT];
 #pragma unroll
             for (int i = 0; i < MT; i++) acc[i] = 0.0f;
-            uint32_t sraw = __ldg(srow);                  // scale of group 0, then one group ahead
-            for (int g = 0; g < ng; g++, it++) {
-                const float sc = bf16_bits_to_f32(sraw);
-                if (g + 1 < ng) sraw = __ldg(srow + (size_t)(g + 1) * pr.N);
-                const int ab = it % NACC;
-                if (!mbar_wait(afull(ab), (it / NACC) & 1, &g_w4tc_err)) { ok = false; break; }
+            uint32_t sraw[GU];                            // scales of the unit's groups, one unit ahead
+#pragma unroll
+            for (int j = 0; j < GU; j++) sraw[j] = j < ng ? __ldg(srow + (size_t)j * pr.N) : 0u;
+            for (int g0 = 0; g0 < ng; g0 += GU, it++) {
+                const int gu = min(GU, ng - g0);
+                float sc[GU];
+#pragma unroll
+                for (int j = 0; j < GU; j++) {
+                    sc[j] = bf16_bits_to_f32(sraw[j]);
+                    const int gn = g0 + GU + j;
+                    if (gn < ng) sraw[j] = __ldg(srow + (size_t)gn * pr.N);
+                }
+                const int ab = it % NAU;
+                if (!mbar_wait(afull(ab), (it / NAU) & 1, &g_w4tc_err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * MT;
+                for (int j = 0; j < gu; j++) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * GU + j) * MT;
 #pragma unroll
-                for (int c = 0; c < MT / 16; c++) {
-                    uint32_t v[16];
-                    tmem_ld16(taddr + c * 16, v);
-                    tmem_wait_ld();
+                    for (int c = 0; c < MT / 16; c++) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + c * 16, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c * 16 + i]);
+                        for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(__uint_as_float(v[i]), sc[j], acc[c * 16 + i]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
