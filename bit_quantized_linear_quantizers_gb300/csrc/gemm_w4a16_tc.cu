@@ -29,8 +29,10 @@
 //               lane); per group it loads the MT partial sums, multiplies them
 //               by the group's bf16 scale and adds them into fp32 registers
 //               (the scale is not folded into bf16 weights, which would round);
-//               at the end of the tile it rounds to bf16 and stores column n of
-//               every token row.
+//               at the end of the tile it rounds to bf16 into a shared-memory
+//               tile [MT][128], from which each promotion warp's lane 0 writes
+//               its rows to Y with bulk asynchronous stores (one 256-byte row
+//               each), so the warps return to the accumulators at once.
 // Every wait is bounded; on expiry the kernel records QZ_ERR_TIMEOUT and winds
 // down.
 #include "qz_tc.cuh"
@@ -75,7 +77,9 @@ struct TcLayout {
     static constexpr int A_OFF = GU * W_BYTES;                        // activations after the weights
     static constexpr int STAGE = (GU * (W_BYTES + A_BYTES) + 1023) / 1024 * 1024;
     static constexpr int STAGES = MT == 64 ? 4 : 6;       // 192 KB of ring
-    static constexpr int SMEM = STAGES * STAGE + 512 + 1024;
+    static constexpr int YT_OFF = STAGES * STAGE + 1024;                // output tile after the barriers
+    static constexpr int YT_BYTES = MT * TN * 2;
+    static constexpr int SMEM = YT_OFF + YT_BYTES + 1024;
     static constexpr uint32_t ACC_COLS = NAU * GU * MT;                 // accumulators first
     static constexpr uint32_t WCOLS = GU * 64;                          // TMEM columns of one weight unit
     static constexpr uint32_t TMEM_COLS = ACC_COLS + NWT * WCOLS <= 128 ? 128
@@ -133,7 +137,10 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
     auto wempty = [&](int b) { return smem_u32(bars + 2 * S + NWT + b); };
     auto afull = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + b); };
     auto aempty = [&](int b) { return smem_u32(bars + 2 * S + 2 * NWT + NAU + b); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NWT + 2 * NAU);
+    auto ep_free = [&]() { return smem_u32(bars + 2 * S + 2 * NWT + 2 * NAU); };      // output tile free
+    auto ep_full = [&]() { return smem_u32(bars + 2 * S + 2 * NWT + 2 * NAU + 1); };  // output tile written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NWT + 2 * NAU + 2);
+    uint16_t* ytile = reinterpret_cast<uint16_t*>(smem + L::YT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto find = [&](int tile) {                   // last problem with tile_begin <= tile
@@ -158,6 +165,8 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
             mbar_init(afull(b), 1);
             mbar_init(aempty(b), PROMO_WARPS);
         }
+        mbar_init(ep_free(), PROMO_WARPS);
+        mbar_init(ep_full(), PROMO_WARPS);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -272,7 +281,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
         // ------------------------------------------------ promotion + epilogue
         const int q = warp & 3;                          // TMEM lane quarter
         const int n = q * 32 + lane;                     // weight column within the tile
-        uint32_t it = 0;
+        uint32_t it = 0, tcount = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < P.total_tiles && ok; tile += gridDim.x) {
             const TcProb& pr = P.p[find(tile)];
@@ -314,14 +323,37 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
                 if (lane == 0) mbar_arrive(aempty(ab));
             }
             if (!ok) break;
-            if (col_ok) {
-                const int mrows = min(pr.M, MT);
-                uint16_t* ycol = pr.Y + n0 + n;
-#pragma unroll
-                for (int m = 0; m < MT; m++)
-                    if (m < mrows) ycol[(size_t)m * pr.N] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+            // the output tile: free (this warp's stores of the last tile have read
+            // it), written by all four warps, then stored row by row
+            const uint32_t tp = tcount & 1;
+            if (lane == 0) {
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(ep_free());
             }
+            if (!mbar_wait(ep_free(), tp, &g_w4tc_err)) break;
+#pragma unroll
+            for (int m = 0; m < MT; m++) ytile[m * TN + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(ep_full());
+                if (!mbar_wait(ep_full(), tp, &g_w4tc_err)) { ok = false; }
+                else {
+                    const int mrows = min(pr.M, MT);
+                    const uint32_t rb = (uint32_t)min(TN, pr.N - n0) * 2;           // bytes of a row in Y
+                    for (int m = q; m < mrows; m += PROMO_WARPS) {
+                        const uint32_t src = smem_u32(ytile + m * TN);
+                        uint16_t* dst = pr.Y + (size_t)m * pr.N + n0;
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                     ::"l"(dst), "r"(src), "r"(rb) : "memory");
+                    }
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            tcount++;
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
