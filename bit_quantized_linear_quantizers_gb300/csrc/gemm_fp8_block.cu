@@ -44,7 +44,31 @@ constexpr int SD = 2;                            // K blocks of scales kept in f
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+// Each epilogue warp stages 32 rows x 128 bytes of its bf16 output in its own
+// slice of shared memory (16-byte chunks swizzled by row), then writes them back
+// row-wise: eight lanes cover one row's 128 contiguous bytes, so a store
+// instruction writes four whole 128-byte row segments instead of 32 scattered
+// 16-byte pieces (110.3 -> 107.7 us at 2048 x 14336 x 4096).
+constexpr int STG_OFF = STAGES * STAGE_BYTES + 1024;
+constexpr int STG_WARP = 32 * 128;
+constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_WARP + 1024;
+constexpr int SMEM_BYTES_Q = STAGES * STAGE_BYTES + 256 + 1024;   // quantized output: no staging
+
+// Row-wise write-back of a warp's staged 32 x 128-byte block: row i goes to
+// dst + i * pitch (bytes), 16-byte aligned.
+__device__ __forceinline__ void stage_put(uint8_t* stg, int lane, int j, uint4 v) {
+    *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+}
+__device__ __forceinline__ void stage_flush(const uint8_t* stg, int lane, uint8_t* dst, size_t pitch) {
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; it++) {
+        const int rr = it * 4 + (lane >> 3), c = lane & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+        *reinterpret_cast<uint4*>(dst + (size_t)rr * pitch + c * 16) = v;
+    }
+    __syncwarp();
+}
 
 // QOUT: the epilogue also quantizes its output for the next layer, FP8 E4M3
 // with one scale per row and 128 columns ("量化部署实战", 练习 2: the
@@ -146,6 +170,7 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const int q = warp & 3;                   // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;            // column slice of the 256-wide tile
         const int r = q * 32 + lane;              // row within the tile
+        uint8_t* stg = QOUT ? nullptr : smem + STG_OFF + (warp - 2) * STG_WARP;
         uint32_t ac = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -220,17 +245,37 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 Yqs[(size_t)(m0 + r) * (N / 128) + (n0 + h * EPI_COLS) / 128] = sq;
                 if (Y == nullptr) continue;
             }
-            uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * EPI_COLS);
-#pragma unroll
-            for (int j = 0; j < EPI_COLS / 8; j++) {
-                uint4 o;
-                uint32_t* w = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    __nv_bfloat162 p = __floats2bfloat162_rn(acc[j * 8 + 2 * e], acc[j * 8 + 2 * e + 1]);
-                    w[e] = *reinterpret_cast<uint32_t*>(&p);
+            if constexpr (!QOUT) {
+                #pragma unroll
+                for (int hf = 0; hf < EPI_COLS / 64; hf++) {          // 64 bf16 columns = 128 bytes a row
+                    #pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        uint4 o;
+                        uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+                        #pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int c = hf * 64 + j * 8 + 2 * e;
+                            __nv_bfloat162 p = __floats2bfloat162_rn(acc[c], acc[c + 1]);
+                            w[e] = *reinterpret_cast<uint32_t*>(&p);
+                        }
+                        stage_put(stg, lane, j, o);
+                    }
+                    stage_flush(stg, lane, reinterpret_cast<uint8_t*>(Y + (size_t)(m0 + q * 32) * N + n0 + h * EPI_COLS + hf * 64),
+                                (size_t)N * 2);
                 }
-                yrow[j] = o;
+            } else {
+                uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * EPI_COLS);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 8; j++) {
+                    uint4 o;
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        __nv_bfloat162 p = __floats2bfloat162_rn(acc[j * 8 + 2 * e], acc[j * 8 + 2 * e + 1]);
+                        w[e] = *reinterpret_cast<uint32_t*>(&p);
+                    }
+                    yrow[j] = o;
+                }
             }
         }
     }
@@ -266,8 +311,8 @@ qz_status gemm_fp8_block_quant_launch(const uint8_t* qA, const float* sA, const 
     const int tiles = (M / BM) * (N / BN);
     const int grid = std::min(tiles, num_sms());
     if (Yq) {
-        QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<true>, SMEM_BYTES));
-        fp8_block_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, Yq, Yqs, M, N, K);
+        QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<true>, SMEM_BYTES_Q));
+        fp8_block_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES_Q, st>>>(ta, tb, sA, sB, Y, Yq, Yqs, M, N, K);
     } else {
         QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<false>, SMEM_BYTES));
         fp8_block_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, nullptr, nullptr, M, N, K);
