@@ -54,6 +54,12 @@ constexpr int STG_WARP = 32 * 128;
 constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_WARP + 1024;
 constexpr int SMEM_BYTES_Q = STAGES * STAGE_BYTES + 256 + 1024;   // quantized output: no staging
 
+// acc (two fp32 lanes) += v * s per lane, each lane one correctly rounded fma
+// (the paired fp32 FMA of sm_100+: half the instructions of two fmaf).
+__device__ __forceinline__ void fma2(uint64_t& acc, uint32_t v0, uint32_t v1, uint64_t s2) {
+    asm("{ .reg .b64 t; mov.b64 t, {%1, %2}; fma.rn.f32x2 %0, t, %3, %0; }" : "+l"(acc) : "r"(v0), "r"(v1), "l"(s2));
+}
+
 // Row-wise write-back of a warp's staged 32 x 128-byte block: row i goes to
 // dst + i * pitch (bytes), 16-byte aligned.
 __device__ __forceinline__ void stage_put(uint8_t* stg, int lane, int j, uint4 v) {
@@ -177,9 +183,14 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int m0 = (tile % mt) * BM, n0 = (tile / mt) * BN;
             const float* sa_row = sA + (size_t)(m0 + r) * nkb;
             const float* sb_row = sB + (size_t)((n0 + h * EPI_COLS) / 128) * nkb;
-            float acc[EPI_COLS];
+            // plain output: columns 2i, 2i+1 as one fp32 pair (paired FMAs, 106.9 -> 104.2 us);
+            // the output-quantizing instance keeps scalar FMAs (its epilogue needs the registers)
+            uint64_t acc2[QOUT ? 1 : EPI_COLS / 2];
+            float accf[QOUT ? EPI_COLS : 1];
 #pragma unroll
-            for (int i = 0; i < EPI_COLS; i++) acc[i] = 0.0f;
+            for (int i = 0; i < (QOUT ? 1 : EPI_COLS / 2); i++) acc2[i] = 0ull;
+#pragma unroll
+            for (int i = 0; i < (QOUT ? EPI_COLS : 1); i++) accf[i] = 0.0f;
             // Scales of the next SD K blocks stay in flight as raw loads (an L2
             // round trip is longer than one block's MMAs); each is multiplied out
             // only when its block is promoted, so no load is waited on early.
@@ -195,6 +206,7 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     const int kb = kb0 + u;
                     if (kb >= nkb || !ok) break;
                     const float scale = ra[u] * rb[u];
+                    const uint64_t s2 = ((uint64_t)__float_as_uint(scale) << 32) | __float_as_uint(scale);
                     if (kb + SD < nkb) {
                         ra[u] = __ldg(sa_row + kb + SD);
                         rb[u] = __ldg(sb_row + kb + SD);
@@ -208,9 +220,14 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         uint32_t v[16];
                         tmem_ld16(taddr + c * 16, v);
                         tmem_wait_ld();
+                        if constexpr (QOUT) {
 #pragma unroll
-                        for (int i = 0; i < 16; i++)
-                            acc[c * 16 + i] = fmaf(__uint_as_float(v[i]), scale, acc[c * 16 + i]);
+                            for (int i = 0; i < 16; i++)
+                                accf[c * 16 + i] = fmaf(__uint_as_float(v[i]), scale, accf[c * 16 + i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; i++) fma2(acc2[c * 8 + i], v[2 * i], v[2 * i + 1], s2);
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -219,6 +236,17 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
             }
             if (!ok) break;
+            float acc[EPI_COLS];
+            if constexpr (QOUT) {
+#pragma unroll
+                for (int i = 0; i < EPI_COLS; i++) acc[i] = accf[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPI_COLS / 2; i++) {
+                    acc[2 * i] = __uint_as_float((uint32_t)acc2[i]);
+                    acc[2 * i + 1] = __uint_as_float((uint32_t)(acc2[i] >> 32));
+                }
+            }
             if (QOUT) {
                 // the bf16 output (what this kernel would store), then its 1x128 FP8 group:
                 // s = max(amax, 1e-12) / 448, code = E4M3(y / s), quotients correctly rounded
