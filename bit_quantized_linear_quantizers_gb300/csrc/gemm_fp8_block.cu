@@ -176,7 +176,6 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const int q = warp & 3;                   // TMEM lane quarter of this warp
         const int h = (warp - 2) >> 2;            // column slice of the 256-wide tile
         const int r = q * 32 + lane;              // row within the tile
-        uint8_t* stg = QOUT ? nullptr : smem + STG_OFF + (warp - 2) * STG_WARP;
         uint32_t ac = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -274,6 +273,9 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 if (Y == nullptr) continue;
             }
             if constexpr (!QOUT) {
+                // re-derived here: keeping the aligned base live through the
+                // promotion loop costs registers (spills at the 168-register cap)
+                uint8_t* stg = smem_raw + (STG_OFF + (warp - 2) * STG_WARP + (smem - smem_raw));
                 #pragma unroll
                 for (int hf = 0; hf < EPI_COLS / 64; hf++) {          // 64 bf16 columns = 128 bytes a row
                     #pragma unroll
