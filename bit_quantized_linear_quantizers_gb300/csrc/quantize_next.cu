@@ -205,17 +205,14 @@ kv_head_encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict
 
 // ------------------------------------ K per channel with a zero point
 
-// Kernel 1: per head y and token chunk x, the min and max of every channel d
-// over the chunk's tokens: partial[((y * tc + x) * 2 + {0 min, 1 max}) * D + d].
+// Launch 1, K part: per head y and token chunk x, the min and max of every
+// channel d over the chunk's tokens: partial[((y * tc + x) * 2 + {0 min, 1 max}) * D + d].
 // Thread layout: D/8 channel octets x (256 / (D/8)) token lanes.
-__global__ void __launch_bounds__(kT)
-kzp_stats_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, float* __restrict__ partial) {
-    __shared__ float smn[kT * 8], smx[kT * 8];
-    pdl_wait();
+__device__ __forceinline__ void kzp_stats(const uint16_t* __restrict__ k, int64_t T, int D, int tc, int64_t y, int cx,
+                                          float* __restrict__ partial, float* smn, float* smx) {
     const int oc = D / 8, lanes = kT / oc;
     const int o = threadIdx.x % oc, tl = threadIdx.x / oc;
-    const int64_t y = blockIdx.y;
-    const int64_t t0 = T * blockIdx.x / tc, t1 = T * (blockIdx.x + 1) / tc;
+    const int64_t t0 = T * cx / tc, t1 = T * (cx + 1) / tc;
     const uint16_t* x = k + y * T * D;
     float mn[8], mx[8];
 #pragma unroll
@@ -246,49 +243,40 @@ kzp_stats_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, float
             a = fminf(a, smn[(l * oc + od) * 8 + jd]);
             b = fmaxf(b, smx[(l * oc + od) * 8 + jd]);
         }
-        float* p = partial + (y * tc + blockIdx.x) * 2 * D;
+        float* p = partial + (y * tc + cx) * 2 * D;
         p[d] = a;
         p[D + d] = b;
     }
-    pdl_trigger();
 }
 
-// Kernel 2: one thread per channel folds the token chunks' min and max into
-// the channel's zero point and scale.
+// Launch 2: every CTA (token chunk x, head y) first folds the head's chunk
+// minima and maxima into each channel's zero point and scale (the CTAs of
+// chunk 0 store them), then encodes its tokens: code = E4M3(fl(x - z) / s).
 __global__ void __launch_bounds__(kT)
-kzp_finalize_kernel(const float* __restrict__ partial, int64_t BH, int D, int tc, float* __restrict__ k_scale,
-                    float* __restrict__ k_zero) {
-    pdl_wait();
-    pdl_trigger();
-    const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;          // channel (y, d)
-    if (i >= BH * D) return;
-    const int64_t y = i / D;
-    const int d = (int)(i - y * D);
-    float a = INFINITY, b = -INFINITY;
-    for (int c = 0; c < tc; c++) {
-        const float* p = partial + (y * tc + c) * 2 * D;
-        a = fminf(a, __ldg(p + d));
-        b = fmaxf(b, __ldg(p + D + d));
-    }
-    const float z = __fmul_rn(0.5f, __fadd_rn(b, a));
-    // fl(x - z) is monotone in x, so the largest |fl(x - z)| sits at an end of the range
-    const float amax = fmaxf(__fsub_rn(b, z), __fsub_rn(z, a));
-    k_zero[i] = z;
-    k_scale[i] = div1(fmaxf(amax, kAmaxMin), Recip(kFp8Max));
-}
-
-// Kernel 3: every CTA encodes its tokens of head y: code = E4M3(fl(x - z) / s).
-__global__ void __launch_bounds__(kT)
-kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, const float* __restrict__ k_scale,
-                  const float* __restrict__ k_zero, uint8_t* __restrict__ codes) {
+kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, const float* __restrict__ partial,
+                  float* __restrict__ k_scale, float* __restrict__ k_zero, uint8_t* __restrict__ codes) {
     __shared__ float zs[256], ss[256], rs[256];
     pdl_wait();
     const int64_t y = blockIdx.y;
     if (threadIdx.x < D) {
-        const float sv = __ldg(k_scale + y * D + threadIdx.x);
-        zs[threadIdx.x] = __ldg(k_zero + y * D + threadIdx.x);
-        ss[threadIdx.x] = sv;
-        rs[threadIdx.x] = __frcp_rn(sv);
+        const int d = threadIdx.x;
+        float a = INFINITY, b = -INFINITY;
+        for (int c = 0; c < tc; c++) {
+            const float* p = partial + (y * tc + c) * 2 * D;
+            a = fminf(a, __ldcg(p + d));
+            b = fmaxf(b, __ldcg(p + D + d));
+        }
+        const float z = __fmul_rn(0.5f, __fadd_rn(b, a));
+        // fl(x - z) is monotone in x, so the largest |fl(x - z)| sits at an end of the range
+        const float amax = fmaxf(__fsub_rn(b, z), __fsub_rn(z, a));
+        const float sv = div1(fmaxf(amax, kAmaxMin), Recip(kFp8Max));
+        if (blockIdx.x == 0) {
+            k_zero[y * D + d] = z;
+            k_scale[y * D + d] = sv;
+        }
+        zs[d] = z;
+        ss[d] = sv;
+        rs[d] = __frcp_rn(sv);
     }
     __syncthreads();
     const int oc = D / 8, lanes = kT / oc;
@@ -317,14 +305,13 @@ kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, cons
 
 // V per token in one pass: D/8 threads per token row each hold 8 values; the
 // row's amax is a shuffle over those threads, then each encodes its 8 values.
+// CTA vb of nvb takes a grid-stride share of the rows.
 template <int TPR>
-__global__ void __launch_bounds__(kT)
-v_token_kernel(const uint16_t* __restrict__ v, int64_t rows, uint8_t* __restrict__ codes, float* __restrict__ scales) {
-    pdl_wait();
-    pdl_trigger();
+__device__ __forceinline__ void v_token(const uint16_t* __restrict__ v, int64_t rows, uint8_t* __restrict__ codes,
+                                        float* __restrict__ scales, int64_t vb, int64_t nvb) {
     constexpr int D = TPR * 8;
-    const int64_t tid = (int64_t)blockIdx.x * kT + threadIdx.x;
-    const int64_t nthreads = (int64_t)gridDim.x * kT;
+    const int64_t tid = vb * kT + threadIdx.x;
+    const int64_t nthreads = nvb * kT;
     const int sub = threadIdx.x % TPR;
     for (int64_t i = tid; i < ((rows * TPR + kT - 1) / kT) * kT; i += nthreads) {   // warp-uniform trip count
         const int64_t r = i / TPR;
@@ -343,6 +330,22 @@ v_token_kernel(const uint16_t* __restrict__ v, int64_t rows, uint8_t* __restrict
             if (sub == 0) scales[r] = s;
         }
     }
+}
+
+// Launch 1: the first tc * BH CTAs take the K statistics (chunk x, head y), the
+// remaining ones encode V per token; the two parts are independent.
+template <int TPR>
+__global__ void __launch_bounds__(kT)
+kzp_stats_v_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t BH, int64_t T, int tc,
+                   float* __restrict__ partial, uint8_t* __restrict__ vc, float* __restrict__ v_scale) {
+    __shared__ float smn[kT * 8], smx[kT * 8];
+    pdl_wait();
+    const int64_t kblocks = BH * tc;
+    if ((int64_t)blockIdx.x < kblocks)
+        kzp_stats(k, T, TPR * 8, tc, (int64_t)blockIdx.x / tc, (int)((int64_t)blockIdx.x % tc), partial, smn, smx);
+    else
+        v_token<TPR>(v, BH * T, vc, v_scale, (int64_t)blockIdx.x - kblocks, (int64_t)gridDim.x - kblocks);
+    pdl_trigger();
 }
 
 // ------------------------------------------------ SmoothQuant statistics
@@ -537,27 +540,24 @@ qz_status kv_channel_zp_launch(const uint16_t* k, const uint16_t* v, int64_t B, 
                                cudaStream_t st) {
     const int64_t BH = B * H;
     const int tc = kzp_chunks(BH, T);
-    const dim3 grid(tc, (unsigned)BH);
     float* partial = (float*)ws;
-    // V per token (one pass), then K per channel: min/max per chunk, fold, encode
+    // one launch for K's statistics and V per token, one for K's scales and codes
     const int64_t vrows = BH * T;
     const int tpr = (int)(D / 8);
-    const int vgrid = (int)std::max<int64_t>(1, std::min<int64_t>((vrows * tpr + kT - 1) / kT, (int64_t)num_sms() * 8));
-    qz_status sv;
+    const int64_t vblocks = std::max<int64_t>(1, std::min<int64_t>((vrows * tpr + kT - 1) / kT, (int64_t)num_sms() * 2));
+    const dim3 g1((unsigned)(BH * tc + vblocks));
+    qz_status s1;
     switch (tpr) {
-    case 1: sv = launch_pdl(v_token_kernel<1>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
-    case 2: sv = launch_pdl(v_token_kernel<2>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
-    case 4: sv = launch_pdl(v_token_kernel<4>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
-    case 8: sv = launch_pdl(v_token_kernel<8>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
-    case 16: sv = launch_pdl(v_token_kernel<16>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
-    default: sv = launch_pdl(v_token_kernel<32>, dim3(vgrid), dim3(kT), st, v, vrows, vc, v_scale); break;
+    case 1: s1 = launch_pdl(kzp_stats_v_kernel<1>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
+    case 2: s1 = launch_pdl(kzp_stats_v_kernel<2>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
+    case 4: s1 = launch_pdl(kzp_stats_v_kernel<4>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
+    case 8: s1 = launch_pdl(kzp_stats_v_kernel<8>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
+    case 16: s1 = launch_pdl(kzp_stats_v_kernel<16>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
+    default: s1 = launch_pdl(kzp_stats_v_kernel<32>, g1, dim3(kT), st, k, v, BH, T, tc, partial, vc, v_scale); break;
     }
-    QZ_TRY(sv);
-    QZ_TRY(launch_pdl(kzp_stats_kernel, grid, dim3(kT), st, k, T, (int)D, tc, partial));
-    QZ_TRY(launch_pdl(kzp_finalize_kernel, dim3((unsigned)((BH * D + kT - 1) / kT)), dim3(kT), st,
-                      (const float*)partial, BH, (int)D, tc, k_scale, k_zero));
-    QZ_TRY(launch_pdl(kzp_encode_kernel, grid, dim3(kT), st, k, T, (int)D, tc, (const float*)k_scale,
-                      (const float*)k_zero, kc));
+    QZ_TRY(s1);
+    QZ_TRY(launch_pdl(kzp_encode_kernel, dim3(tc, (unsigned)BH), dim3(kT), st, k, T, (int)D, tc,
+                      (const float*)partial, k_scale, k_zero, kc));
     return launch_status();
 }
 
