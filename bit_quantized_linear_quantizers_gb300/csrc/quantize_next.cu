@@ -285,21 +285,27 @@ kzp_encode_kernel(const uint16_t* __restrict__ k, int64_t T, int D, int tc, cons
     const int64_t t0 = T * blockIdx.x / tc, t1 = T * (blockIdx.x + 1) / tc;
     const uint16_t* x = k + y * T * D;
     uint8_t* cy = codes + y * T * D;
-    for (int64_t t = t0 + tl; t < t1; t += lanes) {
-        float val[8];
-        Load8<uint16_t>::run(x + t * D + o * 8, val);
-        float yq[8];
+    for (int64_t t = t0 + tl; t < t1; t += 4 * lanes) {          // four token rows in flight
+        float val[4][8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int d = o * 8 + j;
-            const float r = __fsub_rn(val[j], zs[d]);
-            yq[j] = sign_of(div1(r, Recip(ss[d], rs[d])), r);
+        for (int u = 0; u < 4; u++)
+            if (t + u * lanes < t1) Load8<uint16_t>::run(x + (t + u * lanes) * D + o * 8, val[u]);
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            if (t + u * lanes >= t1) break;
+            float yq[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int d = o * 8 + j;
+                const float r = __fsub_rn(val[u][j], zs[d]);
+                yq[j] = sign_of(div1(r, Recip(ss[d], rs[d])), r);
+            }
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) p[j] = e4m3x2(yq[2 * j], yq[2 * j + 1]);
+            *reinterpret_cast<uint2*>(cy + (t + u * lanes) * D + o * 8) =
+                make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
         }
-        uint32_t p[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) p[j] = e4m3x2(yq[2 * j], yq[2 * j + 1]);
-        *reinterpret_cast<uint2*>(cy + t * D + o * 8) =
-            make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
     }
 }
 
