@@ -85,7 +85,7 @@ __device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, ui
 __device__ __forceinline__ uint2 fp4_encode16(const float v[16], const Recip& d, float* deq) {
     float y[16];
 #pragma unroll
-    for (int j = 0; j < 16; j++) y[j] = div1(v[j], d);
+    for (int j = 0; j < 16; j += 2) div1x2(v[j], v[j + 1], d, y[j], y[j + 1]);
     const uint2 packed = make_uint2(e2m1x8_tiesdown(y), e2m1x8_tiesdown(y + 8));
     if (deq) {
         float o[16];

@@ -87,6 +87,21 @@ __device__ __forceinline__ float div1(float x, const Recip& d) {
     return __fmaf_rn(rem, d.r, q0);
 }
 
+// Two quotients at once with the paired fp32 instructions of sm_100+ (each
+// lane rounds exactly as the scalar mul / fma): the same three steps as div1,
+// the negation moved onto the scale (fma(q0, -s, x) == fma(-q0, s, x)).
+__device__ __forceinline__ void div1x2(float a, float b, const Recip& d, float& qa, float& qb) {
+    asm("{ .reg .b64 x, r2, ns2, q0, rem, q;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 r2, {%4, %4};\n\t"
+        "mov.b64 ns2, {%5, %5};\n\t"
+        "mul.rn.f32x2 q0, x, r2;\n\t"
+        "fma.rn.f32x2 rem, q0, ns2, x;\n\t"
+        "fma.rn.f32x2 q, rem, r2, q0;\n\t"
+        "mov.b64 {%0, %1}, q; }"
+        : "=f"(qa), "=f"(qb) : "f"(a), "f"(b), "f"(d.r), "f"(-d.s));
+}
+
 // y with the sign bit of x (a non-zero quotient already has it; fixes -0).
 __device__ __forceinline__ float sign_of(float y, float x) {
     return __uint_as_float(__float_as_uint(y) | (__float_as_uint(x) & 0x80000000u));
@@ -124,7 +139,13 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float y[8]) {
 __device__ __forceinline__ uint32_t e2m1x8_tiesdown(const float y[8]) {
     float p[8];
 #pragma unroll
-    for (int j = 0; j < 8; j++) p[j] = __fmaf_rn(y[j], -0x1.0p-24f, y[j]);
+    for (int j = 0; j < 8; j += 2)                               // pred of two quotients per paired fma
+        asm("{ .reg .b64 y2, c2, p2;\n\t"
+            "mov.b64 y2, {%2, %3};\n\t"
+            "mov.b64 c2, {%4, %4};\n\t"
+            "fma.rn.f32x2 p2, y2, c2, y2;\n\t"
+            "mov.b64 {%0, %1}, p2; }"
+            : "=f"(p[j]), "=f"(p[j + 1]) : "f"(y[j]), "f"(y[j + 1]), "f"(-0x1.0p-24f));
     const uint32_t w1 = e2m1x8_rne(y), w2 = e2m1x8_rne(p);
     const uint32_t odd = (w1 & 0x11111111u) * 15u;               // nibbles of w1 with an odd code, all ones
     return w2 ^ ((w1 ^ w2) & odd);
