@@ -185,6 +185,29 @@ def test_fp4_ulp_above_midpoints(qz):
     check_nv(qz, syn.to_bf16_bits(x), "nv bf16 midpoints", amax_in=2688.0)
 
 
+def test_fp4_tiny_values_beside_huge_ones(qz):
+    """Blocks whose amax is huge hold tiny values (down to bf16 subnormals) of both signs,
+    zeros of both signs and values one step either side of midpoints: the quotients of the
+    tiny ones underflow to fp32 subnormals or to zero, where the sign of a zero code and
+    the step toward zero must still follow the oracle (fp32 and bf16 inputs)."""
+    rng = np.random.default_rng(21)
+    x = np.zeros((8, 64), np.float32)
+    tiny = np.float32([1e-39, -1e-39, 9.2e-41, -9.2e-41, 1e-45, -1e-45, 2.0 ** -133, -(2.0 ** -133),
+                       1e-30, -1e-30, 0.0, -0.0, 3e-38, -3e-38])
+    for r in range(8):
+        big = np.float32(2.0 ** (r * 16 - 20)) * np.float32(1.5 + r / 8)
+        for b in range(2):
+            row = x[r, b * 32:(b + 1) * 32]
+            row[0] = big if (r + b) % 2 == 0 else -big
+            row[1:1 + len(tiny)] = tiny
+            row[1 + len(tiny):] = rng.standard_normal(31 - len(tiny)).astype(np.float32) * big * np.float32(1e-3)
+    check_mx(qz, x, "mx tiny beside huge")
+    xb = syn.to_bf16_bits(x)
+    check_mx(qz, xb, "mx bf16 tiny beside huge")
+    check_nv(qz, x, "nv tiny beside huge")
+    check_nv(qz, xb, "nv bf16 tiny beside huge")
+
+
 def test_nvfp4_given_amax(qz):
     x = edge_tensor(64, 256, seed=8)
     check_nv(qz, x, "nv given amax", amax_in=float(np.abs(x).max()) * 2.0)
