@@ -69,8 +69,11 @@ struct Prob {
     int tile_begin;                     // first tile index of this problem
 };
 
-struct Params {
-    Prob p[PER_LAUNCH];
+// Kernel parameter block of NP problems: a single call passes a one-problem
+// block, so its launch does not copy a table sized for a whole group.
+template <int NP>
+struct ParamsN {
+    Prob p[NP];
     int count;
     int total_tiles;
 };
@@ -333,8 +336,9 @@ struct SaProb {
     int cta_begin;                      // first CTA of this problem
 };
 
-struct SaParams {
-    SaProb p[SA_MAX_PROBLEMS];
+template <int NP>                       // NP = 1 for a single call, SA_MAX_PROBLEMS for a group
+struct SaParamsN {
+    SaProb p[NP];
     int count;
 };
 
@@ -360,9 +364,9 @@ __device__ __forceinline__ void mma_bf16_z(float c[4], const uint32_t a[4], uint
 }
 
 // ONE: every problem of the launch has a single token.
-template <bool ONE>
+template <bool ONE, int NP>
 __global__ void __launch_bounds__(RD_WARPS * 32, 3)
-w4a16_bulk_kernel(const __grid_constant__ SaParams P) {
+w4a16_bulk_kernel(const __grid_constant__ SaParamsN<NP> P) {
     extern __shared__ uint8_t sa_dyn[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sa_dyn) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -504,9 +508,9 @@ w4a16_bulk_kernel(const __grid_constant__ SaParams P) {
 
 // ------------------------------------------------ TMA-staged kernel
 
-template <int MT>
+template <int MT, int NP>
 __global__ void __launch_bounds__((2 * ntmax_for(MT) / 16 + 1) * 32, 1)
-w4a16_kernel(const __grid_constant__ Params P, int nt, int ns) {
+w4a16_kernel(const __grid_constant__ ParamsN<NP> P, int nt, int ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int MB = MT / 8;                       // 8-token MMA blocks
@@ -745,8 +749,9 @@ qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st
 
 // Bulk-staged launch for up to 8 tokens and K <= SA_KMAX: one CTA per 32
 // columns of every problem, programmatic dependent launch.
-qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
-    SaParams P;                                   // the kernel parameter block (copied at launch)
+template <int NP>
+qz_status launch_bulk_n(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+    SaParamsN<NP> P;                              // the kernel parameter block (copied at launch)
     int total = 0, kmax = 0, mmax = 0;
     P.count = count;
     for (int i = 0; i < count; i++) {
@@ -773,9 +778,9 @@ qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t 
     {
         std::lock_guard<std::mutex> lock(smem_mu);
         if (smem > smem_set[dev]) {
-            if (cudaFuncSetAttribute(w4a16_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            if (cudaFuncSetAttribute(w4a16_bulk_kernel<true, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                     cudaSuccess ||
-                cudaFuncSetAttribute(w4a16_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaFuncSetAttribute(w4a16_bulk_kernel<false, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                     cudaSuccess)
                 return QZ_ERR_CUDA;
             smem_set[dev] = smem;
@@ -791,14 +796,18 @@ qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = mmax == 1 ? cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<true>, P)
-                                    : cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<false>, P);
+    const cudaError_t e = mmax == 1 ? cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<true, NP>, P)
+                                    : cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<false, NP>, P);
     if (e != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
-template <int MT>
-qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
+qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+    return count == 1 ? launch_bulk_n<1>(problems, count, st) : launch_bulk_n<SA_MAX_PROBLEMS>(problems, count, st);
+}
+
+template <int MT, int NP>
+qz_status launch_mt(const ParamsN<NP>& P, int nt, cudaStream_t st) {
     // One persistent CTA per SM (or per tile, if fewer), ring as deep as fits.
     const Layout L(nt, MT);
     const uint32_t budget = 200u * 1024u;
@@ -813,7 +822,7 @@ qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
     {
         std::lock_guard<std::mutex> lock(smem_mu);
         if (smem > smem_set[dev]) {
-            if (cudaFuncSetAttribute(w4a16_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            if (cudaFuncSetAttribute(w4a16_kernel<MT, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                     cudaSuccess)
                 return QZ_ERR_CUDA;
             smem_set[dev] = smem;
@@ -831,12 +840,13 @@ qz_status launch_mt(const Params& P, int nt, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w4a16_kernel<MT>, P, nt, ns) != cudaSuccess) return QZ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, w4a16_kernel<MT, NP>, P, nt, ns) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
-qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
-    Params P;                                     // the kernel parameter block (copied at launch)
+template <int NP>
+qz_status launch_chunk_n(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
+    ParamsN<NP> P;                                // the kernel parameter block (copied at launch)
     int total = 0;
     P.count = count;
     for (int i = 0; i < count; i++) {
@@ -853,7 +863,12 @@ qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int 
         total += (q.N + nt - 1) / nt;
     }
     P.total_tiles = total;
-    return launch_mt<16>(P, nt, st);             // 9..16 tokens (the only width this kernel serves)
+    return launch_mt<16, NP>(P, nt, st);         // 9..16 tokens (the only width this kernel serves)
+}
+
+qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
+    return count == 1 ? launch_chunk_n<1>(problems, count, nt, mt, st)
+                      : launch_chunk_n<PER_LAUNCH>(problems, count, nt, mt, st);
 }
 
 } // namespace
