@@ -134,8 +134,9 @@ struct RdProb {
     int cta_begin;                      // first CTA of this problem
 };
 
-struct RdParams {
-    RdProb p[RD_MAX_PROBLEMS];
+template <int NP>                       // NP = 1 for a single call, RD_MAX_PROBLEMS for a group
+struct RdParamsN {
+    RdProb p[NP];
     int count;
 };
 
@@ -177,9 +178,9 @@ __device__ __forceinline__ void rd_load(RdGroup& G, const RdProb& pr, int n0, in
 
 // ZP: unsigned codes with one zero point per group and column; the group sum
 // is sum(a * (u + 128)) - (128 + z) * sum(a).
-template <int MT, bool ZP = false>
+template <int MT, bool ZP, int NP>
 __global__ void __launch_bounds__(RD_WARPS * 32, MT <= 8 ? 3 : 2)
-w4a16_rd_kernel(const __grid_constant__ RdParams P) {
+w4a16_rd_kernel(const __grid_constant__ RdParamsN<NP> P) {
     constexpr int MB = MT / 8;
     __shared__ float red[RD_WARPS][MT][RD_COLS + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -716,9 +717,9 @@ int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
 // Register-direct launch for up to 8 tokens: one CTA per 32 columns of every
 // problem, programmatic dependent launch.
-template <int MT, bool ZP = false>
-qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros = nullptr) {
-    RdParams P;                                   // the kernel parameter block (copied at launch)
+template <int MT, bool ZP, int NP>
+qz_status launch_rd_n(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros) {
+    RdParamsN<NP> P;                              // the kernel parameter block (copied at launch)
     int total = 0;
     P.count = count;
     for (int i = 0; i < count; i++) {
@@ -743,8 +744,14 @@ qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT, ZP>, P) != cudaSuccess) return QZ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT, ZP, NP>, P) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
+}
+
+template <int MT, bool ZP = false>
+qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros = nullptr) {
+    return count == 1 ? launch_rd_n<MT, ZP, 1>(problems, count, st, zeros)
+                      : launch_rd_n<MT, ZP, RD_MAX_PROBLEMS>(problems, count, st, zeros);
 }
 
 // Bulk-staged launch for up to 8 tokens and K <= SA_KMAX: one CTA per 32
