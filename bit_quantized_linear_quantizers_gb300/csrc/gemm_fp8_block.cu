@@ -40,7 +40,7 @@ constexpr int B_BYTES = BN * BK;                  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);   // columns per promotion thread
-constexpr int SD = 2;                            // K blocks of scales kept in flight
+constexpr int SD = 1;                            // K blocks of scales kept in flight
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
