@@ -217,7 +217,8 @@ def int8_operands(M, N, K, seed):
     return qa, sa, qb, sb
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 512), (256, 512, 1024), (384, 768, 192)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 512), (256, 512, 1024), (384, 768, 192),
+                                   (640, 512, 256)])
 def test_int8_gemm_full_check(qz, M, N, K):
     qa, sa, qb, sb = int8_operands(M, N, K, seed=M + N + K)
     y = host(qz.qz_gemm_int8(dev(qa), dev_f32(sa), dev(qb), dev_f32(sb)))
