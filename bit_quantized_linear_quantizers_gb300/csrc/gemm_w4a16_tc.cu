@@ -87,26 +87,6 @@ struct TcLayout {
     static constexpr uint32_t IDESC = idesc_dense(1u, 1u, TN, MT);   // bf16 x bf16 -> fp32
 };
 
-// D (TMEM) (+)= A (TMEM, 128 lanes x K/2 columns of bf16 pairs) x B (smem desc)
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
-                 ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
-// 32 consecutive 32-bit columns of this thread's TMEM lane from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-                   "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-                   "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-                   "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-                   "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 // Packed word -> 8 exact bf16 integers (element 2B in the low nibble of byte B,
 // two's complement). One byte-permute brings the even code of byte B (from w)
 // and the odd one (from w >> 4) into the low nibbles of the two halves; one
@@ -234,7 +214,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
                             const int slab = ks >> 2, kk = ks & 3;       // 64-element slab, 32-byte step
                             const uint32_t at = tmem_base + L::ACC_COLS + wb * L::WCOLS + j * 64 + ks * 8;
                             const uint64_t bd = sdesc_k_sw128(sa + slab * (MT * 128)) + kk * 2;
-                            mma_bf16_ts(d, at, bd, L::IDESC, ks > 0);
+                            mma_f16_ts(d, at, bd, L::IDESC, ks > 0);
                         }
                     }
                     tc_commit(empty(s));
