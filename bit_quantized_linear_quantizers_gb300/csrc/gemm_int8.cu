@@ -254,15 +254,25 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t tc = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, tc++) {
             const int nc = (tile / mt) * BN + ch * EPI_COLS;        // this thread's first column
+            // the tile's scales are fetched while its accumulators fill: sA of this thread's two
+            // rows, sB of column nc + 32 c + lane (shared across the warp by shuffles)
+            float sav[MH], sbv[EPI_COLS / 32];
+#pragma unroll
+            for (int mh = 0; mh < MH; mh++) {
+                const int m = (tile % mt) * TM + mh * BM + r;
+                sav[mh] = m < M ? __ldg(sA + m) : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < EPI_COLS / 32; c++) sbv[c] = nc + c * 32 < N ? __ldg(sB + nc + c * 32 + lane) : 0.f;
             if (!mbar_wait(tfull, tc & 1, &g_int8_err)) break;
             tc_fence_after();
-#pragma unroll 1
+#pragma unroll
             for (int mh = 0; mh < MH; mh++) {
                 const int m0 = (tile % mt) * TM + mh * BM;
                 if (m0 >= M) break;                   // M % 128 == 0: a half lies wholly inside or outside
-                const float sa = __ldg(sA + m0 + r);
+                const float sa = sav[mh];
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + mh * BN + ch * EPI_COLS;
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < EPI_COLS / 32; c++) {
                     const int n = nc + c * 32;
                     if (n >= N) break;                // the last column tile is ragged; N % 32 == 0
@@ -273,9 +283,9 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const float4 s0 = __ldg(reinterpret_cast<const float4*>(sB + n + j * 8));
-                        const float4 s1 = __ldg(reinterpret_cast<const float4*>(sB + n + j * 8) + 1);
-                        const float sb[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                        float sb[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) sb[e] = __shfl_sync(0xffffffffu, sbv[c], j * 8 + e);
                         uint4 o;
                         uint32_t* w = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
