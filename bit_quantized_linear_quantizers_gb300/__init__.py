@@ -491,7 +491,7 @@ def qz_prepare_fp4_scales(scales, K: int, nv: bool = True, out=None, stream=None
 
 def qz_gemm_nvfp4_grouped(problems, ws=None, stream=None):
     """Run independent NVFP4 problems [(qA, sA, gA, qB, sB_prepared, gB, Y), ...] (decode
-    shapes, M <= 128) with one scale re-layout launch and one GEMM launch per 80 problems."""
+    shapes, M <= 128) with one scale re-layout launch and one GEMM launch per 72 problems."""
     arr = (_Nvfp4Problem * len(problems))()
     kmax = 0
     d = _device()

@@ -29,7 +29,13 @@
 //  warp 1      MMA issuer: 4 MMAs (K = 64 each) per stage into one
 //              256-column fp32 accumulator.
 //  warps 2-9   epilogue: drain the accumulator into registers (then release it
-//              so the next tile's MMAs start), apply gA*gB, round to bf16, store.
+//              so the next tile's MMAs start), apply gA*gB, round to bf16, and
+//              write 32-row x 16-column chunks through a 1 KB staging tile
+//              (32-byte swizzle: the row-per-lane writes are conflict-free)
+//              with one TMA store each. Stored straight from registers, a lane
+//              per row made every store instruction touch 32 lines, and those
+//              wavefronts competed with the tensor core's operand reads in
+//              the L1 data stage.
 //
 // The CTAs walk a table of problems (one entry for qz_gemm_nvfp4/mxfp4, a
 // decoder step's linears for the grouped call): tile t belongs to the last
@@ -61,7 +67,10 @@ constexpr int THREADS = 64 + EPI_WARPS * 32 + 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 256;                  // scale-factor ring after the accumulator
 constexpr uint32_t SF_COLS_PER_STAGE = 48;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 256 + 1024;
+constexpr int STG_WARP = 32 * 32;                 // epilogue staging: 32 rows x 16 bf16 (32-byte swizzle)
+constexpr int STG_OFF = STAGES * STAGE_BYTES;     // after the stages (1 KB aligned)
+constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_WARP;
+constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
 static_assert((3 * STAGES + 2) * 8 + 4 <= 256, "barriers and the TMEM slot fit their region");
 
 // Row-major scales sf[R][KS] -> atoms[ceil(R/128)][KS/4][512]: byte
@@ -109,10 +118,15 @@ qz_status relayout(const RelayParams& P, cudaStream_t st) {
     return launch_status();
 }
 
-// One GEMM problem of a launch (kernel parameter space: 80 of them fit).
-struct Fp4Prob {
+// One GEMM problem of a launch: its tensor maps and its other fields, kept in
+// two arrays (a tensor map is 128-byte aligned, so one struct of both would pad
+// each entry to 512 bytes; as two arrays 72 problems fit the kernel parameter space).
+struct Fp4Maps {
     CUtensorMap tmA;                  // A codes [M, K/2] u8, box 128 B x 128 rows
     CUtensorMap tmB;                  // B^T codes [N, K/2] u8, box 128 B x 256 rows
+    CUtensorMap tmY;                  // Y bf16 [M, N], box 16 x 32, 32-byte swizzle (stores)
+};
+struct Fp4Prob {
     const uint8_t* sfA;               // A scales, tensor-core atoms, rows padded to 128
     const uint8_t* sfB;               // B scales, tensor-core atoms
     const float* gA;                  // NVFP4 tensor scales (unused for MXFP4)
@@ -123,13 +137,24 @@ struct Fp4Prob {
     int tile_begin;                   // first tile of this problem in the launch
 };
 
-constexpr int FP4_PER_LAUNCH = 80;
+constexpr int FP4_PER_LAUNCH = 72;
+static_assert(sizeof(Fp4Maps) == 384 && sizeof(Fp4Prob) == 64, "problem table layout");
 
 struct Fp4Params {
+    Fp4Maps m[FP4_PER_LAUNCH];
     Fp4Prob p[FP4_PER_LAUNCH];
     int count;
     int total_tiles;
 };
+
+// TMA tensor store of a 2-D box from shared memory, one bulk group per store.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
+                 "cp.async.bulk.commit_group;"
+                 :: "l"(tmap), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <bool NV>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -139,7 +164,7 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2);
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
@@ -183,7 +208,9 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-                const Fp4Prob& pr = P.p[find(tile)];
+                const int pi = find(tile);
+                const Fp4Prob& pr = P.p[pi];
+                const Fp4Maps& mp = P.m[pi];
                 const int local = tile - pr.tile_begin;
                 const int m0 = (local % pr.mt) * BM, n0 = (local / pr.mt) * BN;
                 const int nks = pr.K / (2 * BKB);
@@ -191,15 +218,15 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
                 const uint8_t* sa = pr.sfA + ((size_t)(m0 / 128) * atoms_per_rb) * ATOM;
                 const uint8_t* sb0 = pr.sfB + ((size_t)(n0 / 128) * atoms_per_rb) * ATOM;
                 const uint8_t* sb1 = sb0 + (size_t)atoms_per_rb * ATOM;
-                prefetch_tmap(&pr.tmA);
-                prefetch_tmap(&pr.tmB);
+                prefetch_tmap(&mp.tmA);
+                prefetch_tmap(&mp.tmB);
                 for (int c = 0; c < nks; c++, it++) {
                     const int s = it % STAGES;
                     if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, &g_fp4_err)) { ok = false; break; }
                     const uint32_t st = sbase + s * STAGE_BYTES;
                     mbar_arrive_expect_tx(full(s), A_BYTES + B_BYTES + sf_bytes);
-                    tma_load_2d(st, &pr.tmA, c * BKB, m0, full(s));     // rows >= M read as zeros
-                    tma_load_2d(st + A_BYTES, &pr.tmB, c * BKB, n0, full(s));
+                    tma_load_2d(st, &mp.tmA, c * BKB, m0, full(s));     // rows >= M read as zeros
+                    tma_load_2d(st + A_BYTES, &mp.tmB, c * BKB, n0, full(s));
                     const size_t off = (size_t)c * G * ATOM;
                     bulk_g2s(st + A_BYTES + B_BYTES, sa + off, G * ATOM, full(s));
                     bulk_g2s(st + A_BYTES + B_BYTES + G * ATOM, sb0 + off, G * ATOM, full(s));
@@ -278,10 +305,13 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
-        const int q = warp & 3, h = (warp - 2) >> 2, r = q * 32 + lane;
+        const int q = warp & 3, h = (warp - 2) >> 2;
+        uint8_t* stg = smem + STG_OFF + (warp - 2) * STG_WARP;
+        const uint32_t stg_s = smem_u32(stg);
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, tcount++) {
-            const Fp4Prob& pr = P.p[find(tile)];
+            const int pi = find(tile);
+            const Fp4Prob& pr = P.p[pi];
             const int local = tile - pr.tile_begin;
             const int m0 = (local % pr.mt) * BM, n0 = (local / pr.mt) * BN;
             const float gscale = NV ? __ldg(pr.gA) * __ldg(pr.gB) : 1.0f;
@@ -292,28 +322,32 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
 #pragma unroll
             for (int c = 0; c < 4; c++) tmem_ld32(taddr + c * 32, v[c]);
             tmem_wait_ld();
-            float acc[128];
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-#pragma unroll
-                for (int i = 0; i < 32; i++) acc[c * 32 + i] = __uint_as_float(v[c][i]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
-            if (m0 + r >= pr.M) continue;                       // padding rows of a partial tile
-            uint4* yrow = reinterpret_cast<uint4*>(pr.Y + (size_t)(m0 + r) * pr.N + n0 + h * 128);
+            if (lane == 0) mbar_arrive(tempty);          // the next tile's MMAs may start
+            // 16-column chunks through the staging tile, each written by one TMA store
+            // (rows past M fall outside the tensor and are not written)
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                uint4 o;
-                uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+            for (int j = 0; j < 8; j++) {
+                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    __nv_bfloat162 p = __floats2bfloat162_rn(acc[j * 8 + 2 * e] * gscale, acc[j * 8 + 2 * e + 1] * gscale);
-                    w[e] = *reinterpret_cast<uint32_t*>(&p);
+                for (int e = 0; e < 8; e++) {
+                    const __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(v[j >> 1][(j & 1) * 16 + 2 * e]) * gscale,
+                                                                   __uint_as_float(v[j >> 1][(j & 1) * 16 + 2 * e + 1]) * gscale);
+                    w[e] = *reinterpret_cast<const uint32_t*>(&p);
                 }
-                yrow[j] = o;
+                if (lane == 0) bulk_wait_read0();        // the previous store has read the staging tile
+                __syncwarp();
+                const int sw = (lane >> 2) & 1;          // 32-byte swizzle: chunk c of row r at c ^ ((r >> 2) & 1)
+                *reinterpret_cast<uint4*>(stg + lane * 32 + ((0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(stg + lane * 32 + ((1 ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tma_store_2d(&P.m[pi].tmY, stg_s, n0 + h * 128 + j * 16, m0 + q * 32);
             }
         }
+        if (lane == 0) bulk_wait_all0();                 // stores complete before the CTA exits
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -328,10 +362,11 @@ size_t round1k(size_t b) { return (b + 1023) & ~size_t(1023); }
 
 // Fills problem slot `p` (tensor maps and tile bookkeeping); false if a
 // tensor map cannot be encoded.
-bool fill_problem(Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA, const float* gA, const uint8_t* qB,
+bool fill_problem(Fp4Maps& mp, Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA, const float* gA, const uint8_t* qB,
                   const uint8_t* sfB, const float* gB, uint16_t* Y, int M, int N, int K, int& tiles) {
-    if (!encode_tmap_2d_u8(&p.tmA, qA, (uint64_t)K / 2, (uint64_t)M, (uint64_t)K / 2, BKB, BM) ||
-        !encode_tmap_2d_u8(&p.tmB, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN))
+    if (!encode_tmap_2d_u8(&mp.tmA, qA, (uint64_t)K / 2, (uint64_t)M, (uint64_t)K / 2, BKB, BM) ||
+        !encode_tmap_2d_u8(&mp.tmB, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN) ||
+        !encode_tmap_2d_swz(&mp.tmY, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 16, 32, 32))
         return false;
     p.sfA = sfA; p.sfB = sfB; p.gA = gA; p.gB = gB; p.Y = Y;
     p.M = M; p.N = N; p.K = K;
@@ -387,7 +422,7 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
     QZ_TRY(relayout(R, st));
     Fp4Params P;
     int tiles = 0;
-    if (!fill_problem(P.p[0], qA, wsA, gA, qB, wsB, gB, Y, M, N, K, tiles)) return QZ_ERR_CUDA;
+    if (!fill_problem(P.m[0], P.p[0], qA, wsA, gA, qB, wsB, gB, Y, M, N, K, tiles)) return QZ_ERR_CUDA;
     P.count = 1;
     P.total_tiles = tiles;
     return launch_table(nv, P, st);
@@ -418,7 +453,7 @@ qz_status gemm_nvfp4_grouped_launch(const qz_nvfp4_problem* problems, int count,
         P.count = std::min(share, count - i0);
         for (int i = 0; i < P.count; i++) {
             const qz_nvfp4_problem& q = problems[i0 + i];
-            if (!fill_problem(P.p[i], q.qA, wsb + (size_t)(i0 + i) * slot, q.gA, q.qB, q.sB_prepared, q.gB, q.Y,
+            if (!fill_problem(P.m[i], P.p[i], q.qA, wsb + (size_t)(i0 + i) * slot, q.gA, q.qB, q.sB_prepared, q.gB, q.Y,
                               q.M, q.N, q.K, tiles))
                 return QZ_ERR_CUDA;
         }

@@ -330,9 +330,9 @@ qz_status int8_error_read_and_clear() {
 qz_status gemm_int8_launch(const int8_t* qA, const float* sA, const int8_t* qB, const float* sB, uint16_t* Y, int M,
                            int N, int K, cudaStream_t st) {
     CUtensorMap ta, tb, ty;
-    if (!encode_tmap_2d_sw64(&ta, qA, 1, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, TM)) return QZ_ERR_CUDA;
+    if (!encode_tmap_2d_swz(&ta, qA, 1, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, TM, 64)) return QZ_ERR_CUDA;
     if (!encode_tmap_2d(&tb, qB, 1, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN, false)) return QZ_ERR_CUDA;
-    if (!encode_tmap_2d_sw64(&ty, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 32, 32)) return QZ_ERR_CUDA;
+    if (!encode_tmap_2d_swz(&ty, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 32, 32, 64)) return QZ_ERR_CUDA;
     QZ_TRY(opt_in_smem((const void*)int8_gemm_kernel, SMEM_BYTES));
     const int tiles = ((M + TM - 1) / TM) * ((N + BN - 1) / BN);
     int8_gemm_kernel<<<std::min(tiles, num_sms()), THREADS, SMEM_BYTES, st>>>(ta, tb, ty, sA, sB, M, N, K);

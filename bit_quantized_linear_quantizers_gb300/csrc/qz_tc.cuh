@@ -190,7 +190,7 @@ bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint6
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
-bool encode_tmap_2d_sw64(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
-                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+bool encode_tmap_2d_swz(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 
 } // namespace qz

@@ -58,12 +58,18 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-// As encode_tmap_2d, with the 64-byte swizzle: within each 512-byte block of
-// eight 64-byte rows, 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
-bool encode_tmap_2d_sw64(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
-                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+// As encode_tmap_2d, with the 32-, 64- or 128-byte swizzle (swizzle_bytes):
+// 16-byte chunk c of a row sits at chunk c ^ ((address >> 7) & (swizzle_bytes / 16 - 1))
+// within its block, i.e. for 32-byte rows c ^ ((r >> 2) & 1), for 64-byte rows
+// c ^ ((r >> 1) & 3), for 128-byte rows c ^ (r & 7).
+bool encode_tmap_2d_swz(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
     std::call_once(g_once, load_encode);
     if (!g_encode) return false;
+    const CUtensorMapSwizzle sw = swizzle_bytes == 32    ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : swizzle_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
     const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT32;
@@ -72,8 +78,8 @@ bool encode_tmap_2d_sw64(CUtensorMap* map, const void* base, int elem_bytes, uin
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

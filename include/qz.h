@@ -303,7 +303,7 @@ typedef struct qz_nvfp4_problem {
 /* Runs `count` independent NVFP4 GEMMs of decode shape (the linears of a
  * decoder step, "量化部署实战", 精度比较: every linear of the block quantized)
  * with one scale re-layout launch for all A operands and one GEMM launch per
- * 80 problems, the problems' 128 x 256 output tiles shared out over the SMs.
+ * 72 problems, the problems' 128 x 256 output tiles shared out over the SMs.
  * Same arithmetic as qz_gemm_nvfp4. Shapes per problem: 1 <= M <= 128,
  * N % 256 == 0, K % 256 == 0. count <= 256. Alignment: codes, prepared scales
  * and Y 16 B, sA 4 B. ws: qz_workspace_size(QZ_OP_GEMM_NVFP4_GROUPED, count,

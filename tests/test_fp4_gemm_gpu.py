@@ -198,7 +198,7 @@ def test_nvfp4_grouped_matches_single_call(qz):
 
 
 def test_nvfp4_grouped_more_than_one_launch(qz):
-    """85 problems: two GEMM launches (80 problems fit one launch's parameters)."""
+    """85 problems: two GEMM launches (72 problems fit one launch's parameters)."""
     shapes = [(8 + (i % 3), 256, 256) for i in range(85)]
     ops = grouped_case(qz, shapes, 31)
     for i in (0, 41, 79, 80, 84):
