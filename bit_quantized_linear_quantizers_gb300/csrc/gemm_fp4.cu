@@ -147,15 +147,6 @@ struct Fp4Params {
     int total_tiles;
 };
 
-// TMA tensor store of a 2-D box from shared memory, one bulk group per store.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
-                 "cp.async.bulk.commit_group;"
-                 :: "l"(tmap), "r"(src), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 template <bool NV>
 __global__ void __launch_bounds__(THREADS, 1)
 fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {

@@ -27,6 +27,7 @@
 #include "qz_tc.cuh"
 
 #include <algorithm>
+#include <cstring>
 
 namespace qz {
 
@@ -45,10 +46,11 @@ constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = idesc_dense(0u, 0u, BM, BN);   // E4M3 x E4M3 -> fp32
 // Each epilogue warp stages 32 rows x 128 bytes of its bf16 output in its own
-// slice of shared memory (16-byte chunks swizzled by row), then writes them back
-// row-wise: eight lanes cover one row's 128 contiguous bytes, so a store
-// instruction writes four whole 128-byte row segments instead of 32 scattered
-// 16-byte pieces (110.3 -> 107.7 us at 2048 x 14336 x 4096).
+// slice of shared memory (16-byte chunk j of row r at chunk j ^ (r & 7): the
+// TMA 128-byte swizzle) and one TMA store writes the block. Stored a row per
+// lane, each store instruction touched 32 lines (110.3 us at 2048 x 14336 x
+// 4096); read back row-wise and stored by the warp, 107.7 us, but those loads
+// and stores crowd the L1 data stage, which the MMA's operand reads keep busy.
 constexpr int STG_OFF = STAGES * STAGE_BYTES + 1024;
 constexpr int STG_WARP = 32 * 128;
 constexpr int SMEM_BYTES = STG_OFF + EPI_WARPS * STG_WARP + 1024;
@@ -60,20 +62,9 @@ __device__ __forceinline__ void fma2(uint64_t& acc, uint32_t v0, uint32_t v1, ui
     asm("{ .reg .b64 t; mov.b64 t, {%1, %2}; fma.rn.f32x2 %0, t, %3, %0; }" : "+l"(acc) : "r"(v0), "r"(v1), "l"(s2));
 }
 
-// Row-wise write-back of a warp's staged 32 x 128-byte block: row i goes to
-// dst + i * pitch (bytes), 16-byte aligned.
+// 16-byte chunk j of the lane's row in a warp's staged 32 x 128-byte block.
 __device__ __forceinline__ void stage_put(uint8_t* stg, int lane, int j, uint4 v) {
     *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
-}
-__device__ __forceinline__ void stage_flush(const uint8_t* stg, int lane, uint8_t* dst, size_t pitch) {
-    __syncwarp();
-#pragma unroll
-    for (int it = 0; it < 8; it++) {
-        const int rr = it * 4 + (lane >> 3), c = lane & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
-        *reinterpret_cast<uint4*>(dst + (size_t)rr * pitch + c * 16) = v;
-    }
-    __syncwarp();
 }
 
 // QOUT: the epilogue also quantizes its output for the next layer, FP8 E4M3
@@ -84,7 +75,7 @@ __device__ __forceinline__ void stage_flush(const uint8_t* stg, int lane, uint8_
 template <bool QOUT>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const float* __restrict__ sA, const float* __restrict__ sB, uint16_t* __restrict__ Y,
+                      const __grid_constant__ CUtensorMap tmY, const float* __restrict__ sA, const float* __restrict__ sB, uint16_t* __restrict__ Y,
                       uint8_t* __restrict__ Yq, float* __restrict__ Yqs, int M, int N, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -278,6 +269,8 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 uint8_t* stg = smem_raw + (STG_OFF + (warp - 2) * STG_WARP + (smem - smem_raw));
                 #pragma unroll
                 for (int hf = 0; hf < EPI_COLS / 64; hf++) {          // 64 bf16 columns = 128 bytes a row
+                    if (lane == 0) bulk_wait_read0();                 // the previous store has read the block
+                    __syncwarp();
                     #pragma unroll
                     for (int j = 0; j < 8; j++) {
                         uint4 o;
@@ -290,8 +283,9 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         }
                         stage_put(stg, lane, j, o);
                     }
-                    stage_flush(stg, lane, reinterpret_cast<uint8_t*>(Y + (size_t)(m0 + q * 32) * N + n0 + h * EPI_COLS + hf * 64),
-                                (size_t)N * 2);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tma_store_2d(&tmY, smem_u32(stg), n0 + h * EPI_COLS + hf * 64, m0 + q * 32);
                 }
             } else {
                 uint4* yrow = reinterpret_cast<uint4*>(Y + (size_t)(m0 + r) * N + n0 + h * EPI_COLS);
@@ -308,6 +302,8 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
             }
         }
+        if (!QOUT && lane == 0) bulk_wait_all0();            // stores complete before the CTA exits
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -335,17 +331,20 @@ qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_
 
 qz_status gemm_fp8_block_quant_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
                                       uint16_t* Y, uint8_t* Yq, float* Yqs, int M, int N, int K, cudaStream_t st) {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     if (!encode_tmap_2d_u8(&ta, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM)) return QZ_ERR_CUDA;
     if (!encode_tmap_2d_u8(&tb, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN)) return QZ_ERR_CUDA;
+    memset(&ty, 0, sizeof(ty));                   // the output-quantizing instance stores without TMA
+    if (!Yq && !encode_tmap_2d_swz(&ty, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32, 128))
+        return QZ_ERR_CUDA;
     const int tiles = (M / BM) * (N / BN);
     const int grid = std::min(tiles, num_sms());
     if (Yq) {
         QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<true>, SMEM_BYTES_Q));
-        fp8_block_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES_Q, st>>>(ta, tb, sA, sB, Y, Yq, Yqs, M, N, K);
+        fp8_block_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES_Q, st>>>(ta, tb, ty, sA, sB, Y, Yq, Yqs, M, N, K);
     } else {
         QZ_TRY(opt_in_smem((const void*)fp8_block_gemm_kernel<false>, SMEM_BYTES));
-        fp8_block_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sA, sB, Y, nullptr, nullptr, M, N, K);
+        fp8_block_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, ty, sA, sB, Y, nullptr, nullptr, M, N, K);
     }
     return launch_status();
 }

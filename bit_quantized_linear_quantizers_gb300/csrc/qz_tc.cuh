@@ -152,6 +152,18 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------------- TMA
 
+// 2-D tiled TMA store of a box from shared memory (x = inner coordinate, y =
+// outer; elements outside the tensor are not written), committed as its own
+// bulk group. Before the source is rewritten: bulk_wait_read0; before exit:
+// bulk_wait_all0.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
+                 "cp.async.bulk.commit_group;"
+                 :: "l"(tmap), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 2-D tiled TMA load of box (x = inner coordinate, y = outer) into shared memory.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
