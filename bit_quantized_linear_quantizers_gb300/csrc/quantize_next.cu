@@ -82,6 +82,7 @@ template <typename T>
 __global__ void __launch_bounds__(kT)
 int4_zp_kernel(const T* __restrict__ w, int64_t K, int64_t N, int64_t ldw, int32_t* __restrict__ qweight,
                uint16_t* __restrict__ scale, uint8_t* __restrict__ zero, float* __restrict__ deq) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     __shared__ float tile[128][65];
     __shared__ float plo[4][64], phi[4][64];
     __shared__ float sc[64], zf[64];
@@ -137,6 +138,7 @@ int4_zp_kernel(const T* __restrict__ w, int64_t K, int64_t N, int64_t ldw, int32
         }
         qweight[(g * 16 + o) * N + n0 + c] = (int32_t)word;
     }
+    pdl_trigger();                                // the next call may launch as this one drains
 }
 
 // ------------------------------------------------------ FP8 KV per head
@@ -146,6 +148,7 @@ int4_zp_kernel(const T* __restrict__ w, int64_t K, int64_t N, int64_t ldw, int32
 __global__ void __launch_bounds__(kT)
 kv_head_amax_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t BH, int64_t L,
                     int chunks, float* __restrict__ partial) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     __shared__ float red[kW];
     const int64_t y = blockIdx.y;
     const uint16_t* x = (y < BH ? k + y * L : v + (y - BH) * L);
@@ -201,6 +204,7 @@ kv_head_encode_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict
         Load8<uint16_t>::run(x + i * 8, val);
         reinterpret_cast<uint2*>(codes)[i] = e4m3x8(val, d);
     }
+    pdl_trigger();                                // the next call may launch as this one drains
 }
 
 // ------------------------------------ K per channel with a zero point
@@ -361,6 +365,7 @@ kzp_stats_v_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ 
 template <typename T>
 __global__ void __launch_bounds__(kT)
 col_amax_partial_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int chunks, float* __restrict__ partial) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     const int64_t c8 = (int64_t)blockIdx.y * kT + threadIdx.x;          // column octet
     if (c8 * 8 >= cols) return;
     const int64_t r0 = rows * blockIdx.x / chunks, r1 = rows * (blockIdx.x + 1) / chunks;
@@ -390,6 +395,7 @@ col_amax_final_kernel(const float* __restrict__ partial, int64_t cols, int chunk
 // s = fl(sqrt(max(ax, 1e-12))) / fl(sqrt(max(aw, 1e-12))), all IEEE-rounded.
 __global__ void __launch_bounds__(kT)
 smooth_factors_kernel(const float* __restrict__ xm, const float* __restrict__ wm, int64_t n, float* __restrict__ s) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     const int64_t j = (int64_t)blockIdx.x * kT + threadIdx.x;
     if (j >= n) return;
     const float ax = fmaxf(__ldg(xm + j), kAmaxMin), aw = fmaxf(__ldg(wm + j), kAmaxMin);
@@ -432,6 +438,7 @@ template <typename T, int OP, int CPT>                // CPT: 8-element chunks p
 __global__ void __launch_bounds__(kT)
 int8_row_cta_kernel(const T* __restrict__ x, int64_t cols, const float* __restrict__ f,
                     int8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     __shared__ float red[kW];
     const int64_t r = blockIdx.x;
     const T* xr = x + r * cols;
@@ -459,6 +466,7 @@ int8_row_cta_kernel(const T* __restrict__ x, int64_t cols, const float* __restri
         const int64_t c = ((int64_t)u * kT + threadIdx.x) * 8;
         if (c < cols) int8_encode8(v[u], d, s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
     }
+    pdl_trigger();                                // the next call may launch as this one drains
 }
 
 // Wider rows: one warp per row, two passes (the second re-reads the row).
@@ -466,6 +474,7 @@ template <typename T, int OP>
 __global__ void __launch_bounds__(kT)
 int8_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ f,
                  int8_t* __restrict__ codes, float* __restrict__ scales, float* __restrict__ deq) {
+    pdl_wait();                                   // the previous kernel on the stream has finished
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kT + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t)gridDim.x * kW;
@@ -489,6 +498,7 @@ int8_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, const floa
             int8_encode8(v, d, s, codes + r * cols + c, deq ? deq + r * cols + c : nullptr);
         }
     }
+    pdl_trigger();                                // the next call may launch as this one drains
 }
 
 int kv_head_chunks(int64_t BH, int64_t L) {
@@ -518,10 +528,11 @@ qz_status int4_zp_launch(const void* w, qz_dtype wt, int64_t K, int64_t N, int64
                          uint16_t* scale, uint8_t* zero, float* deq, cudaStream_t st) {
     const int64_t nblocks = (K / 128) * (N / 64);
     if (wt == QZ_F32)
-        int4_zp_kernel<float><<<(unsigned)nblocks, kT, 0, st>>>((const float*)w, K, N, ldw, qweight, scale, zero, deq);
+        QZ_TRY(launch_pdl(int4_zp_kernel<float>, dim3((unsigned)nblocks), dim3(kT), st, (const float*)w, K, N, ldw,
+                          qweight, scale, zero, deq));
     else
-        int4_zp_kernel<uint16_t><<<(unsigned)nblocks, kT, 0, st>>>((const uint16_t*)w, K, N, ldw, qweight, scale, zero,
-                                                                   deq);
+        QZ_TRY(launch_pdl(int4_zp_kernel<uint16_t>, dim3((unsigned)nblocks), dim3(kT), st, (const uint16_t*)w, K, N, ldw,
+                          qweight, scale, zero, deq));
     return launch_status();
 }
 
@@ -530,12 +541,12 @@ qz_status kv_per_head_launch(const uint16_t* k, const uint16_t* v, int64_t BH, i
     const int chunks = kv_head_chunks(BH, L);
     const dim3 grid(chunks, (unsigned)(2 * BH));
     if (mode == QZ_SCALE_GIVEN) {
-        kv_head_encode_kernel<true><<<grid, kT, 0, st>>>(k, v, BH, L, chunks, nullptr, ks, vs, kc, vc);
+        QZ_TRY(launch_pdl(kv_head_encode_kernel<true>, grid, dim3(kT), st, k, v, BH, L, chunks, (const float*)nullptr,
+                          ks, vs, kc, vc));
         return launch_status();
     }
     float* partial = (float*)ws;
-    kv_head_amax_kernel<<<grid, kT, 0, st>>>(k, v, BH, L, chunks, partial);
-    QZ_TRY(launch_status());
+    QZ_TRY(launch_pdl(kv_head_amax_kernel, grid, dim3(kT), st, k, v, BH, L, chunks, partial));
     QZ_TRY(launch_pdl(kv_head_encode_kernel<false>, grid, dim3(kT), st, k, v, BH, L, chunks, (const float*)partial,
                       ks, vs, kc, vc));
     return launch_status();
@@ -573,17 +584,17 @@ qz_status col_amax_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols
     const dim3 grid(chunks, (unsigned)((cols / 8 + kT - 1) / kT));
     float* partial = (float*)ws;
     if (xt == QZ_F32)
-        col_amax_partial_kernel<float><<<grid, kT, 0, st>>>((const float*)x, rows, cols, chunks, partial);
+        QZ_TRY(launch_pdl(col_amax_partial_kernel<float>, grid, dim3(kT), st, (const float*)x, rows, cols, chunks, partial));
     else
-        col_amax_partial_kernel<uint16_t><<<grid, kT, 0, st>>>((const uint16_t*)x, rows, cols, chunks, partial);
-    QZ_TRY(launch_status());
+        QZ_TRY(launch_pdl(col_amax_partial_kernel<uint16_t>, grid, dim3(kT), st, (const uint16_t*)x, rows, cols, chunks,
+                          partial));
     QZ_TRY(launch_pdl(col_amax_final_kernel, dim3((unsigned)((cols + kT - 1) / kT)), dim3(kT), st,
                       (const float*)partial, cols, chunks, out));
     return launch_status();
 }
 
 qz_status smooth_factors_launch(const float* xm, const float* wm, int64_t n, float* s, cudaStream_t st) {
-    smooth_factors_kernel<<<(unsigned)((n + kT - 1) / kT), kT, 0, st>>>(xm, wm, n, s);
+    QZ_TRY(launch_pdl(smooth_factors_kernel, dim3((unsigned)((n + kT - 1) / kT)), dim3(kT), st, xm, wm, n, s));
     return launch_status();
 }
 
@@ -592,13 +603,13 @@ qz_status launch_i8(const void* x, int64_t rows, int64_t cols, const float* f, i
                     float* deq, cudaStream_t st) {
     const int64_t cpt = (cols / 8 + kT - 1) / kT;               // chunks per thread, one CTA per row
     switch (cpt) {
-    case 1: int8_row_cta_kernel<T, OP, 1><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
-    case 2: int8_row_cta_kernel<T, OP, 2><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
-    case 3: int8_row_cta_kernel<T, OP, 3><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
-    case 4: int8_row_cta_kernel<T, OP, 4><<<(unsigned)rows, kT, 0, st>>>((const T*)x, cols, f, codes, scales, deq); break;
+    case 1: QZ_TRY(launch_pdl(int8_row_cta_kernel<T, OP, 1>, dim3((unsigned)rows), dim3(kT), st, (const T*)x, cols, f, codes, scales, deq)); break;
+    case 2: QZ_TRY(launch_pdl(int8_row_cta_kernel<T, OP, 2>, dim3((unsigned)rows), dim3(kT), st, (const T*)x, cols, f, codes, scales, deq)); break;
+    case 3: QZ_TRY(launch_pdl(int8_row_cta_kernel<T, OP, 3>, dim3((unsigned)rows), dim3(kT), st, (const T*)x, cols, f, codes, scales, deq)); break;
+    case 4: QZ_TRY(launch_pdl(int8_row_cta_kernel<T, OP, 4>, dim3((unsigned)rows), dim3(kT), st, (const T*)x, cols, f, codes, scales, deq)); break;
     default: {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kW - 1) / kW, (int64_t)num_sms() * 8));
-        int8_rows_kernel<T, OP><<<grid, kT, 0, st>>>((const T*)x, rows, cols, f, codes, scales, deq);
+        QZ_TRY(launch_pdl(int8_rows_kernel<T, OP>, dim3(grid), dim3(kT), st, (const T*)x, rows, cols, f, codes, scales, deq));
     }
     }
     return launch_status();
