@@ -429,7 +429,7 @@ qz_status qz_gemm_fp8_block_quant(const uint8_t* qA, const float* sA, const uint
                                   uint16_t* Y, uint8_t* y_codes, float* y_scales, int M, int N, int K,
                                   void* stream);
 
-/* NVFP4 GEMM that allocates nothing and takes no workspace. (The surveyed
+/* NVFP4 GEMM that allocates nothing and takes no workspace. (The quantization
  * pages have no counterpart: this is an interface convenience of this library.)
  * Some callers cannot call cudaMalloc or hand this library a workspace: runtimes
  * whose device memory is planned once at start-up and parcelled out by their own

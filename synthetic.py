@@ -3,7 +3,7 @@
 This module only draws numbers. It holds none of the quantization or GEMM
 arithmetic: the kernels and the oracle each receive these arrays as inputs.
 
-Shapes and distributions follow the workloads of the surveyed pages:
+Shapes and distributions follow the workloads of the quantization pages:
 
 * the fake-quant weight study of "量化部署实战" (anrans.github.io, section
   精度比较): linear weights ~ N(0, 0.02) with a few outlier channels;
