@@ -718,7 +718,8 @@ int choose_mt(int m) { return m <= 8 ? 8 : m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 // Register-direct launch for up to 8 tokens: one CTA per 32 columns of every
 // problem, programmatic dependent launch.
 template <int MT, bool ZP, int NP>
-qz_status launch_rd_n(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros) {
+qz_status launch_rd_n(const qz_w4a16_problem* problems, int count, cudaStream_t st, bool early,
+                      const uint8_t* const* zeros) {
     RdParamsN<NP> P;                              // the kernel parameter block (copied at launch)
     int total = 0;
     P.count = count;
@@ -743,21 +744,22 @@ qz_status launch_rd_n(const qz_w4a16_problem* problems, int count, cudaStream_t 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 1 : 0;                 // without it: after all earlier work on the stream
     if (cudaLaunchKernelEx(&cfg, w4a16_rd_kernel<MT, ZP, NP>, P) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
 template <int MT, bool ZP = false>
-qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st, const uint8_t* const* zeros = nullptr) {
-    return count == 1 ? launch_rd_n<MT, ZP, 1>(problems, count, st, zeros)
-                      : launch_rd_n<MT, ZP, RD_MAX_PROBLEMS>(problems, count, st, zeros);
+qz_status launch_rd(const qz_w4a16_problem* problems, int count, cudaStream_t st, bool early,
+                    const uint8_t* const* zeros = nullptr) {
+    return count == 1 ? launch_rd_n<MT, ZP, 1>(problems, count, st, early, zeros)
+                      : launch_rd_n<MT, ZP, RD_MAX_PROBLEMS>(problems, count, st, early, zeros);
 }
 
 // Bulk-staged launch for up to 8 tokens and K <= SA_KMAX: one CTA per 32
 // columns of every problem, programmatic dependent launch.
 template <int NP>
-qz_status launch_bulk_n(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
+qz_status launch_bulk_n(const qz_w4a16_problem* problems, int count, cudaStream_t st, bool early) {
     SaParamsN<NP> P;                              // the kernel parameter block (copied at launch)
     int total = 0, kmax = 0, mmax = 0;
     P.count = count;
@@ -802,19 +804,20 @@ qz_status launch_bulk_n(const qz_w4a16_problem* problems, int count, cudaStream_
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 1 : 0;                 // without it: after all earlier work on the stream
     const cudaError_t e = mmax == 1 ? cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<true, NP>, P)
                                     : cudaLaunchKernelEx(&cfg, w4a16_bulk_kernel<false, NP>, P);
     if (e != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
-qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t st) {
-    return count == 1 ? launch_bulk_n<1>(problems, count, st) : launch_bulk_n<SA_MAX_PROBLEMS>(problems, count, st);
+qz_status launch_bulk(const qz_w4a16_problem* problems, int count, cudaStream_t st, bool early) {
+    return count == 1 ? launch_bulk_n<1>(problems, count, st, early)
+                      : launch_bulk_n<SA_MAX_PROBLEMS>(problems, count, st, early);
 }
 
 template <int MT, int NP>
-qz_status launch_mt(const ParamsN<NP>& P, int nt, cudaStream_t st) {
+qz_status launch_mt(const ParamsN<NP>& P, int nt, cudaStream_t st, bool early) {
     // One persistent CTA per SM (or per tile, if fewer), ring as deep as fits.
     const Layout L(nt, MT);
     const uint32_t budget = 200u * 1024u;
@@ -846,13 +849,14 @@ qz_status launch_mt(const ParamsN<NP>& P, int nt, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 1 : 0;                 // without it: after all earlier work on the stream
     if (cudaLaunchKernelEx(&cfg, w4a16_kernel<MT, NP>, P, nt, ns) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
 
 template <int NP>
-qz_status launch_chunk_n(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
+qz_status launch_chunk_n(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st,
+                         bool early) {
     ParamsN<NP> P;                                // the kernel parameter block (copied at launch)
     int total = 0;
     P.count = count;
@@ -870,12 +874,12 @@ qz_status launch_chunk_n(const qz_w4a16_problem* problems, int count, int nt, in
         total += (q.N + nt - 1) / nt;
     }
     P.total_tiles = total;
-    return launch_mt<16, NP>(P, nt, st);         // 9..16 tokens (the only width this kernel serves)
+    return launch_mt<16, NP>(P, nt, st, early);         // 9..16 tokens (the only width this kernel serves)
 }
 
-qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st) {
-    return count == 1 ? launch_chunk_n<1>(problems, count, nt, mt, st)
-                      : launch_chunk_n<PER_LAUNCH>(problems, count, nt, mt, st);
+qz_status launch_chunk(const qz_w4a16_problem* problems, int count, int nt, int mt, cudaStream_t st, bool early) {
+    return count == 1 ? launch_chunk_n<1>(problems, count, nt, mt, st, early)
+                      : launch_chunk_n<PER_LAUNCH>(problems, count, nt, mt, st, early);
 }
 
 } // namespace
@@ -885,10 +889,10 @@ size_t ws_gemm_w4a16(int, int, int) { return 0; }
 // W4A16 with unsigned codes and a zero point per group and column, up to 16
 // tokens: the register-direct kernel.
 qz_status gemm_w4a16_zp_launch(const uint16_t* A, const int32_t* qweight, const uint16_t* scale, const uint8_t* zero,
-                               uint16_t* Y, int M, int N, int K, cudaStream_t st) {
+                               uint16_t* Y, int M, int N, int K, cudaStream_t st, bool early) {
     const qz_w4a16_problem p = {A, qweight, scale, Y, M, N, K};
     const uint8_t* z[1] = {zero};
-    return M <= 8 ? launch_rd<8, true>(&p, 1, st, z) : launch_rd<16, true>(&p, 1, st, z);
+    return M <= 8 ? launch_rd<8, true>(&p, 1, st, early, z) : launch_rd<16, true>(&p, 1, st, early, z);
 }
 
 qz_status w4a16_error_read_and_clear() {
@@ -898,7 +902,8 @@ qz_status w4a16_error_read_and_clear() {
     return v ? QZ_ERR_TIMEOUT : QZ_OK;
 }
 
-qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, size_t, cudaStream_t st) {
+qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, size_t, cudaStream_t st,
+                            bool early) {
     const int sms = num_sms();
     int mmax = 0;
     for (int i = 0; i < count; i++) mmax = std::max(mmax, problems[i].M);
@@ -914,7 +919,7 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     if (mt == 8 && kmax <= SA_KMAX) {             // up to 8 tokens: bulk-staged kernel
         const int sh = share(SA_MAX_PROBLEMS);
         for (int i = 0; i < count; i += sh) {
-            const qz_status s = launch_bulk(problems + i, std::min(sh, count - i), st);
+            const qz_status s = launch_bulk(problems + i, std::min(sh, count - i), st, early);
             if (s != QZ_OK) return s;
         }
         return QZ_OK;
@@ -922,12 +927,12 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     if (mt == 8) {                                // deeper K: register-direct kernel
         const int sh = share(RD_MAX_PROBLEMS);
         for (int i = 0; i < count; i += sh) {
-            const qz_status s = launch_rd<8>(problems + i, std::min(sh, count - i), st);
+            const qz_status s = launch_rd<8>(problems + i, std::min(sh, count - i), st, early);
             if (s != QZ_OK) return s;
         }
         return QZ_OK;
     }
-    if (mt >= 32) return w4a16_tc_launch(problems, count, mt, st);   // 17..64 tokens: tcgen05
+    if (mt >= 32) return w4a16_tc_launch(problems, count, mt, st, early);   // 17..64 tokens: tcgen05
     int nt = ntmax_for(mt);
     if (count == 1) {
         const int N = problems[0].N;
@@ -935,7 +940,7 @@ qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void*, 
     }
     const int sh = share(PER_LAUNCH);
     for (int i = 0; i < count; i += sh) {
-        const qz_status s = launch_chunk(problems + i, std::min(sh, count - i), nt, mt, st);
+        const qz_status s = launch_chunk(problems + i, std::min(sh, count - i), nt, mt, st, early);
         if (s != QZ_OK) return s;
     }
     return QZ_OK;

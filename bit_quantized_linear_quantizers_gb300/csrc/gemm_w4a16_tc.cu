@@ -344,7 +344,7 @@ w4a16_tc_kernel(const __grid_constant__ TcParams P) {
 }
 
 template <int MT>
-qz_status launch_tc(const TcParams& P, cudaStream_t st) {
+qz_status launch_tc(const TcParams& P, cudaStream_t st, bool early) {
     using L = TcLayout<MT>;
     QZ_TRY(opt_in_smem((const void*)w4a16_tc_kernel<MT>, L::SMEM));
     cudaLaunchConfig_t cfg = {};
@@ -356,7 +356,7 @@ qz_status launch_tc(const TcParams& P, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 1 : 0;                 // without it: after all earlier work on the stream
     if (cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<MT>, P) != cudaSuccess) return QZ_ERR_CUDA;
     return launch_status();
 }
@@ -371,7 +371,7 @@ qz_status w4a16_tc_error_read_and_clear() {
 }
 
 // Problems with 17..64 tokens (mt = 32 or 64 padded rows), up to 80 per launch.
-qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st) {
+qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st, bool early) {
     // as few launches as the parameter space allows, with equal shares of problems
     const int launches = (count + TC_PER_LAUNCH - 1) / TC_PER_LAUNCH;
     const int share = (count + launches - 1) / launches;
@@ -399,7 +399,7 @@ qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, c
             tiles += (q.N + TN - 1) / TN;
         }
         P.total_tiles = tiles;
-        const qz_status s = mt == 32 ? launch_tc<32>(P, st) : launch_tc<64>(P, st);
+        const qz_status s = mt == 32 ? launch_tc<32>(P, st, early) : launch_tc<64>(P, st, early);
         if (s != QZ_OK) return s;
     }
     return QZ_OK;

@@ -517,6 +517,7 @@ nvfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
              float* __restrict__ deq) {
     __shared__ float red[kWarps];
     __shared__ float tab_s[128], tab_r[128];
+    if (!partial) pdl_wait();                     // a given amax and x may be the previous kernel's output
     const float amax_t = partial ? reduce_partials(partial, nparts, red) : __ldg(amax_in);
     const float g = div_rn(fmaxf(amax_t, kAmaxMin), kFp8Max * kFp4Max);
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;

@@ -5,7 +5,9 @@
 #include "qz_gemm.cuh"
 #include "qz_next.cuh"
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 namespace qz {
 
@@ -116,6 +118,50 @@ qz_status opt_in_smem(const void* fn, int bytes) {
     }
     e->bytes = bytes;
     return QZ_OK;
+}
+
+namespace {
+struct StreamInt4 {
+    int dev;
+    cudaStream_t st;
+    Int4Writes w;
+};
+std::mutex g_int4_mu;
+std::vector<StreamInt4> g_int4;         // one entry per device and stream an INT4 quantizer ran on
+uint64_t g_int4_gen;
+
+StreamInt4* find_int4(int dev, cudaStream_t st) {
+    for (StreamInt4& e : g_int4)
+        if (e.dev == dev && e.st == st) return &e;
+    return nullptr;
+}
+} // namespace
+
+void note_int4_writes(cudaStream_t st, const Span* w, int n) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_int4_mu);
+    StreamInt4* e = find_int4(dev, st);
+    if (!e) {
+        g_int4.push_back(StreamInt4{dev, st, {}});
+        e = &g_int4.back();
+    }
+    e->w.gen = ++g_int4_gen;
+    e->w.n = std::min(n, 3);
+    for (int i = 0; i < e->w.n; i++) e->w.s[i] = w[i];
+}
+
+Int4Writes int4_writes(cudaStream_t st) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_int4_mu);
+    const StreamInt4* e = find_int4(dev, st);
+    return e ? e->w : Int4Writes{0, 0, {}};
+}
+
+void clear_int4_writes(cudaStream_t st, uint64_t gen) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_int4_mu);
+    StreamInt4* e = find_int4(dev, st);
+    if (e && e->w.gen == gen) e->w.n = 0;
 }
 
 } // namespace qz
@@ -244,7 +290,10 @@ qz_status qz_quantize_int4_g128(const void* w, qz_dtype wt, int64_t K, int64_t N
     if (!is_aligned(qweight, 16) || !is_aligned(scale_bf16, 16) || (dequant && !is_aligned(dequant, 16)))
         return QZ_ERR_ALIGNMENT;
     QZ_TRY(device_check());
-    return quantize_int4_launch(w, wt, K, N, ldw, qweight, scale_bf16, dequant, (cudaStream_t)stream);
+    QZ_TRY(quantize_int4_launch(w, wt, K, N, ldw, qweight, scale_bf16, dequant, (cudaStream_t)stream));
+    const Span out[2] = {{qweight, (size_t)K * N / 2}, {scale_bf16, (size_t)K * N / 64}};
+    note_int4_writes((cudaStream_t)stream, out, 2);
+    return QZ_OK;
 }
 
 qz_status qz_kv_write_fp8(const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
@@ -293,7 +342,17 @@ qz_status qz_gemm_w4a16_grouped(const qz_w4a16_problem* problems, int count, voi
     const size_t need = ws_gemm_w4a16(mmax, (int)nsum, kmax);
     if (need && (!ws || ws_bytes < need || !is_aligned(ws, 16))) return QZ_ERR_WORKSPACE;
     QZ_TRY(device_check());
-    return gemm_w4a16_launch(problems, count, ws, ws_bytes, (cudaStream_t)stream);
+    // Weights an INT4 quantizer call may still be writing: launch after all
+    // earlier work on the stream instead of under dependent launch.
+    const Int4Writes rec = int4_writes((cudaStream_t)stream);
+    bool early = true;
+    for (int i = 0; i < count && rec.n && early; i++) {
+        const qz_w4a16_problem& p = problems[i];
+        early = !w4a16_reads_in_flight(rec, p.qweight, p.scale_bf16, nullptr, p.N, p.K);
+    }
+    QZ_TRY(gemm_w4a16_launch(problems, count, ws, ws_bytes, (cudaStream_t)stream, early));
+    if (!early) clear_int4_writes((cudaStream_t)stream, rec.gen);
+    return QZ_OK;
 }
 
 qz_status qz_gemm_fp8_block(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,

@@ -60,7 +60,10 @@ qz_status qz_quantize_int4_g128_zp(const void* w, qz_dtype wt, int64_t K, int64_
         !is_aligned(scale_bf16, 16) || !is_aligned(zero, 16) || (dequant && !is_aligned(dequant, 16)))
         return QZ_ERR_ALIGNMENT;
     QZ_TRY(device_check());
-    return int4_zp_launch(w, wt, K, N, ldw, qweight, scale_bf16, zero, dequant, (cudaStream_t)stream);
+    QZ_TRY(int4_zp_launch(w, wt, K, N, ldw, qweight, scale_bf16, zero, dequant, (cudaStream_t)stream));
+    const Span out[3] = {{qweight, (size_t)K * N / 2}, {scale_bf16, (size_t)K * N / 64}, {zero, (size_t)K * N / 128}};
+    note_int4_writes((cudaStream_t)stream, out, 3);
+    return QZ_OK;
 }
 
 qz_status qz_gemm_w4a16_zp(const uint16_t* A, const int32_t* qweight, const uint16_t* scale_bf16,
@@ -72,7 +75,12 @@ qz_status qz_gemm_w4a16_zp(const uint16_t* A, const int32_t* qweight, const uint
         !is_aligned(zero, 4))
         return QZ_ERR_ALIGNMENT;
     QZ_TRY(device_check());
-    return gemm_w4a16_zp_launch(A, qweight, scale_bf16, zero, Y, M, N, K, (cudaStream_t)stream);
+    // as qz_gemm_w4a16_grouped: weights still in flight -> no dependent launch
+    const Int4Writes rec = int4_writes((cudaStream_t)stream);
+    const bool early = !w4a16_reads_in_flight(rec, qweight, scale_bf16, zero, N, K);
+    QZ_TRY(gemm_w4a16_zp_launch(A, qweight, scale_bf16, zero, Y, M, N, K, (cudaStream_t)stream, early));
+    if (!early) clear_int4_writes((cudaStream_t)stream, rec.gen);
+    return QZ_OK;
 }
 
 static qz_status w4a16_fp4_checks(const uint16_t* A, const uint8_t* qB, const uint8_t* sB, const uint16_t* Y,

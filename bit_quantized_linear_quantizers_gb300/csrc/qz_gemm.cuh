@@ -14,8 +14,11 @@ size_t ws_gemm_w4a16(int M, int N, int K);
 size_t ws_gemm_fp8_block(int M, int N, int K);
 size_t ws_gemm_fp4(int M, int N, int K);
 
+// early: launch under programmatic dependent launch (the kernels read their
+// weights before waiting for the previous kernel on the stream); false: after
+// all earlier work on the stream.
 qz_status gemm_w4a16_launch(const qz_w4a16_problem* problems, int count, void* ws, size_t ws_bytes,
-                            cudaStream_t st);
+                            cudaStream_t st, bool early);
 qz_status gemm_fp8_block_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
                                 uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
 qz_status gemm_fp8_block_quant_launch(const uint8_t* qA, const float* sA, const uint8_t* qB, const float* sB,
@@ -36,7 +39,7 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
 qz_status w4a16_error_read_and_clear();
 qz_status w4a16_tc_error_read_and_clear();
 // tcgen05 W4A16 for 17..64 tokens (mt = 32 or 64: the token count padded)
-qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st);
+qz_status w4a16_tc_launch(const qz_w4a16_problem* problems, int count, int mt, cudaStream_t st, bool early);
 qz_status fp8_block_error_read_and_clear();
 qz_status fp4_error_read_and_clear();
 qz_status selftest_error_read_and_clear();

@@ -189,6 +189,46 @@ qz_status launch_status();             // cudaGetLastError -> qz_status
 bool is_aligned(const void* p, size_t a);
 qz_status opt_in_smem(const void* fn, int bytes);   // thread-safe dynamic shared-memory opt-in
 
+// Stream order of INT4 weights. The W4A16 kernels start under programmatic
+// dependent launch: each lets the next kernel on the stream launch at its entry,
+// and reads its weights (not its activations) before griddepcontrol.wait. An
+// INT4 quantizer call lets its successor start only after its own wait, so its
+// outputs can still be in flight when a W4A16 kernel starts only if that kernel
+// follows it directly or through other W4A16 launches. Per device and stream,
+// the library keeps the byte ranges of the last INT4 quantizer call; a W4A16
+// call whose weights overlap them launches after all earlier work on the stream
+// and then clears the record. Other launches only complete earlier work, so
+// they leave the record as it is (at worst one later call waits needlessly).
+struct Span {
+    const void* p;
+    size_t bytes;
+};
+struct Int4Writes {
+    uint64_t gen;                      // changes with every noted call
+    int n;                             // 0: nothing in flight
+    Span s[3];
+};
+void note_int4_writes(cudaStream_t st, const Span* w, int n);   // n <= 3
+Int4Writes int4_writes(cudaStream_t st);                         // current device
+void clear_int4_writes(cudaStream_t st, uint64_t gen);           // unless noted again since gen
+
+inline bool spans_overlap(const Span& a, const Span& b) {
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a.bytes && b.bytes && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Does one W4A16 problem read (qweight int32 [K/8, N], scale bf16 [K/128, N],
+// zero uint8 [K/128, N] or none) overlap the recorded ranges?
+inline bool w4a16_reads_in_flight(const Int4Writes& rec, const void* qweight, const void* scale,
+                                  const void* zero, int N, int K) {
+    const size_t kn = (size_t)K * (size_t)N;
+    const Span r[3] = {{qweight, kn / 2}, {scale, kn / 64}, {zero, zero ? kn / 128 : 0}};
+    for (int i = 0; i < rec.n; i++)
+        for (const Span& x : r)
+            if (spans_overlap(rec.s[i], x)) return true;
+    return false;
+}
+
 } // namespace qz
 
 // Internal launchers (quantize.cu).

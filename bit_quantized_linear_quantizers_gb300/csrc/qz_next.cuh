@@ -25,7 +25,7 @@ qz_status int8_rows_launch(const void* x, qz_dtype xt, int64_t rows, int64_t col
                            int8_t* codes, float* scales, float* deq, cudaStream_t st);
 
 qz_status gemm_w4a16_zp_launch(const uint16_t* A, const int32_t* qweight, const uint16_t* scale, const uint8_t* zero,
-                               uint16_t* Y, int M, int N, int K, cudaStream_t st);
+                               uint16_t* Y, int M, int N, int K, cudaStream_t st, bool early);
 qz_status gemm_w4a16_fp4_launch(bool nv, const uint16_t* A, const uint8_t* qB, const uint8_t* sB, const float* gB,
                                 uint16_t* Y, int M, int N, int K, cudaStream_t st);
 qz_status gemm_int8_launch(const int8_t* qA, const float* sA, const int8_t* qB, const float* sB, uint16_t* Y, int M,

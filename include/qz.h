@@ -11,6 +11,17 @@
  *   default stream). Every call only enqueues work on that stream and returns
  *   without synchronising; outputs are valid in stream order. A workspace must
  *   not be shared by calls that may run concurrently.
+ * Early start: most calls launch under programmatic dependent launch, so their
+ *   kernels may begin while the previous kernel on the stream is still running.
+ *   Each waits for that kernel before it reads or writes anything, with one
+ *   exception. The INT4 W4A16 GEMMs (qz_gemm_w4a16, _grouped, _zp) read qweight,
+ *   scale_bf16 and zero BEFORE that wait, so the weight stream overlaps the
+ *   previous kernel's tail. The library tracks the outputs of its own INT4
+ *   quantizers per device and stream. A W4A16 call whose weights such a call may
+ *   still be writing is launched only after the stream's earlier work. Weights
+ *   written by other code must not come from the kernel enqueued directly
+ *   before the W4A16 call on its stream. Any synchronisation, copy or other
+ *   kernel between the two is enough.
  * Layout: row-major, leading dimension in elements. Packed 4-bit codes put
  *   the even-index element in the low nibble of each byte. bf16 data is passed
  *   as uint16_t bit patterns. Scales use the row-major layouts given per call.
