@@ -7,15 +7,17 @@ element 2^31 and is the block times 2^4, so the tensor's amax lies past the
 32-bit boundary. Outputs are pre-filled with a sentinel. Checked against the
 oracle, bit for bit, on rows on both sides of the boundary: the row-local
 formats on those rows, the 128 x 128 blocks and INT4 groups that hold them, and
-the per-tensor formats (FP8 per tensor, NVFP4) on a subset that includes the row
-holding the tensor's maximum, which fixes the same per-tensor scale."""
+the per-tensor formats (FP8 per tensor, NVFP4, the KV write) on a subset that
+includes the row holding the tensor's maximum, which fixes the same per-tensor
+scale. The block-scaled GEMMs (FP8, NVFP4, MXFP4, INT8) run at M x N = 65664 x
+32768 (2,151,677,952 outputs), sampled on rows on both sides of output 2^31."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synthetic as syn
-from gpu_util import assert_same_bytes, host
+from gpu_util import assert_same_bytes, check_gemm, host
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +74,7 @@ def max_row(base_f32):
 
 
 def sentinel(shape, dtype=torch.uint8):
-    return torch.full(shape, 0xA5, dtype=dtype, device="cuda")
+    return torch.full(shape, -91 if dtype == torch.int8 else 0xA5, dtype=dtype, device="cuda")   # byte 0xA5
 
 
 @pytest.mark.parametrize("gran", [oracle.FP8_PER_ROW, oracle.FP8_GROUP_1x128])
@@ -148,3 +150,106 @@ def test_int4_g128_past_2_31(qz, big):
         rq, rs, _ = oracle.quant_int4_g128(host_rows(base, rows), want_deq=False)
         assert_same_bytes(host(qw[g * 16:g * 16 + 16]), rq, f"int4 codes, group {g}")
         assert_same_bytes(host(sc[g:g + 1]).view(np.uint16), rs, f"int4 scales, group {g}")
+
+
+def test_int8_rows_past_2_31(qz, big):
+    x, base = big
+    q, s, _ = qz.qz_quantize_int8_rows(x, codes=sentinel((ROWS, COLS), torch.int8),
+                                       scales=torch.full((ROWS,), -1.0, device="cuda"))
+    torch.cuda.synchronize()
+    rows = np.array(SAMPLE)
+    rq, rs, _ = oracle.quant_int8_rows(host_rows(base, rows), want_deq=False)
+    idx = torch.from_numpy(rows).cuda()
+    assert_same_bytes(host(q[idx]).view(np.uint8), rq.view(np.uint8), "int8 codes")
+    assert_same_bytes(host(s[idx]), rs, "int8 scales")
+
+
+def test_kv_write_past_2_31(qz, big):
+    """K and V both the whole tensor as [1, 1, 524544, 4096]: each is one per-tensor FP8
+    quantization of 2,148,532,224 elements."""
+    x, base = big
+    kv = x.view(1, 1, ROWS, COLS)
+    kc, vc, ks, vs = qz.qz_kv_write_fp8(kv, kv, k_codes=sentinel(kv.shape), v_codes=sentinel(kv.shape))
+    torch.cuda.synchronize()
+    rows = np.array(SAMPLE + [max_row(base)])
+    sub = syn.to_bf16_bits(host_rows(base, rows))                 # exact: the values are bf16
+    rkc, rvc, rks, rvs, _, _ = oracle.kv_write_fp8(sub, sub)
+    idx = torch.from_numpy(rows).cuda()
+    assert_same_bytes(host(ks), np.float32([rks]), "k scale (amax past 2^31)")
+    assert_same_bytes(host(vs), np.float32([rvs]), "v scale")
+    assert_same_bytes(host(kc[0, 0][idx]), rkc, "k codes")
+    assert_same_bytes(host(vc[0, 0][idx]), rvc, "v codes")
+
+
+# ---------------------------------------------------- GEMM outputs past 2^31
+
+GM, GN = 65664, 32768                              # M x N = 2,151,677,952 outputs
+GROWS = [0, 1, 65535, 65536, GM - 1]               # row 65536 starts at output 2^31
+GCOLS = [0, 255, 256, 16384, GN - 1]
+
+
+def gemm_samples(seed):
+    rng = np.random.default_rng(seed)
+    ii, jj = np.meshgrid(GROWS, GCOLS, indexing="ij")
+    ii = np.concatenate([ii.ravel(), rng.integers(0, GM, 1000), rng.integers(65536, GM, 500)])
+    jj = np.concatenate([jj.ravel(), rng.integers(0, GN, 1500)])
+    return ii, jj
+
+
+def gemm_operands(K, seed):
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((GM, K)).astype(np.float32)
+    a[:, rng.choice(K, 2, replace=False)] *= np.float32(20)
+    bt = (rng.standard_normal((GN, K)) * 0.02).astype(np.float32)
+    return syn.to_bf16_bits(a), syn.to_bf16_bits(bt)
+
+
+def gather(Y, ii, jj):
+    return host(Y[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()])
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_fp8_block_gemm_output_past_2_31(qz):
+    a, bt = gemm_operands(128, seed=1)
+    qa, sa, _ = oracle.quant_fp8(a, oracle.FP8_GROUP_1x128, want_deq=False)
+    qb, sb, _ = oracle.quant_fp8(bt, oracle.FP8_BLOCK_128x128, want_deq=False)
+    Y = qz.qz_gemm_fp8_block(dev(qa), dev(sa), dev(qb), dev(sb))
+    torch.cuda.synchronize()
+    ii, jj = gemm_samples(1)
+    y_ref, bound = oracle.gemm_fp8_block(qa, sa, qb, sb, ii, jj)
+    check_gemm(gather(Y, ii, jj), y_ref, bound, "fp8 block GEMM, outputs past 2^31", 1e-3)
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+def test_fp4_gemm_output_past_2_31(qz, fmt):
+    a, bt = gemm_operands(256, seed=2)
+    if fmt == "nv":
+        ca, sa, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+        cb, sb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+        ops = (ca, sa, ga, cb, sb, gb)
+        Y = qz.qz_gemm_nvfp4(dev(ca), dev(sa), dev(np.float32([ga])), dev(cb), dev(sb), dev(np.float32([gb])))
+        ref = oracle.gemm_nvfp4
+    else:
+        ca, ea, _ = oracle.quant_mxfp4(a, want_deq=False)
+        cb, eb, _ = oracle.quant_mxfp4(bt, want_deq=False)
+        ops = (ca, ea, cb, eb)
+        Y = qz.qz_gemm_mxfp4(dev(ca), dev(ea), dev(cb), dev(eb))
+        ref = oracle.gemm_mxfp4
+    torch.cuda.synchronize()
+    ii, jj = gemm_samples(2)
+    y_ref, bound = ref(*ops, ii, jj)
+    check_gemm(gather(Y, ii, jj), y_ref, bound, f"{fmt}fp4 GEMM, outputs past 2^31", 1e-3)
+
+
+def test_int8_gemm_output_past_2_31(qz):
+    a, bt = gemm_operands(64, seed=3)
+    qa, sa, _ = oracle.quant_int8_rows(a, want_deq=False)
+    qb, sb, _ = oracle.quant_int8_rows(bt, want_deq=False)
+    Y = qz.qz_gemm_int8(dev(qa), dev(sa), dev(qb), dev(sb))
+    torch.cuda.synchronize()
+    ii, jj = gemm_samples(3)
+    y_ref, bound = oracle.gemm_int8(qa, sa, qb, sb, ii, jj)
+    check_gemm(gather(Y, ii, jj), y_ref, bound, "int8 GEMM, outputs past 2^31", 1e-3)
