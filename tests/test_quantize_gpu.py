@@ -114,6 +114,27 @@ def test_fp8_config3_full_size_sampled(qz):
         assert_same_bytes(sb[bi:bi + 1, bj:bj + 1], rs, f"B block scale {bi},{bj}")
 
 
+@pytest.mark.parametrize("shape,dtype", [((2048, 4096), "bf16"), ((1000, 4224), "f32"), ((3001, 1280), "bf16"),
+                                         ((8192, 4096), "bf16")])
+def test_fp8_group_large_contiguous(qz, shape, dtype):
+    """FP8 1x128 on large contiguous tensors: the bench's A (2048 x 4096 bf16), group
+    counts that leave a ragged last grid-stride step, fp32 input, and a 67 MB tensor.
+    The format is row-local, so rows are compared bit for bit (codes, scales,
+    dequant): the first two, the last two and 60 at random."""
+    rows, cols = shape
+    x = edge_tensor(rows, cols, seed=rows)
+    x = syn.to_bf16_bits(x) if dtype == "bf16" else x
+    c, s, d = qz.qz_quantize_fp8(to_dev(x), oracle.FP8_GROUP_1x128, dequant=True)
+    c, s, d = host(c), host(s), host(d)
+    assert qz.qz_device_error() == 0
+    pick = {0, 1, rows - 2, rows - 1} | set(np.random.default_rng(rows).choice(rows, 60, replace=False).tolist())
+    pick = np.array(sorted(pick))
+    rc, rs, rd = oracle.quant_fp8(x[pick], oracle.FP8_GROUP_1x128)
+    assert_same_bytes(c[pick], rc, f"large {shape} {dtype} codes")
+    assert_same_bytes(s[pick], rs, f"large {shape} {dtype} scales")
+    assert_same_bytes(d[pick], rd, f"large {shape} {dtype} dequant")
+
+
 # ------------------------------------------------------------- MXFP4
 
 def check_mx(qz, x, what):
