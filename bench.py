@@ -488,6 +488,28 @@ def fp4_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp4_peak):
                           "frac": round(fl / us / 1e6 / fp4_peak, 4)}
         except qz.QZError as e:
             rows[name] = {"unavailable": str(e)}
+    # f1 for NVFP4: the GEMM's output leaves as NVFP4 codes + block scales (tensor amax
+    # given: the plain GEMM's own output amax), against the GEMM then the quantizer
+    if "nvfp4_gemm_8192x4096x4096" in rows and "us" in rows["nvfp4_gemm_8192x4096x4096"]:
+        with torch.cuda.stream(stream):
+            qz.qz_gemm_nvfp4(*nvA[0], *nvB, Y=ys[0], ws=ws, stream=stream)
+            amax = ys[0].float().abs().max().reshape(1)
+            yq = qz.qz_gemm_nvfp4_quant(*nvA[0], *nvB, amax, ws=ws, stream=stream)
+            sep = qz.qz_quantize_nvfp4(ys[1], global_amax_in=amax, stream=stream)[:3]
+        us_fused = timer(lambda i: qz.qz_gemm_nvfp4_quant(*nvA[i % na], *nvB, amax, y_codes=yq[0], y_scales=yq[1],
+                                                          y_global=yq[2], ws=ws, stream=stream), 4 * na)
+
+        def separate(i):
+            qz.qz_gemm_nvfp4(*nvA[i % na], *nvB, Y=ys[1], ws=ws, stream=stream)
+            qz.qz_quantize_nvfp4(ys[1], codes=sep[0], scale_e4m3=sep[1], global_scale=sep[2], global_amax_in=amax,
+                                 stream=stream)
+        us_sep = timer(separate, 4 * na)
+        rows["nvfp4_gemm_with_nvfp4_output_8192x4096x4096"] = {
+            "fused_us": round(us_fused, 2), "gemm_then_quantizer_us": round(us_sep, 2),
+            "tflops_fused": round(fl / us_fused / 1e6, 1), "frac_of_fp4_peak_fused": round(fl / us_fused / 1e6 / fp4_peak, 4),
+            "hbm_bytes_saved_per_call": M4 * N4 * 2 * 2,
+            "note": "fused: NVFP4 codes + block scales with a given tensor amax; separate: bf16 output written, "
+                    "read back and quantized with the same amax"}
     del a_d, bt_d
 
 

@@ -24,7 +24,8 @@ __all__ = [
     "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
     "qz_kv_write_fp8_per_head", "qz_kv_write_fp8_channel_zp", "qz_quantize_int4_g128_zp", "qz_gemm_w4a16_zp",
     "qz_gemm_w4a16_nvfp4", "qz_gemm_w4a16_mxfp4", "qz_col_amax", "qz_smooth_factors", "qz_quantize_int8_rows",
-    "qz_gemm_int8", "qz_gemm_fp8_block_quant", "SMOOTH_NONE", "SMOOTH_DIVIDE", "SMOOTH_MULTIPLY",
+    "qz_gemm_int8", "qz_gemm_fp8_block_quant", "qz_gemm_nvfp4_quant", "SMOOTH_NONE", "SMOOTH_DIVIDE",
+    "SMOOTH_MULTIPLY",
 ]
 
 F32, BF16 = 0, 1
@@ -90,6 +91,7 @@ _SIGS = {
     "qz_quantize_int8_rows": (_I, [_P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P]),
     "qz_gemm_int8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "qz_gemm_fp8_block_quant": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "qz_gemm_nvfp4_quant": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -443,6 +445,31 @@ def qz_gemm_nvfp4(qA, sA, gA, qB, sB, gB, Y=None, ws=None, stream=None):
     buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), d)
     _check(lib.qz_gemm_nvfp4(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4")
     return Y
+
+
+def qz_gemm_nvfp4_quant(qA, sA, gA, qB, sB, gB, y_amax, y_codes=None, y_scales=None, y_global=None, ws=None,
+                        stream=None):
+    """NVFP4 GEMM whose output leaves quantized to NVFP4 with the given tensor amax
+    (device fp32 scalar). Returns (codes u8 [M, N/2], E4M3 block scales u8 [M, N/16],
+    tensor scale fp32 [1]): what qz_quantize_nvfp4 gives for the bf16 output with that
+    amax."""
+    M, K = qA.shape[0], qA.shape[1] * 2
+    N = qB.shape[0]
+    d = _device()
+    dev = qA.device
+    if y_codes is None:
+        y_codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    if y_scales is None:
+        y_scales = torch.empty((M, N // 16), dtype=torch.uint8, device=dev)
+    if y_global is None:
+        y_global = torch.empty((1,), dtype=torch.float32, device=dev)
+    args = (_arg(qA, "qA", d, 1, M * K // 2), _arg(sA, "sA", d, 1, M * (K // 16)), _arg(gA, "gA", d, torch.float32, 1),
+            _arg(qB, "qB", d, 1, N * K // 2), _arg(sB, "sB", d, 1, N * (K // 16)), _arg(gB, "gB", d, torch.float32, 1),
+            _arg(y_amax, "y_amax", d, torch.float32, 1), _arg(y_codes, "y_codes", d, 1, M * N // 2),
+            _arg(y_scales, "y_scales", d, 1, M * N // 16), _arg(y_global, "y_global", d, torch.float32, 1))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), d)
+    _check(lib.qz_gemm_nvfp4_quant(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4_quant")
+    return y_codes, y_scales, y_global
 
 
 def qz_gemm_nvfp4_noalloc(qA, sA, gA, qB, sB, gB, Y=None, stream=None):

@@ -45,6 +45,7 @@
 #include "qz_tc.cuh"
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 namespace qz {
@@ -140,14 +141,28 @@ struct Fp4Prob {
 constexpr int FP4_PER_LAUNCH = 72;
 static_assert(sizeof(Fp4Maps) == 384 && sizeof(Fp4Prob) == 64, "problem table layout");
 
+// NVFP4 output of a single-problem launch (QOUT): codes [M, N/2], E4M3 block
+// scales [M, N/16], the tensor scale g from the caller's amax.
+struct Fp4Qout {
+    uint8_t* codes;
+    uint8_t* scales;
+    const float* amax;
+    float* g;
+};
+
 struct Fp4Params {
     Fp4Maps m[FP4_PER_LAUNCH];
     Fp4Prob p[FP4_PER_LAUNCH];
+    Fp4Qout q;
     int count;
     int total_tiles;
 };
 
-template <bool NV>
+// QOUT (NVFP4 only): instead of bf16 Y the epilogue writes Y quantized for the
+// next layer: each value rounded to bf16 as the plain epilogue rounds it, then
+// NVFP4 with the caller's tensor amax, exactly as qz_quantize_nvfp4 with a given
+// amax encodes that bf16 tensor (one thread per row: 16-byte code stores).
+template <bool NV, bool QOUT = false>
 __global__ void __launch_bounds__(THREADS, 1)
 fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
     constexpr int G = NV ? 4 : 2;                 // scale atoms per row block per stage
@@ -316,6 +331,36 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);          // the next tile's MMAs may start
+            if constexpr (QOUT) {
+                const float g = div_rn(fmaxf(__ldg(P.q.amax), kAmaxMin), kFp8Max * kFp4Max);
+                if (tcount == 0 && blockIdx.x == 0 && warp == 2 && lane == 0) *P.q.g = g;
+                const Recip dg(g), d6(kFp4Max);
+                const int row = m0 + q * 32 + lane;
+                if (row < pr.M) {
+                    const int c0 = n0 + h * 128;         // this thread's 128 columns
+                    uint8_t* crow = P.q.codes + (size_t)row * (pr.N / 2) + c0 / 2;
+                    uint32_t sc[2] = {0u, 0u};
+#pragma unroll
+                    for (int b2 = 0; b2 < 4; b2++) {     // two 16-column blocks per 16-byte store
+                        uint2 pk[2];
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            const int b = 2 * b2 + u;
+                            float y[16];
+#pragma unroll
+                            for (int e = 0; e < 16; e++)
+                                y[e] = __bfloat162float(__float2bfloat16_rn(
+                                    __uint_as_float(v[b >> 1][(b & 1) * 16 + e]) * gscale));
+                            uint32_t bcode;
+                            pk[u] = nvfp4_block16(y, g, dg, d6, bcode);
+                            sc[b >> 2] |= bcode << (8 * (b & 3));
+                        }
+                        *reinterpret_cast<uint4*>(crow + 16 * b2) = make_uint4(pk[0].x, pk[0].y, pk[1].x, pk[1].y);
+                    }
+                    *reinterpret_cast<uint2*>(P.q.scales + (size_t)row * (pr.N / 16) + c0 / 16) = make_uint2(sc[0], sc[1]);
+                }
+                continue;
+            }
             // 16-column chunks through the staging tile, each written by one TMA store
             // (rows past M fall outside the tensor and are not written)
 #pragma unroll
@@ -356,9 +401,10 @@ size_t round1k(size_t b) { return (b + 1023) & ~size_t(1023); }
 bool fill_problem(Fp4Maps& mp, Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA, const float* gA, const uint8_t* qB,
                   const uint8_t* sfB, const float* gB, uint16_t* Y, int M, int N, int K, int& tiles) {
     if (!encode_tmap_2d_u8(&mp.tmA, qA, (uint64_t)K / 2, (uint64_t)M, (uint64_t)K / 2, BKB, BM) ||
-        !encode_tmap_2d_u8(&mp.tmB, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN) ||
-        !encode_tmap_2d_swz(&mp.tmY, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 16, 32, 32))
+        !encode_tmap_2d_u8(&mp.tmB, qB, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, BKB, BN))
         return false;
+    if (Y && !encode_tmap_2d_swz(&mp.tmY, Y, 2, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 16, 32, 32)) return false;
+    if (!Y) memset(&mp.tmY, 0, sizeof(mp.tmY));                 // QOUT: no bf16 output
     p.sfA = sfA; p.sfB = sfB; p.gA = gA; p.gB = gB; p.Y = Y;
     p.M = M; p.N = N; p.K = K;
     p.mt = (M + BM - 1) / BM;
@@ -367,11 +413,14 @@ bool fill_problem(Fp4Maps& mp, Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA
     return true;
 }
 
-qz_status launch_table(bool nv, const Fp4Params& P, cudaStream_t st) {
-    const void* fn = nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
+qz_status launch_table(bool nv, const Fp4Params& P, cudaStream_t st, bool qout = false) {
+    const void* fn = qout ? (const void*)fp4_gemm_kernel<true, true>
+                          : nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
     QZ_TRY(opt_in_smem(fn, SMEM_BYTES));
     const int grid = std::min(P.total_tiles, num_sms());
-    if (nv)
+    if (qout)
+        fp4_gemm_kernel<true, true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
+    else if (nv)
         fp4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
     else
         fp4_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(P);
@@ -401,7 +450,13 @@ qz_status fp4_error_read_and_clear() {
 
 qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
                           const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
-                          int M, int N, int K, void* ws, size_t, cudaStream_t st) {
+                          int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st) {
+    return gemm_fp4_launch_q(nv, qA, sA, gA, qB, sB, gB, Y, nullptr, M, N, K, ws, ws_bytes, st);
+}
+
+qz_status gemm_fp4_launch_q(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
+                            const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
+                            const qz_nvfp4_out* yq, int M, int N, int K, void* ws, size_t, cudaStream_t st) {
     uint8_t* wsA = static_cast<uint8_t*>(ws);
     uint8_t* wsB = wsA + round1k(sf_bytes(true, M, K));
     const int ks = K / (nv ? 16 : 32);
@@ -414,9 +469,10 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
     Fp4Params P;
     int tiles = 0;
     if (!fill_problem(P.m[0], P.p[0], qA, wsA, gA, qB, wsB, gB, Y, M, N, K, tiles)) return QZ_ERR_CUDA;
+    P.q = yq ? Fp4Qout{yq->codes, yq->scales, yq->amax, yq->g} : Fp4Qout{nullptr, nullptr, nullptr, nullptr};
     P.count = 1;
     P.total_tiles = tiles;
-    return launch_table(nv, P, st);
+    return launch_table(nv, P, st, yq != nullptr);
 }
 
 qz_status gemm_nvfp4_grouped_launch(const qz_nvfp4_problem* problems, int count, void* ws, size_t,

@@ -79,24 +79,6 @@ __device__ __forceinline__ void fp8_encode8(const float v[8], const Recip& d, ui
     }
 }
 
-// Encode one 16-element block to E2M1 with scale d.s (correctly rounded
-// quotients, ties to the smaller magnitude); returns the 16 nibbles (element j
-// at bit 4j of word j / 8); writes the dequantized block if asked.
-__device__ __forceinline__ uint2 fp4_encode16(const float v[16], const Recip& d, float* deq) {
-    float y[16];
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) div1x2(v[j], v[j + 1], d, y[j], y[j + 1]);
-    const uint2 packed = make_uint2(e2m1x8_tiesdown(y), e2m1x8_tiesdown(y + 8));
-    if (deq) {
-        float o[16];
-#pragma unroll
-        for (int j = 0; j < 16; j++) o[j] = __fmul_rn(e2m1_value((j < 8 ? packed.x : packed.y) >> (4 * (j & 7))), d.s);
-#pragma unroll
-        for (int q = 0; q < 4; q++) reinterpret_cast<float4*>(deq)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-    }
-    return packed;
-}
-
 // Element offset of chunk i (8 elements per chunk when VEC, 1 otherwise).
 template <bool VEC>
 __device__ __forceinline__ int64_t chunk_offset(int64_t i, bool contig, int64_t cpr, int64_t ldx) {

@@ -391,6 +391,19 @@ qz_status qz_gemm_nvfp4(const uint8_t* qA, const uint8_t* sA, const float* gA,
     return gemm_fp4_launch(true, qA, sA, gA, qB, sB, gB, Y, M, N, K, ws, ws_bytes, (cudaStream_t)stream);
 }
 
+qz_status qz_gemm_nvfp4_quant(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                              const uint8_t* qB, const uint8_t* sB, const float* gB,
+                              const float* y_amax, uint8_t* y_codes, uint8_t* y_scales, float* y_global,
+                              int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+    if (!gA || !gB || !y_amax || !y_codes || !y_scales || !y_global) return QZ_ERR_INVALID_ARG;
+    // the bf16 output is not written: Y's checks run on a stand-in aligned pointer
+    QZ_TRY(fp4_gemm_checks(qA, sA, qB, sB, y_codes, M, N, K, ws, ws_bytes));
+    if (!is_aligned(y_scales, 8) || !is_aligned(y_amax, 4) || !is_aligned(y_global, 4)) return QZ_ERR_ALIGNMENT;
+    QZ_TRY(device_check());
+    const qz_nvfp4_out yq{y_codes, y_scales, y_amax, y_global};
+    return gemm_fp4_launch_q(true, qA, sA, gA, qB, sB, gB, nullptr, &yq, M, N, K, ws, ws_bytes, (cudaStream_t)stream);
+}
+
 qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
                         uint16_t* Y, int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
     QZ_TRY(fp4_gemm_checks(qA, eA, qB, eB, Y, M, N, K, ws, ws_bytes));

@@ -33,6 +33,20 @@ constexpr int kNvfp4MaxProblems = 256;
 qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
                           const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
                           int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
+// NVFP4 output of qz_gemm_nvfp4_quant: codes [M, N/2], E4M3 block scales
+// [M, N/16], the tensor scale g computed from the caller's amax.
+struct qz_nvfp4_out {
+    uint8_t* codes;
+    uint8_t* scales;
+    const float* amax;
+    float* g;
+};
+// As gemm_fp4_launch; with yq (NVFP4 only) the output is quantized instead of
+// written as bf16 (Y unused).
+qz_status gemm_fp4_launch_q(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
+                            const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
+                            const qz_nvfp4_out* yq, int M, int N, int K, void* ws, size_t ws_bytes,
+                            cudaStream_t st);
 
 // Device error words of the GEMM translation units (read and cleared by
 // qz_device_error). Each returns QZ_OK, QZ_ERR_TIMEOUT or QZ_ERR_CUDA.

@@ -177,6 +177,37 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
     return (c & 8u) ? -v : v;
 }
 
+// Encode one 16-element block to E2M1 with scale d.s (correctly rounded
+// quotients, ties to the smaller magnitude); returns the 16 nibbles (element j
+// at bit 4j of word j / 8); writes the dequantized block if asked.
+__device__ __forceinline__ uint2 fp4_encode16(const float v[16], const Recip& d, float* deq) {
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) div1x2(v[j], v[j + 1], d, y[j], y[j + 1]);
+    const uint2 packed = make_uint2(e2m1x8_tiesdown(y), e2m1x8_tiesdown(y + 8));
+    if (deq) {
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) o[j] = __fmul_rn(e2m1_value((j < 8 ? packed.x : packed.y) >> (4 * (j & 7))), d.s);
+#pragma unroll
+        for (int q = 0; q < 4; q++) reinterpret_cast<float4*>(deq)[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+    return packed;
+}
+
+// NVFP4 block of 16 values with tensor scale g (dg = Recip(g), d6 = Recip(6)):
+// the block scale code E4M3(amax16 / 6 / g) and the 16 E2M1 codes of v / s with
+// s = max(E4M3 value, 1e-12) * g (element j at bit 4j of word j / 8).
+__device__ __forceinline__ uint2 nvfp4_block16(const float v[16], float g, const Recip& dg, const Recip& d6,
+                                               uint32_t& bcode) {
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; j++) m = fmaxf(m, fabsf(v[j]));
+    bcode = e4m3_code(div1(div1(m, d6), dg));
+    const float sv = __fmul_rn(fmaxf(e4m3_value(bcode), kAmaxMin), g);
+    return fp4_encode16(v, Recip(sv), nullptr);
+}
+
 __device__ __forceinline__ float warp_max(float v, int width) {
     for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;

@@ -440,6 +440,25 @@ qz_status qz_gemm_fp8_block_quant(const uint8_t* qA, const float* sA, const uint
                                   uint16_t* Y, uint8_t* y_codes, float* y_scales, int M, int N, int K,
                                   void* stream);
 
+/* NVFP4 GEMM whose epilogue quantizes its output to NVFP4 for the next layer
+ * ("量化部署实战", 练习 2: activation scales computed at the end of the previous
+ * kernel; 格式速查: NVFP4, E2M1 + E4M3 per 16 + fp32 per tensor). The same
+ * arithmetic as qz_gemm_nvfp4 up to the bf16 output y, which is then encoded
+ * exactly as qz_quantize_nvfp4(y, global_amax_in = y_amax) would:
+ *   g = max(*y_amax, 1e-12) / 2688 (written to y_global);
+ *   per 16 columns: s_code = E4M3(amax16 / 6 / g), s = max(e4m3(s_code), 1e-12) * g,
+ *   codes = E2M1(y / s).
+ * The tensor amax is the caller's (a calibrated or previous-step value): the
+ * kernel cannot know the output's own amax before every tile is done. Blocks
+ * whose amax exceeds it saturate as in the quantizer.
+ * y_codes: [M, N/2] bytes (16 B aligned); y_scales: E4M3 [M, N/16] (8 B aligned);
+ * y_amax, y_global: one fp32 each (device). No bf16 output is written. Other
+ * shapes, layouts, workspace and alignment as qz_gemm_nvfp4. */
+qz_status qz_gemm_nvfp4_quant(const uint8_t* qA, const uint8_t* sA, const float* gA,
+                              const uint8_t* qB, const uint8_t* sB, const float* gB,
+                              const float* y_amax, uint8_t* y_codes, uint8_t* y_scales, float* y_global,
+                              int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
 /* NVFP4 GEMM that allocates nothing and takes no workspace. (The quantization
  * pages have no counterpart: this is an interface convenience of this library.)
  * Some callers cannot call cudaMalloc or hand this library a workspace: runtimes

@@ -120,6 +120,13 @@ def test_gemm_validation(qz):
     assert L.qz_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 200, 256, NULL, 0, NULL) == 2
     assert L.qz_gemm_mxfp4(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 100, NULL, 0, NULL) == 2
     assert L.qz_gemm_mxfp4(ODD, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 3
+    # qA, sA, gA, qB, sB, gB, y_amax, y_codes, y_scales, y_global, M, N, K, ws, ws_bytes, stream
+    q = L.qz_gemm_nvfp4_quant
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 1  # amax
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, 128, 256, 256, NULL, 0, NULL) == 1
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 200, 256, NULL, 0, NULL) == 2  # N
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ODD, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 3   # codes
+    assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 7  # ws
 
 
 def test_grouped_nvfp4_and_prepare_validation(qz):

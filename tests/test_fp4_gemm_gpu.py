@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synthetic as syn
-from gpu_util import bf16_bits_to_f64, check_gemm, host
+from gpu_util import assert_same_bytes, bf16_bits_to_f64, check_gemm, host
 
 pytestmark = pytest.mark.gpu
 
@@ -223,3 +223,52 @@ def test_nvfp4_grouped_qwen_layer(qz):
     qz.qz_gemm_nvfp4_grouped(probs)
     for (name, y_ref, bound), p in zip(refs, probs):
         check(host(p[6]), y_ref, bound, f"qwen {name}")
+
+
+# ---------------------------------------- NVFP4 GEMM with NVFP4 output
+
+def test_nvfp4_gemm_quantized_output_exact_case(qz):
+    """Unit scales and E2M1 codes of small integers make every sum exact, so the output
+    the epilogue quantizes is the oracle's exact product rounded once to bf16: codes,
+    block scales and the tensor scale bit-exact against the oracle's NVFP4 quantizer of
+    that output with the same given amax (a value below the output's own amax, so
+    some blocks saturate, and one above it)."""
+    rng = np.random.default_rng(31)
+    M, N, K = 256, 512, 256
+    mag = np.array([0, 2, 4, 5, 6, 7])                    # 0, 1, 2, 3, 4, 6
+    ca = (rng.choice(mag, (M, K)) | (rng.integers(0, 2, (M, K)) << 3)).astype(np.uint8)
+    cb = (rng.choice(mag, (N, K)) | (rng.integers(0, 2, (N, K)) << 3)).astype(np.uint8)
+    va = np.vectorize(oracle.e2m1_decode)(ca)
+    vb = np.vectorize(oracle.e2m1_decode)(cb)
+    ybf = syn.to_bf16_bits((va @ vb.T).astype(np.float32))
+    one = 0x38
+    ops = (dev(pack(ca)), dev(np.full((M, K // 16), one, np.uint8)), dev(np.float32([1.0])),
+           dev(pack(cb)), dev(np.full((N, K // 16), one, np.uint8)), dev(np.float32([1.0])))
+    amax = float(np.abs(bf16_bits_to_f64(ybf)).max())
+    for given in (amax * 0.25, amax * 1.5):
+        codes, sb, g = qz.qz_gemm_nvfp4_quant(*ops, dev(np.float32([given])))
+        rc, rs, rg, _ = oracle.quant_nvfp4(ybf, amax_in=np.float32(given), want_deq=False)
+        assert_same_bytes(host(codes), rc, f"codes, amax {given}")
+        assert_same_bytes(host(sb), rs, f"block scales, amax {given}")
+        assert_same_bytes(host(g).reshape(np.shape(rg)), np.asarray(rg, np.float32), f"tensor scale, amax {given}")
+    assert qz.qz_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (384, 768, 512), (1152, 1024, 768), (8192, 4096, 4096)])
+def test_nvfp4_gemm_quantized_output_matches_gemm_then_quantizer(qz, M, N, K):
+    """Realistic operands over one tile, several tiles in both directions, more tiles
+    than SMs, and the prefill shape: the fused codes, block scales and tensor scale
+    equal qz_quantize_nvfp4 with the same given amax applied to the plain NVFP4 GEMM's
+    bf16 output, bit for bit."""
+    a, bt = inputs(M, N, K, seed=M + N)
+    ca, sa, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+    cb, sb, gb, _ = oracle.quant_nvfp4(bt, want_deq=False)
+    ops = (dev(ca), dev(sa), dev(np.float32([ga])), dev(cb), dev(sb), dev(np.float32([gb])))
+    y = qz.qz_gemm_nvfp4(*ops)
+    amax = dev(np.float32([float(torch.max(torch.abs(y.float())))]))
+    codes, scales, g = qz.qz_gemm_nvfp4_quant(*ops, amax)
+    c2, s2, g2, _ = qz.qz_quantize_nvfp4(y, global_amax_in=amax)
+    assert np.array_equal(host(codes), host(c2)), "codes differ from GEMM then quantizer"
+    assert np.array_equal(host(scales), host(s2)), "block scales differ from GEMM then quantizer"
+    assert np.array_equal(host(g), host(g2)), "tensor scale differs"
+    assert qz.qz_device_error() == 0
