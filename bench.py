@@ -510,6 +510,22 @@ def fp4_rows(qz, syn, stream, dev, pk, timer, ws, bf, rows, q, fp4_peak):
             "hbm_bytes_saved_per_call": M4 * N4 * 2 * 2,
             "note": "fused: NVFP4 codes + block scales with a given tensor amax; separate: bf16 output written, "
                     "read back and quantized with the same amax"}
+    if "mxfp4_gemm_8192x4096x4096" in rows and "us" in rows["mxfp4_gemm_8192x4096x4096"]:
+        with torch.cuda.stream(stream):
+            yq = qz.qz_gemm_mxfp4_quant(*mxA[0], *mxB, ws=ws, stream=stream)
+            sep = qz.qz_quantize_mxfp4(ys[1], stream=stream)[:2]
+        us_fused = timer(lambda i: qz.qz_gemm_mxfp4_quant(*mxA[i % na], *mxB, y_codes=yq[0], y_e8m0=yq[1], ws=ws,
+                                                          stream=stream), 4 * na)
+
+        def separate_mx(i):
+            qz.qz_gemm_mxfp4(*mxA[i % na], *mxB, Y=ys[1], ws=ws, stream=stream)
+            qz.qz_quantize_mxfp4(ys[1], codes=sep[0], scale_e8m0=sep[1], stream=stream)
+        us_sep = timer(separate_mx, 4 * na)
+        rows["mxfp4_gemm_with_mxfp4_output_8192x4096x4096"] = {
+            "fused_us": round(us_fused, 2), "gemm_then_quantizer_us": round(us_sep, 2),
+            "tflops_fused": round(fl / us_fused / 1e6, 1), "frac_of_fp4_peak_fused": round(fl / us_fused / 1e6 / fp4_peak, 4),
+            "hbm_bytes_saved_per_call": M4 * N4 * 2 * 2,
+            "note": "fused: MXFP4 codes + E8M0 scales; separate: bf16 output written, read back and quantized"}
     del a_d, bt_d
 
 

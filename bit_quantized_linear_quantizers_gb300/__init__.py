@@ -24,7 +24,8 @@ __all__ = [
     "qz_gemm_nvfp4_grouped", "qz_quantize_nvfp4_grouped", "Workspace",
     "qz_kv_write_fp8_per_head", "qz_kv_write_fp8_channel_zp", "qz_quantize_int4_g128_zp", "qz_gemm_w4a16_zp",
     "qz_gemm_w4a16_nvfp4", "qz_gemm_w4a16_mxfp4", "qz_col_amax", "qz_smooth_factors", "qz_quantize_int8_rows",
-    "qz_gemm_int8", "qz_gemm_fp8_block_quant", "qz_gemm_nvfp4_quant", "SMOOTH_NONE", "SMOOTH_DIVIDE",
+    "qz_gemm_int8", "qz_gemm_fp8_block_quant", "qz_gemm_nvfp4_quant", "qz_gemm_mxfp4_quant", "SMOOTH_NONE",
+    "SMOOTH_DIVIDE",
     "SMOOTH_MULTIPLY",
 ]
 
@@ -92,6 +93,7 @@ _SIGS = {
     "qz_gemm_int8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "qz_gemm_fp8_block_quant": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "qz_gemm_nvfp4_quant": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "qz_gemm_mxfp4_quant": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -470,6 +472,25 @@ def qz_gemm_nvfp4_quant(qA, sA, gA, qB, sB, gB, y_amax, y_codes=None, y_scales=N
     buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_NVFP4, M, N, K), d)
     _check(lib.qz_gemm_nvfp4_quant(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_nvfp4_quant")
     return y_codes, y_scales, y_global
+
+
+def qz_gemm_mxfp4_quant(qA, eA, qB, eB, y_codes=None, y_e8m0=None, ws=None, stream=None):
+    """MXFP4 GEMM whose output leaves quantized to MXFP4. Returns (codes u8 [M, N/2], E8M0
+    scales u8 [M, N/32]): what qz_quantize_mxfp4 gives for the bf16 output."""
+    M, K = qA.shape[0], qA.shape[1] * 2
+    N = qB.shape[0]
+    d = _device()
+    dev = qA.device
+    if y_codes is None:
+        y_codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    if y_e8m0 is None:
+        y_e8m0 = torch.empty((M, N // 32), dtype=torch.uint8, device=dev)
+    args = (_arg(qA, "qA", d, 1, M * K // 2), _arg(eA, "eA", d, 1, M * (K // 32)),
+            _arg(qB, "qB", d, 1, N * K // 2), _arg(eB, "eB", d, 1, N * (K // 32)),
+            _arg(y_codes, "y_codes", d, 1, M * N // 2), _arg(y_e8m0, "y_e8m0", d, 1, M * N // 32))
+    buf, nb = _ws(ws, qz_workspace_size(OP_GEMM_MXFP4, M, N, K), d)
+    _check(lib.qz_gemm_mxfp4_quant(*args, M, N, K, _ptr(buf), nb, _stream(stream)), "qz_gemm_mxfp4_quant")
+    return y_codes, y_e8m0
 
 
 def qz_gemm_nvfp4_noalloc(qA, sA, gA, qB, sB, gB, Y=None, stream=None):

@@ -158,10 +158,12 @@ struct Fp4Params {
     int total_tiles;
 };
 
-// QOUT (NVFP4 only): instead of bf16 Y the epilogue writes Y quantized for the
-// next layer: each value rounded to bf16 as the plain epilogue rounds it, then
-// NVFP4 with the caller's tensor amax, exactly as qz_quantize_nvfp4 with a given
-// amax encodes that bf16 tensor (one thread per row: 16-byte code stores).
+// QOUT: instead of bf16 Y the epilogue writes Y quantized for the next layer:
+// each value rounded to bf16 as the plain epilogue rounds it, then, in the
+// GEMM's own format, NVFP4 with the caller's tensor amax (exactly as
+// qz_quantize_nvfp4 with a given amax encodes that bf16 tensor) or MXFP4
+// (exactly as qz_quantize_mxfp4 encodes it). One thread per row: 16-byte code
+// stores, the row's scale bytes of the tile in one store.
 template <bool NV, bool QOUT = false>
 __global__ void __launch_bounds__(THREADS, 1)
 fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
@@ -331,6 +333,34 @@ fp4_gemm_kernel(const __grid_constant__ Fp4Params P) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);          // the next tile's MMAs may start
+            if constexpr (QOUT && !NV) {
+                const int row = m0 + q * 32 + lane;
+                if (row < pr.M) {
+                    const int c0 = n0 + h * 128;         // this thread's 128 columns: 4 blocks of 32
+                    uint8_t* crow = P.q.codes + (size_t)row * (pr.N / 2) + c0 / 2;
+                    uint32_t e4 = 0u;
+#pragma unroll
+                    for (int b = 0; b < 4; b++) {
+                        float y[32];
+                        float m = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 32; e++) {
+                            y[e] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(v[b][e])));
+                            m = fmaxf(m, fabsf(y[e]));
+                        }
+                        m = fmaxf(m, kAmaxMin);
+                        const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;   // m is normal
+                        const float inv = __uint_as_float((uint32_t)(127 + 2 - E) << 23);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int o = 0; o < 4; o++) w[o] = mxfp4_encode8<true>(y + 8 * o, inv);
+                        *reinterpret_cast<uint4*>(crow + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+                        e4 |= (uint32_t)(E - 2 + 127) << (8 * b);
+                    }
+                    *reinterpret_cast<uint32_t*>(P.q.scales + (size_t)row * (pr.N / 32) + c0 / 32) = e4;
+                }
+                continue;
+            }
             if constexpr (QOUT) {
                 const float g = div_rn(fmaxf(__ldg(P.q.amax), kAmaxMin), kFp8Max * kFp4Max);
                 if (tcount == 0 && blockIdx.x == 0 && warp == 2 && lane == 0) *P.q.g = g;
@@ -414,12 +444,14 @@ bool fill_problem(Fp4Maps& mp, Fp4Prob& p, const uint8_t* qA, const uint8_t* sfA
 }
 
 qz_status launch_table(bool nv, const Fp4Params& P, cudaStream_t st, bool qout = false) {
-    const void* fn = qout ? (const void*)fp4_gemm_kernel<true, true>
+    const void* fn = qout ? (nv ? (const void*)fp4_gemm_kernel<true, true> : (const void*)fp4_gemm_kernel<false, true>)
                           : nv ? (const void*)fp4_gemm_kernel<true> : (const void*)fp4_gemm_kernel<false>;
     QZ_TRY(opt_in_smem(fn, SMEM_BYTES));
     const int grid = std::min(P.total_tiles, num_sms());
-    if (qout)
+    if (qout && nv)
         fp4_gemm_kernel<true, true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
+    else if (qout)
+        fp4_gemm_kernel<false, true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
     else if (nv)
         fp4_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(P);
     else
@@ -456,7 +488,7 @@ qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const f
 
 qz_status gemm_fp4_launch_q(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
                             const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
-                            const qz_nvfp4_out* yq, int M, int N, int K, void* ws, size_t, cudaStream_t st) {
+                            const qz_fp4_out* yq, int M, int N, int K, void* ws, size_t, cudaStream_t st) {
     uint8_t* wsA = static_cast<uint8_t*>(ws);
     uint8_t* wsB = wsA + round1k(sf_bytes(true, M, K));
     const int ks = K / (nv ? 16 : 32);

@@ -434,41 +434,7 @@ mxfp4_kernel(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx, b
             const float sc = __uint_as_float((uint32_t)(E - 2 + 127) << 23);
             const float inv = __uint_as_float((uint32_t)(127 + 2 - E) << 23);
             if (i < total) {
-                // y = RN(x * 2^(2-E) + 0): the power-of-two scaling, -0 -> +0 except
-                // where a negative product underflows to -0 (the tie rule below
-                // maps that to +0 as well); two lanes per paired fma
-                float y[8];
-#pragma unroll
-                for (int j = 0; j < 8; j += 2)
-                    asm("{ .reg .b64 x2, s2, z2, r2;\n\t"
-                        "mov.b64 x2, {%2, %3}; mov.b64 s2, {%4, %4}; mov.b64 z2, {%5, %5};\n\t"
-                        "fma.rn.f32x2 r2, x2, s2, z2;\n\t"
-                        "mov.b64 {%0, %1}, r2; }"
-                        : "=f"(y[j]), "=f"(y[j + 1]) : "f"(v[u][j]), "f"(v[u][j + 1]), "f"(inv), "f"(0.0f));
-                uint32_t packed;
-                if constexpr (sizeof(T) == 2) {
-                    // bf16 inputs: y = x * 2^(2-E) keeps x's 8 significant bits, so no
-                    // y lies strictly between a midpoint and the fp32 value one ulp
-                    // above it. Stepping every non-zero y one fp32 ulp toward zero
-                    // therefore moves exact midpoints just below themselves (ties go
-                    // down, the pages' rule) and changes no other code; the hardware's
-                    // round-to-nearest-even then gives the exact codes. The step is
-                    // RZ(y * (1 - 2^-24) + 0): the exact product lies less than one ulp
-                    // below |y| (exactly one below a power of two, and for subnormals),
-                    // so rounding toward zero lands on the neighbour toward zero; a
-                    // zero of either sign becomes +0 (an exact -0 + +0 in RZ).
-                    float yd[8];
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2)
-                        asm("{ .reg .b64 y2, c2, z2, r2;\n\t"
-                            "mov.b64 y2, {%2, %3}; mov.b64 c2, {%4, %4}; mov.b64 z2, {%5, %5};\n\t"
-                            "fma.rz.f32x2 r2, y2, c2, z2;\n\t"
-                            "mov.b64 {%0, %1}, r2; }"
-                            : "=f"(yd[j]), "=f"(yd[j + 1]) : "f"(y[j]), "f"(y[j + 1]), "f"(0x1.fffffep-1f), "f"(0.0f));
-                    packed = e2m1x8_rne(yd);
-                } else {
-                    packed = e2m1x8_tiesdown(y);
-                }
+                const uint32_t packed = mxfp4_encode8<sizeof(T) == 2>(v[u], inv);
                 reinterpret_cast<uint32_t*>(codes)[i] = packed;
                 if (deq) {
                     float o[8];

@@ -396,12 +396,25 @@ qz_status qz_gemm_nvfp4_quant(const uint8_t* qA, const uint8_t* sA, const float*
                               const float* y_amax, uint8_t* y_codes, uint8_t* y_scales, float* y_global,
                               int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
     if (!gA || !gB || !y_amax || !y_codes || !y_scales || !y_global) return QZ_ERR_INVALID_ARG;
-    // the bf16 output is not written: Y's checks run on a stand-in aligned pointer
-    QZ_TRY(fp4_gemm_checks(qA, sA, qB, sB, y_codes, M, N, K, ws, ws_bytes));
     if (!is_aligned(y_scales, 8) || !is_aligned(y_amax, 4) || !is_aligned(y_global, 4)) return QZ_ERR_ALIGNMENT;
+    // the bf16 output is not written: Y's checks run on the codes pointer
+    QZ_TRY(fp4_gemm_checks(qA, sA, qB, sB, y_codes, M, N, K, ws, ws_bytes));
     QZ_TRY(device_check());
-    const qz_nvfp4_out yq{y_codes, y_scales, y_amax, y_global};
+    const qz_fp4_out yq{y_codes, y_scales, y_amax, y_global};
     return gemm_fp4_launch_q(true, qA, sA, gA, qB, sB, gB, nullptr, &yq, M, N, K, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+qz_status qz_gemm_mxfp4_quant(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
+                              uint8_t* y_codes, uint8_t* y_e8m0, int M, int N, int K,
+                              void* ws, size_t ws_bytes, void* stream) {
+    if (!y_codes || !y_e8m0) return QZ_ERR_INVALID_ARG;
+    if (!is_aligned(y_e8m0, 4)) return QZ_ERR_ALIGNMENT;
+    // the bf16 output is not written: Y's checks run on the codes pointer
+    QZ_TRY(fp4_gemm_checks(qA, eA, qB, eB, y_codes, M, N, K, ws, ws_bytes));
+    QZ_TRY(device_check());
+    const qz_fp4_out yq{y_codes, y_e8m0, nullptr, nullptr};
+    return gemm_fp4_launch_q(false, qA, eA, nullptr, qB, eB, nullptr, nullptr, &yq, M, N, K, ws, ws_bytes,
+                             (cudaStream_t)stream);
 }
 
 qz_status qz_gemm_mxfp4(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,

@@ -33,19 +33,20 @@ constexpr int kNvfp4MaxProblems = 256;
 qz_status gemm_fp4_launch(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
                           const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
                           int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t st);
-// NVFP4 output of qz_gemm_nvfp4_quant: codes [M, N/2], E4M3 block scales
-// [M, N/16], the tensor scale g computed from the caller's amax.
-struct qz_nvfp4_out {
+// FP4 output of qz_gemm_nvfp4_quant / qz_gemm_mxfp4_quant: codes [M, N/2];
+// scales E4M3 [M, N/16] (NVFP4) or E8M0 [M, N/32] (MXFP4); NVFP4 only: the
+// caller's tensor amax and the tensor scale g computed from it.
+struct qz_fp4_out {
     uint8_t* codes;
     uint8_t* scales;
     const float* amax;
     float* g;
 };
-// As gemm_fp4_launch; with yq (NVFP4 only) the output is quantized instead of
-// written as bf16 (Y unused).
+// As gemm_fp4_launch; with yq the output is quantized, in the GEMM's own
+// format, instead of written as bf16 (Y unused).
 qz_status gemm_fp4_launch_q(bool nv, const uint8_t* qA, const uint8_t* sA, const float* gA,
                             const uint8_t* qB, const uint8_t* sB, const float* gB, uint16_t* Y,
-                            const qz_nvfp4_out* yq, int M, int N, int K, void* ws, size_t ws_bytes,
+                            const qz_fp4_out* yq, int M, int N, int K, void* ws, size_t ws_bytes,
                             cudaStream_t st);
 
 // Device error words of the GEMM translation units (read and cleared by

@@ -208,6 +208,45 @@ __device__ __forceinline__ uint2 nvfp4_block16(const float v[16], float g, const
     return fp4_encode16(v, Recip(sv), nullptr);
 }
 
+// MXFP4: the E2M1 codes of 8 values of one 32-element block whose scale is
+// 2^(E-2), given inv = 2^(2-E) (element j at bit 4j). y = RN(x * 2^(2-E) + 0):
+// the power-of-two scaling, -0 -> +0 except where a negative product underflows
+// to -0 (the tie rule below maps that to +0 as well); two lanes per paired fma.
+// BF16IN (every x has at most 8 significant bits): y keeps x's 8 significant
+// bits, so no y lies strictly between a midpoint and the fp32 value one ulp
+// above it. Stepping every non-zero y one fp32 ulp toward zero therefore moves
+// exact midpoints just below themselves (ties go down, the pages' rule) and
+// changes no other code; the hardware's round-to-nearest-even then gives the
+// exact codes. The step is RZ(y * (1 - 2^-24) + 0): the exact product lies less
+// than one ulp below |y| (exactly one below a power of two, and for
+// subnormals), so rounding toward zero lands on the neighbour toward zero; a
+// zero of either sign becomes +0 (an exact -0 + +0 in RZ). Other inputs take
+// the ties-down encoder.
+template <bool BF16IN>
+__device__ __forceinline__ uint32_t mxfp4_encode8(const float v[8], float inv) {
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2)
+        asm("{ .reg .b64 x2, s2, z2, r2;\n\t"
+            "mov.b64 x2, {%2, %3}; mov.b64 s2, {%4, %4}; mov.b64 z2, {%5, %5};\n\t"
+            "fma.rn.f32x2 r2, x2, s2, z2;\n\t"
+            "mov.b64 {%0, %1}, r2; }"
+            : "=f"(y[j]), "=f"(y[j + 1]) : "f"(v[j]), "f"(v[j + 1]), "f"(inv), "f"(0.0f));
+    if constexpr (BF16IN) {
+        float yd[8];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2)
+            asm("{ .reg .b64 y2, c2, z2, r2;\n\t"
+                "mov.b64 y2, {%2, %3}; mov.b64 c2, {%4, %4}; mov.b64 z2, {%5, %5};\n\t"
+                "fma.rz.f32x2 r2, y2, c2, z2;\n\t"
+                "mov.b64 {%0, %1}, r2; }"
+                : "=f"(yd[j]), "=f"(yd[j + 1]) : "f"(y[j]), "f"(y[j + 1]), "f"(0x1.fffffep-1f), "f"(0.0f));
+        return e2m1x8_rne(yd);
+    } else {
+        return e2m1x8_tiesdown(y);
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v, int width) {
     for (int o = width / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;

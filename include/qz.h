@@ -459,6 +459,18 @@ qz_status qz_gemm_nvfp4_quant(const uint8_t* qA, const uint8_t* sA, const float*
                               const float* y_amax, uint8_t* y_codes, uint8_t* y_scales, float* y_global,
                               int M, int N, int K, void* ws, size_t ws_bytes, void* stream);
 
+/* MXFP4 GEMM whose epilogue quantizes its output to MXFP4 for the next layer
+ * (as qz_gemm_nvfp4_quant; 格式速查: MXFP4, E2M1 + an E8M0 scale per 32). The
+ * same arithmetic as qz_gemm_mxfp4 up to the bf16 output y, then encoded
+ * exactly as qz_quantize_mxfp4(y) would: per 32 columns,
+ * scale = 2^(floor(log2 max(amax32, 1e-12)) - 2), codes = E2M1(y / scale).
+ * No tensor amax is needed. y_codes: [M, N/2] bytes (16 B aligned); y_e8m0:
+ * [M, N/32] (4 B aligned). No bf16 output is written. Other shapes, layouts,
+ * workspace and alignment as qz_gemm_mxfp4. */
+qz_status qz_gemm_mxfp4_quant(const uint8_t* qA, const uint8_t* eA, const uint8_t* qB, const uint8_t* eB,
+                              uint8_t* y_codes, uint8_t* y_e8m0, int M, int N, int K,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* NVFP4 GEMM that allocates nothing and takes no workspace. (The quantization
  * pages have no counterpart: this is an interface convenience of this library.)
  * Some callers cannot call cudaMalloc or hand this library a workspace: runtimes

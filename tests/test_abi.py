@@ -127,6 +127,12 @@ def test_gemm_validation(qz):
     assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 200, 256, NULL, 0, NULL) == 2  # N
     assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ODD, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 3   # codes
     assert q(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 7  # ws
+    # qA, eA, qB, eB, y_codes, y_e8m0, M, N, K, ws, ws_bytes, stream
+    mq = L.qz_gemm_mxfp4_quant
+    assert mq(FAKE, FAKE, FAKE, FAKE, NULL, FAKE, 128, 256, 256, NULL, 0, NULL) == 1
+    assert mq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 100, NULL, 0, NULL) == 2                 # K
+    assert mq(FAKE, FAKE, FAKE, FAKE, FAKE, ODD, 128, 256, 256, NULL, 0, NULL) == 3                  # e8m0
+    assert mq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 256, 256, NULL, 0, NULL) == 7                 # ws
 
 
 def test_grouped_nvfp4_and_prepare_validation(qz):

@@ -272,3 +272,42 @@ def test_nvfp4_gemm_quantized_output_matches_gemm_then_quantizer(qz, M, N, K):
     assert np.array_equal(host(scales), host(s2)), "block scales differ from GEMM then quantizer"
     assert np.array_equal(host(g), host(g2)), "tensor scale differs"
     assert qz.qz_device_error() == 0
+
+
+# ---------------------------------------- MXFP4 GEMM with MXFP4 output
+
+def test_mxfp4_gemm_quantized_output_exact_case(qz):
+    """Unit scales and E2M1 codes of small integers make every sum exact: codes and E8M0
+    scales bit-exact against the oracle's MXFP4 quantizer of the exact product rounded
+    once to bf16."""
+    rng = np.random.default_rng(37)
+    M, N, K = 256, 512, 256
+    mag = np.array([0, 2, 4, 5, 6, 7])                    # 0, 1, 2, 3, 4, 6
+    ca = (rng.choice(mag, (M, K)) | (rng.integers(0, 2, (M, K)) << 3)).astype(np.uint8)
+    cb = (rng.choice(mag, (N, K)) | (rng.integers(0, 2, (N, K)) << 3)).astype(np.uint8)
+    va = np.vectorize(oracle.e2m1_decode)(ca)
+    vb = np.vectorize(oracle.e2m1_decode)(cb)
+    ybf = syn.to_bf16_bits((va @ vb.T).astype(np.float32))
+    codes, e8 = qz.qz_gemm_mxfp4_quant(dev(pack(ca)), dev(np.full((M, K // 32), 127, np.uint8)),
+                                       dev(pack(cb)), dev(np.full((N, K // 32), 127, np.uint8)))
+    rc, re8, _ = oracle.quant_mxfp4(ybf, want_deq=False)
+    assert_same_bytes(host(codes), rc, "codes")
+    assert_same_bytes(host(e8), re8, "E8M0 scales")
+    assert qz.qz_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (384, 768, 512), (1152, 1024, 768), (8192, 4096, 4096)])
+def test_mxfp4_gemm_quantized_output_matches_gemm_then_quantizer(qz, M, N, K):
+    """Realistic operands over one tile, several tiles, more tiles than SMs, and the
+    prefill shape: the fused codes and E8M0 scales equal qz_quantize_mxfp4 applied to
+    the plain MXFP4 GEMM's bf16 output, bit for bit."""
+    a, bt = inputs(M, N, K, seed=M + N + 1)
+    ca, ea, _ = oracle.quant_mxfp4(a, want_deq=False)
+    cb, eb, _ = oracle.quant_mxfp4(bt, want_deq=False)
+    ops = (dev(ca), dev(ea), dev(cb), dev(eb))
+    y = qz.qz_gemm_mxfp4(*ops)
+    codes, e8 = qz.qz_gemm_mxfp4_quant(*ops)
+    c2, e2, _ = qz.qz_quantize_mxfp4(y)
+    assert np.array_equal(host(codes), host(c2)), "codes differ from GEMM then quantizer"
+    assert np.array_equal(host(e8), host(e2)), "E8M0 scales differ from GEMM then quantizer"
+    assert qz.qz_device_error() == 0
