@@ -311,3 +311,41 @@ def test_mxfp4_gemm_quantized_output_matches_gemm_then_quantizer(qz, M, N, K):
     assert np.array_equal(host(codes), host(c2)), "codes differ from GEMM then quantizer"
     assert np.array_equal(host(e8), host(e2)), "E8M0 scales differ from GEMM then quantizer"
     assert qz.qz_device_error() == 0
+
+
+@pytest.mark.parametrize("fmt", ["nv", "mx"])
+def test_fused_output_feeds_the_next_layer(qz, fmt):
+    """Two layers in a row: layer 1's fused FP4 output (codes, block scales and, for
+    NVFP4, the tensor scale) is layer 2's A operand as written, with no bf16 tensor in
+    between. Layer 1's codes equal the oracle quantizer of its bf16 output, and layer 2's
+    output is within the GEMM bound of the oracle's GEMM on those codes."""
+    M, K1, N1, N2 = 256, 512, 768, 512
+    a, w1t = inputs(M, N1, K1, seed=41)
+    _, w2t = inputs(M, N2, N1, seed=42)
+    if fmt == "nv":
+        ca, sa, ga, _ = oracle.quant_nvfp4(a, want_deq=False)
+        c1, s1, g1, _ = oracle.quant_nvfp4(w1t, want_deq=False)
+        c2, s2, g2, _ = oracle.quant_nvfp4(w2t, want_deq=False)
+        l1 = (dev(ca), dev(sa), dev(np.float32([ga])), dev(c1), dev(s1), dev(np.float32([g1])))
+        y1 = qz.qz_gemm_nvfp4(*l1)                              # layer 1's bf16 output, for its amax
+        amax = float(torch.max(torch.abs(y1.float())))
+        yc, ys, yg = qz.qz_gemm_nvfp4_quant(*l1, dev(np.float32([amax])))
+        y2 = qz.qz_gemm_nvfp4(yc, ys, yg, dev(c2), dev(s2), dev(np.float32([g2])))
+        rc, rs, rg, _ = oracle.quant_nvfp4(host(y1), amax_in=np.float32(amax), want_deq=False)
+        assert_same_bytes(host(yc), rc, "layer-1 codes")
+        assert_same_bytes(host(ys), rs, "layer-1 block scales")
+        y_ref, bound = oracle.gemm_nvfp4(rc, rs, float(np.asarray(rg).ravel()[0]), c2, s2, g2)
+    else:
+        ca, ea, _ = oracle.quant_mxfp4(a, want_deq=False)
+        c1, e1, _ = oracle.quant_mxfp4(w1t, want_deq=False)
+        c2, e2, _ = oracle.quant_mxfp4(w2t, want_deq=False)
+        l1 = (dev(ca), dev(ea), dev(c1), dev(e1))
+        y1 = qz.qz_gemm_mxfp4(*l1)
+        yc, ye = qz.qz_gemm_mxfp4_quant(*l1)
+        y2 = qz.qz_gemm_mxfp4(yc, ye, dev(c2), dev(e2))
+        rc, re8, _ = oracle.quant_mxfp4(host(y1), want_deq=False)
+        assert_same_bytes(host(yc), rc, "layer-1 codes")
+        assert_same_bytes(host(ye), re8, "layer-1 E8M0 scales")
+        y_ref, bound = oracle.gemm_mxfp4(rc, re8, c2, e2)
+    check(host(y2), y_ref, bound, f"{fmt} layer 2 on layer 1's fused output")
+    assert qz.qz_device_error() == 0
