@@ -131,6 +131,7 @@ std::vector<StreamInt4> g_int4;         // one entry per device and stream an IN
 uint64_t g_int4_gen;
 
 StreamInt4* find_int4(int dev, cudaStream_t st) {
+    if (st == cudaStreamLegacy) st = nullptr;   // two handles of the legacy default stream, one key
     for (StreamInt4& e : g_int4)
         if (e.dev == dev && e.st == st) return &e;
     return nullptr;
@@ -142,7 +143,7 @@ void note_int4_writes(cudaStream_t st, const Span* w, int n) {
     std::lock_guard<std::mutex> lk(g_int4_mu);
     StreamInt4* e = find_int4(dev, st);
     if (!e) {
-        g_int4.push_back(StreamInt4{dev, st, {}});
+        g_int4.push_back(StreamInt4{dev, st == cudaStreamLegacy ? nullptr : st, {}});
         e = &g_int4.back();
     }
     e->w.gen = ++g_int4_gen;
