@@ -685,7 +685,7 @@ int stream_grid(int64_t threads_needed, int per_sm = 4) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm));
 }
 constexpr int kEncoderCtasPerSm = 16;
-constexpr int kNvfp4CtasPerSm = 8;       // the NVFP4 encoder's CTAs also build a scale table
+constexpr int kNvfp4CtasPerSm = 4;       // the NVFP4 encoder's CTAs also build a scale table (8192 x 4096 bf16: 4 per SM 27.2 us, 6 27.3, 8 27.5, 16 28.2)
 
 bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
     const size_t es = t == QZ_F32 ? 4 : 2;
