@@ -684,7 +684,8 @@ int stream_grid(int64_t threads_needed, int per_sm = 4) {
     const int64_t ctas = (threads_needed + kThreads - 1) / kThreads;
     return (int)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)num_sms() * per_sm));
 }
-constexpr int kEncoderCtasPerSm = 16;
+constexpr int kEncoderCtasPerSm = 16;     // FP8 1x128 (2048 x 4096 bf16: 16 per SM 7.55 us, 8 8.29, 32 8.61)
+constexpr int kMxfp4CtasPerSm = 8;        // MXFP4 (8192 x 4096 bf16: 8 per SM 16.77 us, 16 16.91, 32 17.41)
 constexpr int kNvfp4CtasPerSm = 4;       // the NVFP4 encoder's CTAs also build a scale table (8192 x 4096 bf16: 4 per SM 27.2 us, 6 27.3, 8 27.5, 16 28.2)
 
 bool vec_ok(const void* x, int64_t ldx, int64_t cols, qz_dtype t) {
@@ -763,7 +764,7 @@ qz_status quantize_fp8_launch(const void* x, qz_dtype xt, int64_t rows, int64_t 
 qz_status quantize_mxfp4_launch(const void* x, qz_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
                                 uint8_t* codes, uint8_t* e8m0, float* deq, cudaStream_t st) {
     const bool contig = (ldx == cols);
-    const int grid = stream_grid(rows * cols / 8, kEncoderCtasPerSm);
+    const int grid = stream_grid(rows * cols / 8, kMxfp4CtasPerSm);
     if (xt == QZ_F32)
         mxfp4_kernel<float><<<grid, kThreads, 0, st>>>((const float*)x, rows, cols, ldx, contig, codes, e8m0, deq);
     else
